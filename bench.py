@@ -1,0 +1,423 @@
+"""Benchmark of the multi-LoRA decode hot path on GB300.
+
+One step = one pass of the whole path over the decode batches of the
+Llama-3-8B q/k/v workload (H=4096, q/k/v slices 4096/1024/1024, rank 16,
+4 adapters, bf16, 10 % of tokens without an adapter; one batch each of
+T = 16, 128, 256, 512, 1024 tokens): for every batch, BGMV grouping of the
+token indices, the stacked q/k/v shrink into the fp32 rank buffer, and the
+three-slice expand_slice into the fused q/k/v output (add_inputs, as vLLM
+PR #11579 benchmarks the expand).
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores on the same workload instead (bounded samples per step).
+Multi-GPU (torchrun): every rank runs its own batches, no collective on the
+data path (weak scaling); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import lora_inputs as li  # noqa: E402
+
+METRIC = "LoRA shrink+expand tokens/s and achieved % of HBM/tensor roofline (1×GB300)"
+WORKLOAD = ("decode BGMV, Llama-3-8B q/k/v: H=4096, expand_slice into q/k/v slices "
+            "4096/1024/1024, r=16, L=4 adapters, bf16, T in {16,128,256,512,1024} "
+            "(one batch of each per step), idx uniform over adapters, 10% idx=-1, "
+            "weights N(0,0.02), add_inputs=True")
+H, R, L, SLICES = 4096, 16, 4, li.QKV_SLICES
+NTOT = sum(SLICES)
+E = 2  # bytes per bf16 element
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------- work model
+
+def algorithmic(idx: torch.Tensor):
+    """Algorithmic bytes / flops of one batch (what the method must move).
+
+    shrink: x rows of active tokens + live A rows of used adapters + y written
+    expand_slice: y rows read + live B rows of used adapters + out read and
+                  written for active tokens (add_inputs)."""
+    T = idx.numel()
+    act = idx >= 0
+    Ta = int(act.sum())
+    U = int(torch.unique(idx[act]).numel())
+    S = len(SLICES)
+    sh_bytes = Ta * H * E + U * S * R * H * E + T * S * R * 4
+    sh_flops = 2 * H * S * R * Ta
+    ex_bytes = Ta * S * R * 4 + U * NTOT * R * E + 2 * Ta * NTOT * E
+    ex_flops = 2 * NTOT * R * Ta
+    return sh_bytes, sh_flops, ex_bytes, ex_flops
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=5)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def make_pool(dev, rank: int, l2_bytes: int):
+    """Rotating argument pool: sets of (inputs, adapters, outputs) for every
+    batch size, enough sets that the pool is >= 4x L2, so each step reads
+    data no earlier step left in L2."""
+    import lora_gemv_gb300 as lg
+    per_set = 0
+    for T in li.DECODE_T:
+        per_set += T * (H * E + NTOT * E + len(SLICES) * R * 4 + 4) + L * (len(SLICES) * R * H
+                                                                            + NTOT * R) * E
+    nsets = max(2, -(-4 * l2_bytes // per_set))
+    pool = []
+    for s in range(nsets):
+        batches = []
+        for T in li.DECODE_T:
+            c = li.decode_qkv(T, seed=li.SEED_BASE + 2 + 1000 * rank + 17 * s + T)
+            batches.append({
+                "T": T, "case": c,
+                "x": c.x.to(dev), "A": c.A.to(dev), "B": [b.to(dev) for b in c.B],
+                "out": c.out.to(dev), "idx": c.token_idx.to(dev),
+                "y": torch.empty(T, len(SLICES) * R, dtype=torch.float32, device=dev),
+                "plan": lg.new_plan(T, L, dev),
+            })
+        pool.append(batches)
+    return pool, nsets * per_set
+
+
+def run_step(lg, batches, ev=None):
+    for i, b in enumerate(batches):
+        lg.lora_group_tokens(b["idx"], L, b["plan"])
+        lg.lora_shrink(b["x"], b["A"], b["y"], b["plan"], num_slices=len(SLICES))
+        if ev is not None:
+            ev[i][0].record()
+        lg.lora_expand_slice(b["y"], b["B"], b["out"], b["plan"], b["case"].slice_offsets,
+                             y_slice_stride=R, add_inputs=True)
+        if ev is not None:
+            ev[i][1].record()
+
+
+def e2e_run(lg, dev, steps: int, warmup: int):
+    """Through the public API with host buffers: every step copies the batch's
+    x, token indices and base output from pinned host memory, runs the path
+    and copies the updated output back."""
+    host, devb = [], []
+    for T in li.DECODE_T:
+        c = li.decode_qkv(T, seed=li.SEED_BASE + 2 + 5 * T)
+        host.append({"x": c.x.pin_memory(), "idx": c.token_idx.pin_memory(),
+                     "out": c.out.pin_memory(), "res": torch.empty_like(c.out).pin_memory()})
+        devb.append({"T": T, "case": c, "A": c.A.to(dev), "B": [b.to(dev) for b in c.B],
+                     "x": torch.empty_like(c.x, device=dev),
+                     "idx": torch.empty_like(c.token_idx, device=dev),
+                     "out": torch.empty_like(c.out, device=dev),
+                     "y": torch.empty(T, len(SLICES) * R, dtype=torch.float32, device=dev),
+                     "plan": lg.new_plan(T, L, dev)})
+    h2d = sum(h["x"].numel() * 2 + h["idx"].numel() * 4 + h["out"].numel() * 2 for h in host)
+    d2h = sum(h["out"].numel() * 2 for h in host)
+
+    def step():
+        for h, d in zip(host, devb):
+            d["x"].copy_(h["x"], non_blocking=True)
+            d["idx"].copy_(h["idx"], non_blocking=True)
+            d["out"].copy_(h["out"], non_blocking=True)
+        run_step(lg, devb)
+        for h, d in zip(host, devb):
+            h["res"].copy_(d["out"], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - w0
+    ms = t0.elapsed_time(t1)
+    tokens = steps * sum(li.DECODE_T)
+    return tokens / (ms / 1e3), h2d, d2h, tokens / wall
+
+
+def cpu_baseline(target_s: float = 10.0):
+    """The oracle, as it stands, on the same decode batches on the host cores."""
+    import oracle
+    import numpy as np
+    prepared = []
+    for T in li.DECODE_T:
+        c = li.decode_qkv(T)
+        prepared.append((T, c.token_idx.numpy(), c.x.double().numpy(), c.A.double().numpy(),
+                         [b.double().numpy() for b in c.B], c.out.double().numpy(),
+                         c.slice_offsets))
+    tokens, reps = 0, 0
+    t0 = time.perf_counter()
+    while True:
+        for T, idx, x, A, Bs, out, offs in prepared:
+            lo, _ = oracle.map_tokens(idx, L)
+            y = oracle.shrink(x, A, lo, num_slices=len(SLICES))
+            oracle.expand_slice(y, Bs, offs, lo, out, y_stride=R, add=True)
+            tokens += T
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= target_s:
+            break
+    del np
+    return {"value": tokens / el, "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{reps} full steps ({tokens} tokens of the same five decode batches), "
+                      f"fp64 C loops, OpenMP over tokens, {el:.1f} s"}
+
+
+def main_ours(args):
+    import torch.distributed as dist
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import lora_gemv_gb300 as lg
+    lg.load()
+    props = torch.cuda.get_device_properties(dev)
+    pool, pool_bytes = make_pool(dev, rank, props.L2_cache_size)
+    nsets = len(pool)
+    K, W = args.steps, args.warmup
+
+    for w in range(W):
+        run_step(lg, pool[w % nsets])
+    torch.cuda.synchronize()
+
+    nb = len(li.DECODE_T)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nb)]
+          for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    clocks.start()
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    start.record()
+    for k in range(K):
+        run_step(lg, pool[(W + k) % nsets], ev[k])
+    end.record()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+
+    ms = start.elapsed_time(end)
+    ex_ms = [sum(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)) for i in range(nb)]
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    tokens_rank = K * sum(li.DECODE_T)
+    value = tokens_rank * ws / (ms / 1e3)
+
+    # algorithmic work of the step (same for every pool set up to the random ids)
+    per_T = {}
+    ex_bytes_tot = sh_bytes_tot = 0
+    ex_time_tot = 0.0
+    for i, T in enumerate(li.DECODE_T):
+        sb, sf, eb, ef = algorithmic(pool[0][i]["case"].token_idx)
+        ex_bytes_tot += eb * K
+        sh_bytes_tot += sb * K
+        ex_time_tot += ex_ms[i] / 1e3
+        per_T[str(T)] = {"expand_us": ex_ms[i] / K * 1e3,
+                         "expand_GBps": eb / (ex_ms[i] / K / 1e3) / 1e9,
+                         "expand_bytes": eb, "shrink_bytes": sb}
+    hbm, tf, src = peaks()
+    achieved = ex_bytes_tot / ex_time_tot / 1e9
+    path_bytes = (ex_bytes_tot + sh_bytes_tot) / K
+    path_frac = (path_bytes / (hbm * 1e9)) / (ms / 1e3 / K)
+
+    e2e_v, h2d, d2h, e2e_wall = e2e_run(lg, dev, max(10, K // 10), 3)
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": W, "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, shapes of the workload)",
+        "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": sum(li.DECODE_T),
+                   "parallelism": f"replicas x{ws} (independent batches, no collective)",
+                   "l2": f"rotating argument pool of {nsets} sets ({pool_bytes / 1e6:.0f} MB "
+                         f">= 4x L2 {props.L2_cache_size / 1e6:.0f} MB): inputs larger than L2"},
+        "roofline": {"kernel": "expand_slice", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": f"{src} hbm_gbs", "traffic": None},
+        "path_roofline_frac": path_frac,
+        "gpu_launches": K * nb * 3,
+        "e2e": {"value": e2e_v, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "wall_tokens_per_s": e2e_wall},
+        "clocks": clk,
+        "per_T": per_T,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    prepared = []
+    for T in li.DECODE_T:
+        c = li.decode_qkv(T)
+        prepared.append((T, c.token_idx.numpy(), c.x.double().numpy(), c.A.double().numpy(),
+                         [b.double().numpy() for b in c.B], c.out.double().numpy(),
+                         c.slice_offsets))
+    # Bounded sample per step: a slice of each batch's tokens, sized so the
+    # whole run stays within about two minutes.
+    budget = float(args.ref_budget_s)
+    t0 = time.perf_counter()
+    _ref_step(oracle, prepared, None)
+    full = time.perf_counter() - t0
+    frac = min(1.0, budget / max(1e-6, full * (args.steps + args.warmup)))
+    rows = {T: max(1, int(round(T * frac))) for T in li.DECODE_T}
+    for _ in range(args.warmup):
+        _ref_step(oracle, prepared, rows)
+    t0 = time.perf_counter()
+    tokens = 0
+    for _ in range(args.steps):
+        tokens += _ref_step(oracle, prepared, rows)
+    el = time.perf_counter() - t0
+    v = tokens / el
+    res = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded, shapes of the workload)",
+           "config": {"workload": WORKLOAD, "tokens_per_step_sampled": sum(rows.values())},
+           "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(),
+                            "kind": "oracle",
+                            "sample": f"first {rows} tokens of each decode batch per step"},
+           "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def _ref_step(oracle, prepared, rows):
+    n = 0
+    for T, idx, x, A, Bs, out, offs in prepared:
+        k = T if rows is None else rows[T]
+        lo, _ = oracle.map_tokens(idx[:k], L)
+        y = oracle.shrink(x[:k], A, lo, num_slices=len(SLICES))
+        oracle.expand_slice(y, Bs, offs, lo, out[:k], y_stride=R, add=True)
+        n += k
+    return n
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-budget-s", type=float, default=90.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        main_reference(args)
+    else:
+        main_ours(args)
+
+
+if __name__ == "__main__":
+    main()

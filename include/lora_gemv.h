@@ -1,0 +1,245 @@
+/*
+ * lora_gemv.h - C ABI of the GB300 (sm_103a) multi-LoRA shrink / expand library.
+ *
+ * The operators are the Punica-style multi-LoRA pair named on these pages:
+ *  - vLLM PR #15655 "[Hardware][TPU][V1] Multi-LoRA Optimisations for the V1
+ *    TPU backend", summary list: the LoRA kernel is split into a shrink and
+ *    an expand variant, with block skipping and fast mask creation;
+ *  - vLLM PR #11579 "[misc] Add LoRA kernel micro benchmarks": the operators
+ *    bgmv_shrink, bgmv_expand, bgmv_expand_slice, sgmv_shrink, sgmv_expand,
+ *    sgmv_expand_slice; the add_inputs flag of expand ("group-gemm + outputs");
+ *    the fp32 intermediate between shrink and expand ("f32xf16=>f16"); the
+ *    num_slices of a fused output; split-K shrink that adds partials;
+ *  - Punica issue #17 "The smallest rank supported is 16?": BGMV (one adapter
+ *    per input) versus SGMV (segments of inputs sharing one adapter, the
+ *    "AAABCC" batch), BGMV semantics being a subset of SGMV's, and ranks
+ *    padded up to a common size as the old workaround.
+ *
+ * Definitions (T tokens, H hidden size, L stacked adapters, R rows per slice
+ * = the largest rank, r_l = rank of adapter l <= R, l = adapter of token t,
+ * l = -1 meaning "no LoRA"):
+ *   shrink : y[t, s*R + i] = (add ? y[t, s*R+i] : 0) + scale * sum_h x[t,h] * A[l, s*R+i, h]
+ *            for i < r_l; the term is 0 for i >= r_l and for l = -1.
+ *   expand : out[t, off_s + n] = (add ? out[t, off_s+n] : 0)
+ *                               + scale * sum_{i<r_l} y[t, s*ys + i] * B_s[l, n, i]
+ *            for l >= 0; for l = -1 the row is left untouched (add) or set to 0.
+ *   BGMV and SGMV differ only in how the token -> adapter map is given; both
+ *   are turned into one "plan" (token grouping) that every operator reads.
+ *
+ * Conventions
+ *  - Every pointer argument named x, A, B*, y, out, plan, token_idx, seg_*,
+ *    ranks is a DEVICE pointer on the current CUDA device; host arrays are
+ *    marked "host".  The caller owns all memory.  The library allocates no
+ *    device or host memory, keeps no per-call state and never synchronises
+ *    inside an operator: each operator only enqueues kernels on `stream`,
+ *    so the calls may be captured in a CUDA graph.
+ *  - Matrices are row-major with an explicit leading dimension (in elements).
+ *  - fp16 / bf16 elements are IEEE binary16 / bfloat16; y is fp32.
+ *  - Arithmetic: products of fp16/bf16 values accumulated in fp32 on tensor
+ *    cores; expand feeds y to the tensor cores as a hi+lo pair of the weight
+ *    type scaled per token row by a power of two, so y keeps ~fp32 accuracy;
+ *    the result is rounded once (round-to-nearest-even) to the output type.
+ *    Summation order is not specified: results agree with an exact sum to
+ *    fp32-accumulation accuracy, not bit-for-bit across launch shapes.
+ *  - Errors: argument errors are detected on the host, before anything is
+ *    enqueued, and returned synchronously; nothing is launched then.  A
+ *    failed launch returns LORA_ERR_CUDA.  Conditions only visible on the
+ *    device (bad adapter ids, a malformed segment table, a plan that does not
+ *    match the operator's T / L) are recorded in the plan's error words and
+ *    read back with lora_get_error(); the kernels never trap or spin.
+ *  - Thread safety: all functions are re-entrant.  The first call on a
+ *    device configures kernel attributes once (guarded); make that first
+ *    call outside stream capture.
+ */
+#ifndef LORA_GEMV_H
+#define LORA_GEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the CUDA runtime's stream handle); NULL = legacy default stream. */
+typedef struct CUstream_st *lora_stream_t;
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_ERR_INVALID_ARG = 1, /* a size, stride, pointer or flag is out of its documented range */
+    LORA_ERR_UNSUPPORTED = 2, /* valid but outside this build's limits (e.g. L > LORA_MAX_ADAPTERS) */
+    LORA_ERR_WORKSPACE = 3,   /* plan buffer too small or misaligned */
+    LORA_ERR_CUDA = 4         /* the CUDA runtime reported an error (launch, attribute, device query) */
+} lora_status_t;
+
+typedef enum { LORA_F16 = 0, LORA_BF16 = 1 } lora_dtype_t;
+
+#define LORA_TILE_TOKENS 64      /* tokens per work tile of the plan */
+#define LORA_MAX_RANK 128        /* largest R (rows per slice / max adapter rank) */
+#define LORA_MAX_SLICES 8        /* largest num_slices of shrink / expand_slice */
+#define LORA_MAX_ADAPTERS 1024   /* largest L accepted by lora_group_tokens */
+#define LORA_MAX_TOKENS (1 << 24)
+
+/* Plan header words (int32, at byte offset 0 of the plan). */
+enum {
+    LORA_HDR_MAGIC = 0,    /* LORA_PLAN_MAGIC once a grouping call has run */
+    LORA_HDR_T = 1,
+    LORA_HDR_L = 2,
+    LORA_HDR_KIND = 3,     /* 1 = built from token indices (BGMV), 2 = from segments (SGMV) */
+    LORA_HDR_NACTIVE = 4,  /* tokens with an adapter */
+    LORA_HDR_NGROUPS = 5,
+    LORA_HDR_NTILES = 6,
+    LORA_HDR_BAD_IDS = 7,  /* adapter ids outside [-1, L): treated as -1 */
+    LORA_HDR_ERR = 8,      /* LORA_PLANERR_* bits, OR-ed by grouping and by operators */
+    LORA_HDR_WORDS = 16
+};
+#define LORA_PLAN_MAGIC 0x4C6F5241
+#define LORA_PLANERR_SEG_RANGE 1    /* a segment had start < 0, len < 0 or start+len > T: ignored */
+#define LORA_PLANERR_SEG_ORDER 2    /* a segment began before the end of an earlier one: ignored */
+#define LORA_PLANERR_MISMATCH 4     /* an operator got a plan built for another T or L: it wrote nothing */
+
+/*
+ * Plan layout: byte offsets of each array inside the caller's plan buffer.
+ * The layout depends only on (T, L).
+ *   count[L]          tokens per adapter
+ *   offset[L+1]       exclusive prefix sum of count (BGMV: where adapter l's
+ *                     tokens start in perm)
+ *   perm[T]           token order: perm[0:n_active] = tokens with an adapter,
+ *                     grouped (BGMV: ascending adapter id, ties by token index;
+ *                     SGMV: ascending token index), then the tokens without
+ *                     an adapter in ascending order
+ *   group_lora/start/count[T+1]  maximal runs of one adapter along
+ *                     perm[0:n_active]: adapter id, first perm position, length
+ *   tiles[max_tiles][4]  each group cut into pieces of <= LORA_TILE_TOKENS
+ *                     tokens, then the inactive tokens likewise:
+ *                     {adapter (-1 for inactive), first perm position,
+ *                      token count, group number (-1 for inactive)}
+ */
+typedef struct {
+    int64_t header, count, offset, perm, group_lora, group_start, group_count, tiles;
+    int64_t max_tiles;
+    int64_t bytes; /* total size of the buffer */
+} lora_plan_layout_t;
+
+/* Fills *layout for a plan of T tokens and L adapters.
+ * Errors: LORA_ERR_INVALID_ARG (T < 0, L < 1, layout NULL), LORA_ERR_UNSUPPORTED
+ * (T > LORA_MAX_TOKENS). */
+lora_status_t lora_plan_layout(int32_t T, int32_t L, lora_plan_layout_t *layout);
+
+/* Size in bytes of the plan buffer for (T, L); 0 on invalid arguments.  The
+ * buffer must be 16-byte aligned device memory. */
+size_t lora_workspace_size(int32_t T, int32_t L);
+
+/*
+ * BGMV grouping (Punica issue #17, "each input is for a different model";
+ * vLLM PR #15655 "faster mask creation"): builds the plan from a per-token
+ * adapter index token_idx[T] (device, int32; -1 = no LoRA; other values
+ * outside [0, L) are counted in LORA_HDR_BAD_IDS and treated as -1).
+ * One single-block kernel on `stream`; the grouping is a stable counting sort.
+ * Errors: LORA_ERR_INVALID_ARG (NULL pointers with T > 0, T < 0, L < 1),
+ * LORA_ERR_UNSUPPORTED (L > LORA_MAX_ADAPTERS, T > LORA_MAX_TOKENS),
+ * LORA_ERR_WORKSPACE (plan_bytes < lora_workspace_size(T, L) or plan not
+ * 16-byte aligned), LORA_ERR_CUDA.
+ */
+lora_status_t lora_group_tokens(const int32_t *token_idx, int32_t T, int32_t L,
+                                void *plan, size_t plan_bytes, lora_stream_t stream);
+
+/*
+ * SGMV grouping (Punica issue #17: inputs grouped into segments sharing an
+ * adapter; vLLM PR #11579's seq-len / sort-by-lora-id): builds the plan from
+ * a segment table of num_segs entries (device, int32 each):
+ * segment i covers tokens [seg_start[i], seg_start[i] + seg_len[i]) with
+ * adapter seg_lora[i].  Tokens covered by no segment, and segments with
+ * adapter -1, get no LoRA.  A segment with start < 0, len < 0 or
+ * start + len > T is ignored (LORA_PLANERR_SEG_RANGE); a non-empty segment
+ * that starts before the end of an earlier non-empty in-range segment is
+ * ignored (LORA_PLANERR_SEG_ORDER); adapter ids outside [-1, L) count as bad
+ * ids and act as -1.  Adjacent runs of one adapter are coalesced into one
+ * group.  One single-block kernel on `stream`.
+ * Errors: as lora_group_tokens (num_segs < 0 is LORA_ERR_INVALID_ARG).
+ */
+lora_status_t lora_group_segments(const int32_t *seg_start, const int32_t *seg_len,
+                                  const int32_t *seg_lora, int32_t num_segs, int32_t T,
+                                  int32_t L, void *plan, size_t plan_bytes,
+                                  lora_stream_t stream);
+
+/*
+ * Shrink (bgmv_shrink / sgmv_shrink; vLLM PR #11579, split-K shrink note):
+ *   x    [T, ldx]       activations, dtype `dtype` (ldx >= H)
+ *   A    [L, S*R, H]    stacked adapters, contiguous; S = num_slices slices
+ *                       (q/k/v or gate/up) of R rows each; rows i >= r_l of a
+ *                       slice are never read
+ *   ranks [L] or NULL   per-adapter rank r_l (device int32, clamped to [0, R]);
+ *                       NULL means every adapter has rank R
+ *   y    [T, ldy] fp32  output (ldy >= S*R); every column j < S*R of every
+ *                       row is written (add = 0) or accumulated (add != 0);
+ *                       columns >= S*R are not touched
+ *   plan                from lora_group_tokens / lora_group_segments with
+ *                       the same T and L
+ * Limits: 1 <= R <= LORA_MAX_RANK, 1 <= num_slices <= LORA_MAX_SLICES,
+ * H >= 1.  T == 0 launches nothing.
+ * Errors: LORA_ERR_INVALID_ARG (NULL pointers, bad sizes or strides, bad
+ * dtype), LORA_ERR_UNSUPPORTED, LORA_ERR_CUDA.
+ */
+lora_status_t lora_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_t T, int32_t H,
+                          const void *A, int32_t L, int32_t R, int32_t num_slices,
+                          const int32_t *ranks, float *y, int64_t ldy, const void *plan,
+                          float scale, int add_inputs, lora_stream_t stream);
+
+/*
+ * Expand (bgmv_expand / sgmv_expand; add_inputs as in vLLM PR #11579):
+ *   y    [T, ldy] fp32  the shrink output, columns [0, R) read (r_l of them)
+ *   B    [L, N, R]      adapters, contiguous; column i >= r_l never read
+ *   out  [T, ldo]       dtype `dtype`; columns [0, N) of active tokens are
+ *                       updated; rows of tokens without an adapter are left
+ *                       untouched (add != 0) or zeroed (add == 0)
+ * Equivalent to lora_expand_slice with one slice at offset 0.
+ * Errors: as lora_expand_slice.
+ */
+lora_status_t lora_expand(lora_dtype_t dtype, const float *y, int64_t ldy, int32_t T,
+                          const void *B, int32_t L, int32_t N, int32_t R, const int32_t *ranks,
+                          void *out, int64_t ldo, const void *plan, float scale, int add_inputs,
+                          lora_stream_t stream);
+
+/*
+ * Expand into column slices of a fused output (bgmv_expand_slice /
+ * sgmv_expand_slice; vLLM PR #11579 num_slices), all slices in one launch:
+ *   B_slices   host array of num_slices device pointers, slice s is [L, N_s, R]
+ *   slice_N    host array, N_s >= 0
+ *   slice_offset host array, first out column of slice s; the slices' column
+ *              ranges must not overlap and must lie inside [0, ldo)
+ *   y_slice_stride  slice s reads y columns [s*y_slice_stride, s*y_slice_stride + R)
+ *              (R for a y produced by a stacked shrink); must keep them inside ldy
+ *   out columns outside every slice are never read or written.
+ * Errors: LORA_ERR_INVALID_ARG (NULL pointers, overlapping or out-of-range
+ * slices, bad strides, bad dtype), LORA_ERR_UNSUPPORTED, LORA_ERR_CUDA.
+ */
+lora_status_t lora_expand_slice(lora_dtype_t dtype, const float *y, int64_t ldy, int32_t T,
+                                int32_t num_slices, const void *const *B_slices,
+                                const int32_t *slice_N, const int32_t *slice_offset,
+                                int32_t y_slice_stride, int32_t L, int32_t R,
+                                const int32_t *ranks, void *out, int64_t ldo, const void *plan,
+                                float scale, int add_inputs, lora_stream_t stream);
+
+/*
+ * Reads the plan's device-side error words.  SYNCHRONISES `stream` (a
+ * device-to-host copy); for tests and debugging, not for the hot path.
+ * *bad_ids <- LORA_HDR_BAD_IDS, *err_flags <- LORA_HDR_ERR (either may be NULL).
+ * Errors: LORA_ERR_INVALID_ARG (plan NULL), LORA_ERR_CUDA.
+ */
+lora_status_t lora_get_error(const void *plan, int32_t *bad_ids, int32_t *err_flags,
+                             lora_stream_t stream);
+
+/* Static description of a status code. */
+const char *lora_status_string(lora_status_t status);
+
+/* Thread-local text describing the last non-OK status returned on this thread. */
+const char *lora_last_error_detail(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t lora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LORA_GEMV_H */

@@ -1,0 +1,172 @@
+// Device helpers shared by the plan, shrink and expand kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <limits.h>
+#include <stdint.h>
+
+#include "lora_gemv.h"
+
+namespace lora {
+
+constexpr int kTile = LORA_TILE_TOKENS;  // tokens per plan tile
+constexpr int kMaxSlices = LORA_MAX_SLICES;
+
+// ------------------------------------------------------------------ plan view
+struct PlanView {
+    int32_t *hdr;          // LORA_HDR_WORDS header words (kernels may OR error bits)
+    const int32_t *perm;   // [T]
+    const int4 *tiles;     // [max_tiles] {lora, p0, n, group}
+};
+
+__device__ __forceinline__ bool plan_matches(const PlanView &p, int T, int L) {
+    const volatile int32_t *h = p.hdr;
+    return h[LORA_HDR_MAGIC] == LORA_PLAN_MAGIC && h[LORA_HDR_T] == T && h[LORA_HDR_L] == L;
+}
+
+// ------------------------------------------------------------------ dtype traits
+template <typename E> struct Elem;
+template <> struct Elem<__half> {
+    static __device__ __forceinline__ float to_f(__half v) { return __half2float(v); }
+    static __device__ __forceinline__ __half from_f(float v) { return __float2half_rn(v); }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// mma.sync m16n8k16, fp32 accumulate; A row-major (4 regs), B col-major (2 regs).
+template <typename E>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<__half>(float (&d)[4], const uint32_t (&a)[4],
+                                                 uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float (&d)[4], const uint32_t (&a)[4],
+                                                        uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// 16-byte global->shared async copy; src_bytes in {0, 16} (0 = zero fill).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+                 "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// Streaming 16-byte global accesses for the read-modify-write of out.
+__device__ __forceinline__ uint4 ld_global_v4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};\n" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ int clamp_rank(const int32_t *ranks, int l, int R) {
+    if (ranks == nullptr) return R;
+    int r = __ldg(ranks + l);
+    return r < 0 ? 0 : (r > R ? R : r);
+}
+
+// ------------------------------------------------------------------ block scan
+// Exclusive prefix sum of one value per thread over the whole block
+// (blockDim.x a multiple of 32, <= 1024).  `ws` holds >= 33 ints of shared
+// memory.  Returns the exclusive prefix; *total receives the block sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *ws, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    __syncthreads();
+    if (lane == 31) ws[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nwarps ? ws[lane] : 0;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi += n;
+        }
+        if (lane < nwarps) ws[lane] = wi - w;
+        if (lane == 31) ws[32] = wi;
+    }
+    __syncthreads();
+    int res = ws[warp] + incl - v;
+    *total = ws[32];
+    return res;
+}
+
+// Exclusive prefix max of one value per thread over the block (same
+// contract as block_exclusive_scan; the identity is INT_MIN).  *total
+// receives the block maximum.
+__device__ __forceinline__ int block_exclusive_max(int v, int *ws, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl = max(incl, n);
+    }
+    int excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = INT_MIN;
+    __syncthreads();
+    if (lane == 31) ws[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < nwarps ? ws[lane] : INT_MIN;
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o) wi = max(wi, n);
+        }
+        int ex = __shfl_up_sync(0xffffffffu, wi, 1);
+        if (lane == 0) ex = INT_MIN;
+        if (lane < nwarps) ws[lane] = ex;
+        if (lane == 31) ws[32] = wi;
+    }
+    __syncthreads();
+    int res = max(ws[warp], excl);
+    *total = ws[32];
+    return res;
+}
+
+}  // namespace lora

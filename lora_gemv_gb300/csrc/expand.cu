@@ -1,0 +1,332 @@
+// Expand / expand_slice: out[t, off_s + n] (+)= scale * sum_i y[t, s*ys + i] * B_s[l, n, i].
+//
+// Pages: vLLM PR #11579 "[misc] Add LoRA kernel micro benchmarks"
+// (bgmv_expand, sgmv_expand, the _slice forms with num_slices, add_inputs as
+// "group-gemm + outputs", the f32 x f16 => f16 typing); Punica issue #17
+// (SGMV: tokens sharing an adapter reuse its weights).
+//
+// Design (GB300): the operator is an HBM-bound read-modify-write of out; the
+// adapter tile is small and reused by every token of a plan tile.
+//  - grid.x walks the plan's 64-token tiles (one adapter each), grid.y the
+//    128-column chunks of all slices, so one launch covers every slice;
+//  - a CTA stages B_s[l, n0:n0+128, 0:r_l] and the tile's y rows in shared
+//    memory, then each warp owns 32 output columns of all 64 tokens;
+//  - out is read and written with 16-byte accesses straight from registers:
+//    the MMA columns are permuted (B rows are stored permuted in shared
+//    memory) so that every thread's accumulators are 8 contiguous columns;
+//  - y (fp32) enters the fp16/bf16 tensor-core MMA (m16n8k16, fp32
+//    accumulate) as hi + lo parts after scaling each token row by a power of
+//    two, so the product keeps ~fp32 accuracy of y and never overflows fp16;
+//  - tiles with adapter -1 and adapters of rank 0 load nothing (block
+//    skipping) and, without add_inputs, only store zeros.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lora {
+namespace {
+
+constexpr int kThreads = 128;  // 4 warps
+constexpr int kCols = 128;     // output columns per CTA (32 per warp)
+
+__host__ __device__ constexpr int pitch_of(int ks) { return ks * 16 + 8; }  // elements per smem row
+
+// Shared-memory row of output column j of a chunk: inside each 32-column
+// block, column 8a + 2i + b (a, i in 0..3, b in 0..1) goes to row 8i + 2a + b,
+// so MMA n-tile i reads 8 consecutive rows.
+__device__ __forceinline__ int sigma(int j) {
+    return (j & ~31) + 8 * ((j >> 1) & 3) + 2 * ((j >> 3) & 3) + (j & 1);
+}
+
+template <typename E>
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+    uint4 r;
+    uint32_t *w = reinterpret_cast<uint32_t *>(&r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        E lo = Elem<E>::from_f(v[2 * k]), hi = Elem<E>::from_f(v[2 * k + 1]);
+        w[k] = (uint32_t)(*reinterpret_cast<uint16_t *>(&lo)) |
+               ((uint32_t)(*reinterpret_cast<uint16_t *>(&hi)) << 16);
+    }
+    return r;
+}
+
+template <typename E>
+__device__ __forceinline__ void unpack8(uint4 r, float (&v)[8]) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(&r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint16_t lo = (uint16_t)(w[k] & 0xffffu), hi = (uint16_t)(w[k] >> 16);
+        v[2 * k] = Elem<E>::to_f(*reinterpret_cast<E *>(&lo));
+        v[2 * k + 1] = Elem<E>::to_f(*reinterpret_cast<E *>(&hi));
+    }
+}
+
+template <typename E, bool ADD, bool VEC>
+__global__ void __launch_bounds__(kThreads)
+expand_kernel(const ExpandArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_rows[kTile];
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, q = lane & 3;
+
+    if (!plan_matches(PlanView{a.hdr, a.perm, a.tiles}, a.T, a.L)) {
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+            atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
+        return;
+    }
+
+    // column chunk -> slice
+    const int chunk = blockIdx.y;
+    int s = 0;
+    while (s + 1 < a.num_slices && chunk >= a.chunk_begin[s + 1]) ++s;
+    const int n0 = (chunk - a.chunk_begin[s]) * kCols;
+    const int Ns = a.N[s];
+    const int ncols = min(kCols, Ns - n0);
+    const E *__restrict__ B = static_cast<const E *>(a.B[s]);
+    E *__restrict__ out = static_cast<E *>(a.out);
+    const int64_t col0 = (int64_t)a.off[s] + n0;
+    const int R = a.R;
+    const bool b_vec = (R % 8 == 0) && ((reinterpret_cast<uintptr_t>(B) & 15) == 0);
+
+    const int ks_max = (R + 15) / 16;
+    E *sB = reinterpret_cast<E *>(smem);                  // [kCols][pitch]
+    E *sYh = sB + kCols * pitch_of(ks_max);               // [kTile][pitch]
+    E *sYl = sYh + kTile * pitch_of(ks_max);              // [kTile][pitch]
+    float *sF = reinterpret_cast<float *>(sYl + kTile * pitch_of(ks_max));  // [kTile]
+
+    const int n_tiles = min(a.hdr[LORA_HDR_NTILES], a.max_tiles);
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int4 tl = a.tiles[tile];
+        const int l = tl.x, p0 = tl.y, n = tl.z;
+        const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
+
+        if (threadIdx.x < kTile) {
+            int row = -1;
+            if (threadIdx.x < n) {
+                row = a.perm[p0 + threadIdx.x];
+                if (row < 0 || row >= a.T) row = -1;
+            }
+            s_rows[threadIdx.x] = row;
+        }
+        __syncthreads();
+
+        if (rl == 0) {  // adapter -1 (or rank 0): untouched with add_inputs, else zeros
+            if (!ADD) {
+                for (int it = threadIdx.x; it < kTile * (kCols / 8); it += kThreads) {
+                    const int i = it / (kCols / 8), c8 = (it % (kCols / 8)) * 8;
+                    const int row = s_rows[i];
+                    if (row < 0 || c8 >= ncols) continue;
+                    E *p = out + (int64_t)row * a.ldo + col0 + c8;
+                    if (VEC) {
+                        st_global_v4(p, make_uint4(0, 0, 0, 0));
+                    } else {
+                        for (int k = 0; k < 8 && c8 + k < ncols; ++k) p[k] = Elem<E>::from_f(0.f);
+                    }
+                }
+            }
+            __syncthreads();
+            continue;
+        }
+
+        const int KS = (rl + 15) / 16;
+        const int pitch = pitch_of(KS);
+        const int wcol = warp * 32 + q * 8;  // this thread's 8 columns within the chunk
+        const bool wact = warp * 32 < ncols;
+        const int nmb = (n + 15) / 16;
+
+        // 1) issue the reads of out early (they overlap the staging below)
+        uint4 old[4][2];
+        if (ADD && VEC && wact && wcol < ncols) {
+#pragma unroll
+            for (int mb = 0; mb < 4; ++mb) {
+                if (mb < nmb) {
+                    const int r0 = s_rows[mb * 16 + g], r1 = s_rows[mb * 16 + g + 8];
+                    if (r0 >= 0) old[mb][0] = ld_global_v4(out + (int64_t)r0 * a.ldo + col0 + wcol);
+                    if (r1 >= 0) old[mb][1] = ld_global_v4(out + (int64_t)r1 * a.ldo + col0 + wcol);
+                }
+            }
+        }
+
+        // 2) stage B_s[l, n0 : n0 + kCols, 0 : KS*16) (zero beyond r_l / ncols), rows permuted
+        const E *Bl = B + ((int64_t)l * Ns + n0) * R;
+        for (int it = threadIdx.x; it < kCols * 2 * KS; it += kThreads) {
+            const int j = it / (2 * KS), c8 = (it % (2 * KS)) * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (j < ncols && c8 < rl) {
+                const E *src = Bl + (int64_t)j * R + c8;
+                if (b_vec) {
+                    v = __ldg(reinterpret_cast<const uint4 *>(src));
+                    if (c8 + 8 > rl) {
+                        uint16_t *h = reinterpret_cast<uint16_t *>(&v);
+                        for (int k = rl - c8; k < 8; ++k) h[k] = 0;
+                    }
+                } else {
+                    uint16_t *h = reinterpret_cast<uint16_t *>(&v);
+                    const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src);
+                    for (int k = 0; k < 8 && c8 + k < rl; ++k) h[k] = __ldg(s16 + k);
+                }
+            }
+            *reinterpret_cast<uint4 *>(sB + sigma(j) * pitch + c8) = v;
+        }
+
+        // 3) stage y rows as scaled hi/lo pairs; one warp per token row
+        for (int i = warp; i < kTile; i += kThreads / 32) {
+            const int row = s_rows[i];
+            float v[4];
+            float m = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = lane + 32 * u;
+                v[u] = (row >= 0 && j < rl) ? a.y[(int64_t)row * a.ldy + (int64_t)s * a.y_slice_stride + j]
+                                             : 0.f;
+                m = fmaxf(m, fabsf(v[u]));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            int e = 0;
+            frexpf(m, &e);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = lane + 32 * u;
+                if (j < KS * 16) {
+                    const float vs = ldexpf(v[u], -e);
+                    const E hi = Elem<E>::from_f(vs);
+                    const E lo = Elem<E>::from_f(vs - Elem<E>::to_f(hi));
+                    sYh[i * pitch + j] = hi;
+                    sYl[i * pitch + j] = lo;
+                }
+            }
+            if (lane == 0) sF[i] = ldexpf(a.scale, e);
+        }
+        __syncthreads();
+
+        // 4) tensor-core MMAs + epilogue
+        if (wact) {
+#pragma unroll
+            for (int mb = 0; mb < 4; ++mb) {
+                if (mb >= nmb) break;
+                float acc[4][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t ah[4], al[4];
+                    const int arow = mb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                    const int acol = ks * 16 + 8 * (lane >> 4);
+                    ldmatrix_x4(ah, smem_u32(sYh + arow * pitch + acol));
+                    ldmatrix_x4(al, smem_u32(sYl + arow * pitch + acol));
+#pragma unroll
+                    for (int np = 0; np < 2; ++np) {
+                        uint32_t b[4];
+                        const int brow = warp * 32 + 8 * (2 * np + (lane >> 4)) + (lane & 7);
+                        const int bcol = ks * 16 + 8 * ((lane >> 3) & 1);
+                        ldmatrix_x4(b, smem_u32(sB + brow * pitch + bcol));
+                        mma16816<E>(acc[2 * np], ah, b[0], b[1]);
+                        mma16816<E>(acc[2 * np], al, b[0], b[1]);
+                        mma16816<E>(acc[2 * np + 1], ah, b[2], b[3]);
+                        mma16816<E>(acc[2 * np + 1], al, b[2], b[3]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int i = mb * 16 + g + 8 * h;
+                    const int row = s_rows[i];
+                    if (row < 0) continue;
+                    const float f = sF[i];
+                    float res[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) res[k] = f * acc[k >> 1][2 * h + (k & 1)];
+                    E *p = out + (int64_t)row * a.ldo + col0 + wcol;
+                    if (VEC) {
+                        if (wcol < ncols) {
+                            if (ADD) {
+                                float o[8];
+                                unpack8<E>(old[mb][h], o);
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) res[k] += o[k];
+                            }
+                            st_global_v4(p, pack8<E>(res));
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            if (wcol + k < ncols) {
+                                float r = res[k];
+                                if (ADD) r += Elem<E>::to_f(p[k]);
+                                p[k] = Elem<E>::from_f(r);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <typename E, bool ADD, bool VEC>
+cudaError_t configure_one() {
+    const int ks = LORA_MAX_RANK / 16;
+    const int smem = (kCols + 2 * kTile) * pitch_of(ks) * (int)sizeof(E) + kTile * (int)sizeof(float);
+    return cudaFuncSetAttribute(expand_kernel<E, ADD, VEC>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+template <typename E>
+cudaError_t configure_dtype() {
+    cudaError_t e;
+    if ((e = configure_one<E, false, false>()) != cudaSuccess) return e;
+    if ((e = configure_one<E, false, true>()) != cudaSuccess) return e;
+    if ((e = configure_one<E, true, false>()) != cudaSuccess) return e;
+    return configure_one<E, true, true>();
+}
+
+template <typename E>
+cudaError_t launch_dtype(const ExpandArgs &a, bool vec, dim3 grid, size_t smem, cudaStream_t st) {
+    if (a.add) {
+        if (vec) expand_kernel<E, true, true><<<grid, kThreads, smem, st>>>(a);
+        else expand_kernel<E, true, false><<<grid, kThreads, smem, st>>>(a);
+    } else {
+        if (vec) expand_kernel<E, false, true><<<grid, kThreads, smem, st>>>(a);
+        else expand_kernel<E, false, false><<<grid, kThreads, smem, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t configure_expand_kernels() {
+    cudaError_t e = configure_dtype<__half>();
+    if (e != cudaSuccess) return e;
+    return configure_dtype<__nv_bfloat16>();
+}
+
+cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceInfo &dev,
+                          cudaStream_t stream) {
+    ExpandArgs a = a_in;
+    (void)dev;
+    a.chunk_begin[0] = 0;
+    for (int s = 0; s < a.num_slices; ++s)
+        a.chunk_begin[s + 1] = a.chunk_begin[s] + (a.N[s] + kCols - 1) / kCols;
+    for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s];
+    const int chunks = a.chunk_begin[a.num_slices];
+    if (chunks == 0 || a.T == 0) return cudaSuccess;
+
+    // Vector path: every 8-column group of every slice is 16-byte aligned.
+    bool vec = (reinterpret_cast<uintptr_t>(a.out) & 15) == 0 && a.ldo % 8 == 0;
+    for (int s = 0; s < a.num_slices; ++s) vec = vec && a.off[s] % 8 == 0 && a.N[s] % 8 == 0;
+
+    // Tiles: ceil(T/64) full-or-partial tiles plus at most one ragged tile per
+    // adapter and one for the inactive tokens; CTAs loop if a plan has more.
+    const long long est = (a.T + kTile - 1) / kTile + (long long)std::min(a.L, a.T) + 1;
+    const int gx = (int)std::min<long long>(est, a.max_tiles);
+    dim3 grid(std::max(gx, 1), chunks);
+    const int ks = (a.R + 15) / 16;
+    const size_t smem = (size_t)(kCols + 2 * kTile) * pitch_of(ks) * 2 + kTile * sizeof(float);
+    return dt == LORA_F16 ? launch_dtype<__half>(a, vec, grid, smem, stream)
+                          : launch_dtype<__nv_bfloat16>(a, vec, grid, smem, stream);
+}
+
+}  // namespace lora

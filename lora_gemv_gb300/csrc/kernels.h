@@ -1,0 +1,74 @@
+// Internal interface between the C ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lora_gemv.h"
+
+namespace lora {
+
+// Writable views of the plan arrays (see lora_plan_layout_t).
+struct PlanPtrs {
+    int32_t *hdr, *count, *offset, *perm, *group_lora, *group_start, *group_count;
+    int4 *tiles;
+};
+
+struct ShrinkArgs {
+    const void *x;
+    int64_t ldx;
+    int T, H;
+    const void *A;
+    int L, R, S;
+    const int32_t *ranks;
+    float *y;
+    int64_t ldy;
+    float scale;
+    int add;
+    int32_t *hdr;
+    const int32_t *perm;
+    const int4 *tiles;
+    int max_tiles;
+};
+
+struct ExpandArgs {
+    const float *y;
+    int64_t ldy;
+    int T;
+    void *out;
+    int64_t ldo;
+    int L, R;
+    const int32_t *ranks;
+    int y_slice_stride;
+    float scale;
+    int add;
+    int num_slices;
+    const void *B[LORA_MAX_SLICES];
+    int N[LORA_MAX_SLICES];
+    int off[LORA_MAX_SLICES];
+    int chunk_begin[LORA_MAX_SLICES + 1];  // first column chunk of each slice (prefix sums)
+    int32_t *hdr;
+    const int32_t *perm;
+    const int4 *tiles;
+    int max_tiles;
+};
+
+struct DeviceInfo {
+    int sm_count;
+    int max_cluster;  // largest split-K cluster the shrink kernel can be launched with
+};
+
+cudaError_t configure_plan_kernels();
+cudaError_t configure_shrink_kernels(DeviceInfo *info);
+cudaError_t configure_expand_kernels();
+
+cudaError_t launch_group_tokens(const int32_t *idx, int T, int L, const PlanPtrs &p,
+                                cudaStream_t stream);
+cudaError_t launch_group_segments(const int32_t *ss, const int32_t *sl, const int32_t *slo, int S,
+                                  int T, int L, const PlanPtrs &p, cudaStream_t stream);
+cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo &dev,
+                          cudaStream_t stream);
+cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a, const DeviceInfo &dev,
+                          cudaStream_t stream);
+
+}  // namespace lora

@@ -81,8 +81,9 @@ int oracle_map_tokens(const int32_t *idx, int32_t T, int32_t L, int32_t *lora_of
  * Validity rules (the table is a list of sequences in batch order):
  *  - 0 <= start, 0 <= len, start + len <= T, else the segment is ignored and
  *    bit 1 of *err is set;
- *  - a non-empty segment must not start before the end of the previous
- *    non-empty valid segment, else it is ignored and bit 2 of *err is set;
+ *  - a non-empty segment must not start before the end of any earlier
+ *    non-empty in-range segment (the table lists sequences in batch order),
+ *    else it is ignored and bit 2 of *err is set;
  *  - lora outside [-1, L) is counted as a bad id and the segment acts as -1.
  * Returns the bad-id count.
  */
@@ -97,8 +98,9 @@ int oracle_map_segments(const int32_t *start, const int32_t *len, const int32_t 
         int64_t s0 = start[i], n = len[i];
         if (s0 < 0 || n < 0 || s0 + n > T) { *err |= 1; continue; }
         if (n == 0) continue;
-        if (s0 < prev_end) { *err |= 2; continue; }
-        prev_end = s0 + n;
+        int overlaps = s0 < prev_end;
+        if (s0 + n > prev_end) prev_end = s0 + n;
+        if (overlaps) { *err |= 2; continue; }
         int32_t l = lora[i];
         if (!(l >= -1 && l < L)) { bad++; l = -1; }
         for (int64_t t = s0; t < s0 + n; ++t) lora_of[t] = l;

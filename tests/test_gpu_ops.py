@@ -1,0 +1,300 @@
+"""Shrink / expand / expand_slice on the GPU against the oracle, element by
+element, on the seeded workloads and on edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import lora_inputs as li
+from helpers import assert_close, f64, gpu_plan, gpu_run, oracle_map, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+
+def full_check(lg, case, rows=None):
+    y, out, plan = gpu_run(lg, case)
+    y_ref, o_ref = oracle_run(case, rows)
+    if rows is not None:
+        y, out = y[rows], out[rows]
+    assert_close(y, y_ref, case.dtype, f"{case.name} y")
+    assert_close(out, o_ref, case.dtype, f"{case.name} out")
+    return y, out, plan
+
+
+# ---------------------------------------------------------------- workloads
+
+def test_bgmv_small(cuda_lib):
+    c = li.bgmv_small()
+    y, out, _ = full_check(cuda_lib, c)
+    # inactive tokens: y rows zero, out rows untouched bit for bit
+    m = (c.token_idx == -1).numpy()
+    assert (y.numpy()[m] == 0).all()
+    assert torch.equal(out[m].view(torch.int16), c.out[m].view(torch.int16))
+
+
+@pytest.mark.parametrize("T", li.DECODE_T)
+def test_decode_qkv(cuda_lib, T):
+    c = li.decode_qkv(T)
+    y, out, _ = full_check(cuda_lib, c)
+    m = (c.token_idx == -1).numpy()
+    assert torch.equal(out[m].view(torch.int16), c.out[m].view(torch.int16))
+
+
+@pytest.mark.parametrize("r", (16, 32, 64))
+def test_prefill_gateup(cuda_lib, r):
+    c = li.prefill_gateup(r=r)
+    g = np.random.default_rng(r)
+    rows = np.sort(g.choice(c.T, size=min(c.T, 384), replace=False))
+    full_check(cuda_lib, c, rows)
+
+
+@pytest.mark.parametrize("N,sgmv", [(8192, False), (28672, False), (8192, True)])
+def test_mixed_rank_70b(cuda_lib, N, sgmv):
+    c = li.mixed_rank_70b(N=N, sgmv=sgmv)
+    g = np.random.default_rng(N)
+    rows = np.sort(g.choice(c.T, size=256, replace=False))
+    full_check(cuda_lib, c, rows)
+
+
+@pytest.mark.parametrize("H", li.SWEEP_H)
+@pytest.mark.parametrize("batch,sl", [(16, 1), (512, 1), (16, 8), (2048, 8)])
+def test_sweep_points(cuda_lib, H, batch, sl):
+    c = li.sweep(H=H, batch=batch, seq_len=sl)
+    rows = None
+    if c.T > 512:
+        rows = np.sort(np.random.default_rng(H + batch).choice(c.T, 512, replace=False))
+    full_check(cuda_lib, c, rows)
+
+
+def test_sweep_largest_point_sampled(cuda_lib):
+    """batch 8192 x seq-len 8 = 65536 tokens at H = N = 16384: sampled rows."""
+    c = li.sweep(H=16384, batch=8192, seq_len=8)
+    rows = np.sort(np.random.default_rng(0).choice(c.T, 96, replace=False))
+    full_check(cuda_lib, c, rows)
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_bgmv_equals_sgmv_bitwise(cuda_lib):
+    """Punica issue #17: BGMV semantics are a subset of SGMV's.  The same
+    token -> adapter map given both ways gives bit-identical results."""
+    lg = cuda_lib
+    c = li.prefill_gateup(r=16, H=1024, N=1000, lens=[70, 5, 130, 64, 1, 9, 200, 33])
+    y_s, o_s, _ = gpu_run(lg, c)
+    c.token_idx = c.lora_of_token()
+    y_b, o_b, _ = gpu_run(lg, c)
+    assert torch.equal(y_s, y_b)
+    assert torch.equal(o_s.view(torch.int16), o_b.view(torch.int16))
+
+
+def test_expand_slice_equals_back_to_back(cuda_lib):
+    lg = cuda_lib
+    c = li.decode_qkv(200, seed=77)
+    plan = gpu_plan(lg, c, "cuda")
+    y = torch.randn(c.T, 48, generator=torch.Generator().manual_seed(1)).cuda()
+    Bs = [b.cuda() for b in c.B]
+    o1 = c.out.cuda()
+    lg.lora_expand_slice(y, Bs, o1, plan, c.slice_offsets, y_slice_stride=16)
+    o2 = c.out.cuda()
+    for s in range(3):
+        lg.lora_expand_slice(y, [Bs[s]], o2, plan, [c.slice_offsets[s]], y_slice_stride=0,
+                             ) if s == 0 else lg.lora_expand_slice(
+            y[:, 16 * s:], [Bs[s]], o2, plan, [c.slice_offsets[s]], y_slice_stride=0)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_rank_aware_equals_padded(cuda_lib):
+    """Punica issue #17: zero-padding ranks up to the largest changes nothing."""
+    lg = cuda_lib
+    kw = dict(T=300, H=512, L=8, N=384)
+    cg = li.mixed_rank_70b(pad_fill="garbage", **kw)
+    cz = li.mixed_rank_70b(pad_fill="zero", **kw)
+    y_g, o_g, _ = gpu_run(lg, cg)
+    cz.ranks = None
+    y_z, o_z, _ = gpu_run(lg, cz)
+    assert_close(y_g, f64(y_z), cg.dtype, "y")
+    assert_close(o_g, f64(o_z), cg.dtype, "out")
+    # and both against the oracle
+    y_ref, o_ref = oracle_run(cg)
+    assert_close(y_g, y_ref, cg.dtype, "y vs oracle")
+    assert_close(o_g, o_ref, cg.dtype, "out vs oracle")
+
+
+def test_single_adapter_equals_dense(cuda_lib):
+    """One adapter, every token: shrink = x A^T, expand = out + y B^T (the
+    torch.mm single-LoRA roofline of vLLM PR #11579), checked against a plain
+    fp64 matmul."""
+    lg = cuda_lib
+    g = torch.Generator().manual_seed(5)
+    T, H, R, N = 333, 1536, 16, 2048
+    x = torch.randn(T, H, generator=g).half()
+    A = (torch.randn(1, R, H, generator=g) * 0.02).half()
+    B = (torch.randn(1, N, R, generator=g) * 0.02).half()
+    out0 = torch.randn(T, N, generator=g).half()
+    plan = lg.new_plan(T, 1)
+    lg.lora_group_tokens(torch.zeros(T, dtype=torch.int32).cuda(), 1, plan)
+    y = torch.empty(T, R, device="cuda")
+    lg.lora_shrink(x.cuda(), A.cuda(), y, plan)
+    out = out0.cuda()
+    lg.lora_expand(y, B.cuda(), out, plan, add_inputs=True)
+    torch.cuda.synchronize()
+    y_ref = f64(x) @ f64(A[0]).T
+    assert_close(y, y_ref, torch.float16, "y")
+    assert_close(out, f64(out0) + y_ref @ f64(B[0]).T, torch.float16, "out")
+
+
+# ---------------------------------------------------------------- edge cases
+
+def make_case(T, H, R, L, N_list, dtype, seed, *, S=None, p_neg=0.2, add=True, scale=0.7,
+              sscale=1.3, ranks=None, offsets=None, N_total=None):
+    g = torch.Generator().manual_seed(seed)
+    S = S if S is not None else len(N_list)
+    x = torch.randn(T, H, generator=g).to(dtype)
+    A = (torch.randn(L, S * R, H, generator=g) * 0.05).to(dtype)
+    B = [(torch.randn(L, n, R, generator=g) * 0.05).to(dtype) for n in N_list]
+    if offsets is None:
+        offsets = [sum(N_list[:i]) for i in range(len(N_list))]
+    N_total = N_total or (max(o + n for o, n in zip(offsets, N_list)) if N_list else 0)
+    out = torch.randn(T, N_total, generator=g).to(dtype)
+    idx = torch.randint(0, L, (T,), generator=g, dtype=torch.int32)
+    neg = torch.rand(T, generator=g) < p_neg
+    idx[neg] = -1
+    c = li.Case(f"edge_T{T}_H{H}_R{R}_L{L}", dtype, x, A, B, out, offsets, R, S, L,
+                token_idx=idx, scale=scale, add=add)
+    c.shrink_scale = sscale
+    if ranks is not None:
+        c.ranks = torch.tensor(ranks, dtype=torch.int32)
+    return c
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("T,H,R,L,Ns", [
+    (1, 64, 16, 1, [64]),          # single token
+    (65, 1000, 16, 3, [200]),      # ragged tile, H not a multiple of 64
+    (130, 2049, 16, 4, [2049]),    # odd H and odd N: scalar paths
+    (77, 7, 3, 2, [5]),            # tiny odd everything
+    (129, 4096, 1, 2, [128]),      # rank 1
+    (64, 4096, 20, 5, [1032]),     # rank 20 (not a bin of 16)
+    (100, 640, 128, 3, [384]),     # rank 128, MMA over 8 k-steps
+    (300, 512, 48, 2, [256, 100]), # 2 slices (3 y blocks would exceed)
+])
+def test_edge_shapes(cuda_lib, dtype, T, H, R, L, Ns):
+    c = make_case(T, H, R, L, Ns, dtype, seed=T * 7 + H)
+    full_check(cuda_lib, c)
+
+
+@pytest.mark.parametrize("add", [False, True])
+def test_add_flag_and_inactive_rows(cuda_lib, add):
+    c = make_case(150, 256, 16, 3, [512], torch.float16, seed=3, add=add, p_neg=0.3)
+    y, out, _ = full_check(cuda_lib, c)
+    m = (c.token_idx == -1).numpy()
+    if add:
+        assert torch.equal(out[m].view(torch.int16), c.out[m].view(torch.int16))
+    else:
+        assert (out[m].float() == 0).all()
+    assert (y.numpy()[m] == 0).all()
+
+
+def test_all_tokens_inactive(cuda_lib):
+    c = make_case(100, 128, 16, 2, [256], torch.bfloat16, seed=4, p_neg=1.1)
+    y, out, _ = full_check(cuda_lib, c)
+    assert torch.equal(out.view(torch.int16), c.out.view(torch.int16))
+
+
+def test_mixed_ranks_with_zero_and_slices(cuda_lib):
+    c = make_case(400, 1024, 32, 6, [320, 96, 96], torch.bfloat16, seed=9,
+                  ranks=[0, 1, 7, 16, 31, 32])
+    full_check(cuda_lib, c)
+
+
+def test_slices_with_gaps_and_wide_out(cuda_lib):
+    """Slices placed at offsets with gaps inside a wider out: gap columns untouched."""
+    c = make_case(90, 256, 16, 3, [64, 48], torch.float16, seed=11, offsets=[8, 120],
+                  N_total=200, add=False)
+    y, out, _ = full_check(cuda_lib, c)
+    keep = np.r_[0:8, 72:120, 168:200]
+    assert torch.equal(out[:, keep].view(torch.int16), c.out[:, keep].view(torch.int16))
+
+
+def test_strided_x_y_out(cuda_lib):
+    """Leading dimensions larger than the logical widths."""
+    lg = cuda_lib
+    c = make_case(70, 512, 16, 3, [256], torch.float16, seed=12)
+    dev = "cuda"
+    plan = gpu_plan(lg, c, dev)
+    xb = torch.zeros(c.T, 520, dtype=c.dtype)
+    xb[:, :512] = c.x
+    xd = xb.to(dev)[:, :512]
+    yb = torch.full((c.T, 24), 123.0, device=dev)
+    y = yb[:, :16]
+    ob = torch.zeros(c.T, 264, dtype=c.dtype)
+    ob[:, :256] = c.out
+    od = ob.to(dev)
+    out = od[:, :256]
+    lg.lora_shrink(xd, c.A.to(dev), y, plan, scale=c.shrink_scale)
+    lg.lora_expand(y, c.B[0].to(dev), out, plan, scale=c.scale, add_inputs=True)
+    torch.cuda.synchronize()
+    y_ref, o_ref = oracle_run(c)
+    assert_close(y.cpu(), y_ref, c.dtype, "y")
+    assert_close(out.cpu(), o_ref, c.dtype, "out")
+    assert (yb[:, 16:].cpu() == 123.0).all()
+    assert (od[:, 256:].cpu().float() == 0).all()
+
+
+def test_shrink_add_inputs_accumulates(cuda_lib):
+    lg = cuda_lib
+    c = make_case(80, 384, 16, 2, [64], torch.float16, seed=13)
+    plan = gpu_plan(lg, c, "cuda")
+    y0 = torch.randn(c.T, 16, generator=torch.Generator().manual_seed(2))
+    y = y0.cuda()
+    lg.lora_shrink(c.x.cuda(), c.A.cuda(), y, plan, scale=0.5, add_inputs=True)
+    torch.cuda.synchronize()
+    lo, _, _ = oracle_map(c)
+    ref = oracle.shrink(f64(c.x), f64(c.A), lo, scale=0.5, add=True, y=y0.double().numpy())
+    assert_close(y.cpu(), ref, c.dtype, "y")
+
+
+def test_plan_mismatch_writes_nothing(cuda_lib):
+    lg = cuda_lib
+    c = make_case(50, 128, 16, 3, [64], torch.float16, seed=14)
+    plan = lg.new_plan(c.T, c.L)
+    lg.lora_group_tokens(c.token_idx.cuda(), c.L, plan)
+    # an operator told a different L than the plan was built with
+    y = torch.full((c.T, 16), 7.0, device="cuda")
+    lg.lora_shrink(c.x.cuda(), torch.cat([c.A, c.A]).cuda(), y, plan)
+    torch.cuda.synchronize()
+    assert (y.cpu() == 7.0).all()
+    bad, err = lg.lora_get_error(plan)
+    assert err & lg.PLANERR_MISMATCH
+
+
+def test_empty_batch_is_noop(cuda_lib):
+    lg = cuda_lib
+    plan = lg.new_plan(0, 2)
+    lg.lora_group_tokens(torch.empty(0, dtype=torch.int32, device="cuda"), 2, plan)
+    x = torch.empty(0, 64, dtype=torch.float16, device="cuda")
+    y = torch.empty(0, 16, device="cuda")
+    lg.lora_shrink(x, torch.zeros(2, 16, 64, dtype=torch.float16, device="cuda"), y, plan)
+    lg.lora_expand(y, torch.zeros(2, 32, 16, dtype=torch.float16, device="cuda"),
+                   torch.empty(0, 32, dtype=torch.float16, device="cuda"), plan)
+    torch.cuda.synchronize()
+
+
+def test_rejects_bad_arguments(cuda_lib):
+    lg = cuda_lib
+    c = make_case(10, 64, 16, 2, [32], torch.float16, seed=15)
+    plan = gpu_plan(lg, c, "cuda")
+    y = torch.zeros(10, 16, device="cuda")
+    out = c.out.cuda()
+    B = c.B[0].cuda()
+    with pytest.raises(lg.LoraError):  # overlapping slices
+        lg.lora_expand_slice(y, [B, B], torch.zeros(10, 64, dtype=torch.float16, device="cuda"),
+                             plan, [0, 16], y_slice_stride=0)
+    with pytest.raises(lg.LoraError):  # rank above 128
+        lg.lora_expand(torch.zeros(10, 130, device="cuda"),
+                       torch.zeros(2, 32, 130, dtype=torch.float16, device="cuda"), out, plan)
+    with pytest.raises(lg.LoraError):  # plan too small
+        lg.lora_group_tokens(c.token_idx.cuda(), 2, plan[:64])
+    with pytest.raises(ValueError):  # CPU tensor: no CPU path
+        lg.lora_expand(y.cpu(), B, out, plan)
