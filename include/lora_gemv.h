@@ -177,7 +177,7 @@ lora_status_t lora_group_segments(const int32_t *seg_start, const int32_t *seg_l
  *   plan                from lora_group_tokens / lora_group_segments with
  *                       the same T and L
  * Limits: 1 <= R <= LORA_MAX_RANK, 1 <= num_slices <= LORA_MAX_SLICES,
- * H >= 1.  T == 0 launches nothing.
+ * H >= 1.  T == 0 launches nothing (x and y may then be NULL).
  * Errors: LORA_ERR_INVALID_ARG (NULL pointers, bad sizes or strides, bad
  * dtype), LORA_ERR_UNSUPPORTED, LORA_ERR_CUDA.
  */
@@ -211,6 +211,7 @@ lora_status_t lora_expand(lora_dtype_t dtype, const float *y, int64_t ldy, int32
  *   y_slice_stride  slice s reads y columns [s*y_slice_stride, s*y_slice_stride + R)
  *              (R for a y produced by a stacked shrink); must keep them inside ldy
  *   out columns outside every slice are never read or written.
+ *   T == 0 launches nothing (y and out may then be NULL).
  * Errors: LORA_ERR_INVALID_ARG (NULL pointers, overlapping or out-of-range
  * slices, bad strides, bad dtype), LORA_ERR_UNSUPPORTED, LORA_ERR_CUDA.
  */

@@ -167,7 +167,7 @@ lora_status_t lora_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_
     if (ldx < H) return fail(LORA_ERR_INVALID_ARG, "ldx %lld < H %d", (long long)ldx, H);
     if (ldy < (int64_t)num_slices * R)
         return fail(LORA_ERR_INVALID_ARG, "ldy %lld < num_slices*R", (long long)ldy);
-    if (!x || !A || !y || !plan) return fail(LORA_ERR_INVALID_ARG, "NULL pointer");
+    if (!A || !plan || (T > 0 && (!x || !y))) return fail(LORA_ERR_INVALID_ARG, "NULL pointer");
     if (!aligned(x, 2) || !aligned(A, 2) || !aligned(y, 4) || !aligned(ranks, 4))
         return fail(LORA_ERR_INVALID_ARG, "misaligned pointer");
     if (!aligned(plan, 16)) return fail(LORA_ERR_WORKSPACE, "plan is not 16-byte aligned");
@@ -216,7 +216,7 @@ lora_status_t lora_expand_slice(lora_dtype_t dtype, const float *y, int64_t ldy,
     if (y_slice_stride < 0) return fail(LORA_ERR_INVALID_ARG, "y_slice_stride < 0");
     if ((int64_t)(num_slices - 1) * y_slice_stride + R > ldy)
         return fail(LORA_ERR_INVALID_ARG, "y columns of the last slice exceed ldy");
-    if (!y || !out || !plan) return fail(LORA_ERR_INVALID_ARG, "NULL pointer");
+    if (!plan || (T > 0 && (!y || !out))) return fail(LORA_ERR_INVALID_ARG, "NULL pointer");
     if (!aligned(y, 4) || !aligned(out, 2) || !aligned(ranks, 4))
         return fail(LORA_ERR_INVALID_ARG, "misaligned pointer");
     if (!aligned(plan, 16)) return fail(LORA_ERR_WORKSPACE, "plan is not 16-byte aligned");
