@@ -143,7 +143,7 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- our arm
 
-def make_pool(dev, rank: int, l2_bytes: int):
+def make_pool(dev, rank: int, l2_bytes: int, only_T=None):
     """Rotating argument pool: sets of (inputs, adapters, outputs) for every
     batch size, enough sets that the pool is >= 4x L2, so each step reads
     data no earlier step left in L2."""
@@ -152,11 +152,11 @@ def make_pool(dev, rank: int, l2_bytes: int):
     for T in li.DECODE_T:
         per_set += T * (H * E + NTOT * E + len(SLICES) * R * 4 + 4) + L * (len(SLICES) * R * H
                                                                             + NTOT * R) * E
-    nsets = max(2, -(-4 * l2_bytes // per_set))
+    nsets = max(2, -(-4 * l2_bytes // per_set)) if only_T is None else 1
     pool = []
     for s in range(nsets):
         batches = []
-        for T in li.DECODE_T:
+        for T in (li.DECODE_T if only_T is None else (only_T,)):
             c = li.decode_qkv(T, seed=li.SEED_BASE + 2 + 1000 * rank + 17 * s + T)
             batches.append({
                 "T": T, "case": c,
@@ -254,6 +254,57 @@ def cpu_baseline(target_s: float = 10.0):
                       f"fp64 C loops, OpenMP over tokens, {el:.1f} s"}
 
 
+def _timing_event(external: bool):
+    if external:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    return torch.cuda.Event(enable_timing=True)
+
+
+def capture_steps(lg, pool):
+    """One CUDA graph per pool set holding a whole step (launch overhead off
+    the timed path, as the pages time their kernels).  Timing events bracket
+    every expand_slice inside the graph when torch can record graph event
+    nodes; the last replay of each graph leaves its durations behind."""
+    graphs = []
+    try:
+        _timing_event(True)
+        external = True
+    except TypeError:
+        external = False
+    stream = torch.cuda.Stream()
+    for batches in pool:
+        g = torch.cuda.CUDAGraph()
+        ev = [[_timing_event(True), _timing_event(True)] for _ in batches] if external else None
+        with torch.cuda.graph(g, stream=stream):
+            run_step(lg, batches, ev)
+        graphs.append((g, ev))
+    torch.cuda.synchronize()
+    return graphs, external
+
+
+def expand_only_ms(lg, pool, reps: int = 20):
+    """Fallback timing of expand_slice alone: a graph of one launch per pool
+    set for every batch size, replayed `reps` times between two events."""
+    res = []
+    stream = torch.cuda.Stream()
+    for i in range(len(li.DECODE_T)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for batches in pool:
+                b = batches[i]
+                lg.lora_expand_slice(b["y"], b["B"], b["out"], b["plan"],
+                                     b["case"].slice_offsets, y_slice_stride=R, add_inputs=True)
+        g.replay()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        res.append(t0.elapsed_time(t1) / (reps * len(pool)))
+    return res
+
+
 def main_ours(args):
     import torch.distributed as dist
     ws, rank, local = dist_env()
@@ -268,17 +319,20 @@ def main_ours(args):
     nsets = len(pool)
     K, W = args.steps, args.warmup
 
-    for w in range(W):
+    for w in range(max(W, 1)):  # eager warm-up also configures the kernels before capture
         run_step(lg, pool[w % nsets])
+    torch.cuda.synchronize()
+    graphs, in_graph_events = capture_steps(lg, pool)
+    for w in range(W):
+        graphs[w % nsets][0].replay()
     torch.cuda.synchronize()
 
     nb = len(li.DECODE_T)
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nb)]
-          for _ in range(K)]
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
-                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    clocks = ClockSampler(int(cvd.split(",")[local]) if cvd and all(
+        c.strip().isdigit() for c in cvd.split(",")) else local)
     clocks.start()
     if ws > 1:
         dist.barrier()
@@ -286,7 +340,7 @@ def main_ours(args):
     wall0 = time.perf_counter()
     start.record()
     for k in range(K):
-        run_step(lg, pool[(W + k) % nsets], ev[k])
+        graphs[(W + k) % nsets][0].replay()
     end.record()
     torch.cuda.synchronize()
     if ws > 1:
@@ -295,7 +349,14 @@ def main_ours(args):
     clk = clocks.stop()
 
     ms = start.elapsed_time(end)
-    ex_ms = [sum(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)) for i in range(nb)]
+    if in_graph_events:
+        # durations of every batch's expand_slice in the last replay of each pool set
+        ex_ms = [statistics.fmean(graphs[p][1][i][0].elapsed_time(graphs[p][1][i][1])
+                                  for p in range(nsets)) for i in range(nb)]
+        ex_src = f"CUDA events inside the step graphs (last replay of each of {nsets} sets)"
+    else:
+        ex_ms = expand_only_ms(lg, pool)
+        ex_src = "CUDA events around a graph of expand_slice launches over the pool"
     if ws > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -304,24 +365,23 @@ def main_ours(args):
     tokens_rank = K * sum(li.DECODE_T)
     value = tokens_rank * ws / (ms / 1e3)
 
-    # algorithmic work of the step (same for every pool set up to the random ids)
     per_T = {}
-    ex_bytes_tot = sh_bytes_tot = 0
-    ex_time_tot = 0.0
+    ex_bytes = sh_bytes = 0
+    ex_time = 0.0
     for i, T in enumerate(li.DECODE_T):
         sb, sf, eb, ef = algorithmic(pool[0][i]["case"].token_idx)
-        ex_bytes_tot += eb * K
-        sh_bytes_tot += sb * K
-        ex_time_tot += ex_ms[i] / 1e3
-        per_T[str(T)] = {"expand_us": ex_ms[i] / K * 1e3,
-                         "expand_GBps": eb / (ex_ms[i] / K / 1e3) / 1e9,
+        ex_bytes += eb
+        sh_bytes += sb
+        ex_time += ex_ms[i] / 1e3
+        per_T[str(T)] = {"expand_us": ex_ms[i] * 1e3,
+                         "expand_GBps": eb / (ex_ms[i] / 1e3) / 1e9,
                          "expand_bytes": eb, "shrink_bytes": sb}
     hbm, tf, src = peaks()
-    achieved = ex_bytes_tot / ex_time_tot / 1e9
-    path_bytes = (ex_bytes_tot + sh_bytes_tot) / K
-    path_frac = (path_bytes / (hbm * 1e9)) / (ms / 1e3 / K)
+    achieved = ex_bytes / ex_time / 1e9          # bytes of the 5 launches / their summed time
+    step_s = ms / 1e3 / K
+    path_frac = ((ex_bytes + sh_bytes) / (hbm * 1e9)) / step_s
 
-    e2e_v, h2d, d2h, e2e_wall = e2e_run(lg, dev, max(10, K // 10), 3)
+    e2e_v, h2d, d2h, e2e_wall = e2e_run(lg, dev, max(10, min(K, 300)), 3)
 
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
@@ -330,14 +390,17 @@ def main_ours(args):
         "config": {"workload": WORKLOAD, "tokens_per_step_per_gpu": sum(li.DECODE_T),
                    "parallelism": f"replicas x{ws} (independent batches, no collective)",
                    "l2": f"rotating argument pool of {nsets} sets ({pool_bytes / 1e6:.0f} MB "
-                         f">= 4x L2 {props.L2_cache_size / 1e6:.0f} MB): inputs larger than L2"},
+                         f">= 4x L2 {props.L2_cache_size / 1e6:.0f} MB): inputs larger than L2",
+                   "launch": "each step replayed from a CUDA graph (one per pool set)"},
         "roofline": {"kernel": "expand_slice", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": f"{src} hbm_gbs", "traffic": None},
+                     "peak_source": f"{src} hbm_gbs", "traffic": None,
+                     "timing": ex_src},
         "path_roofline_frac": path_frac,
         "gpu_launches": K * nb * 3,
         "e2e": {"value": e2e_v, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "wall_tokens_per_s": e2e_wall},
+                "d2h_bytes_per_step": d2h, "wall_tokens_per_s": e2e_wall,
+                "how": "public Python API per call (no graph), pinned host buffers"},
         "clocks": clk,
         "per_T": per_T,
         "wall_s_timed": wall,
@@ -401,6 +464,21 @@ def _ref_step(oracle, prepared, rows):
     return n
 
 
+def main_profile(args):
+    """A few eager launches of the path on one decode batch, for profilers
+    (e.g. ncu -k regex:expand -s 2 -c 1 python bench.py --profile --T 1024)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import lora_gemv_gb300 as lg
+    lg.load()
+    pool, _ = make_pool(dev, 0, 0, only_T=args.T)
+    for _ in range(args.profile_reps):
+        for batches in pool:
+            run_step(lg, batches)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": True, "T": args.T, "reps": args.profile_reps}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,7 +488,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-budget-s", type=float, default=90.0)
+    ap.add_argument("--profile", action="store_true",
+                    help="run a few eager steps of one decode batch (for ncu), no timing")
+    ap.add_argument("--T", type=int, default=1024, help="batch size for --profile")
+    ap.add_argument("--profile-reps", type=int, default=3)
     args = ap.parse_args()
+    if args.profile:
+        return main_profile(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":

@@ -61,6 +61,19 @@ __device__ __forceinline__ void unpack8(uint4 r, float (&v)[8]) {
     }
 }
 
+// v = hi + lo with hi = round(v) and lo = round(v - hi) in the weight type.
+template <typename E>
+__device__ __forceinline__ void split_hilo8(const float (&v)[8], uint4 &hi, uint4 &lo) {
+    float h[8], l[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        h[k] = Elem<E>::to_f(Elem<E>::from_f(v[k]));
+        l[k] = v[k] - h[k];
+    }
+    hi = pack8<E>(h);
+    lo = pack8<E>(l);
+}
+
 template <typename E, bool ADD, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 expand_kernel(const ExpandArgs a) {
@@ -70,7 +83,12 @@ expand_kernel(const ExpandArgs a) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
 
-    if (!plan_matches(PlanView{a.hdr, a.perm, a.tiles}, a.T, a.L)) {
+    // The plan header and this CTA's first tile are read together.
+    const int4 h0 = __ldcg(reinterpret_cast<const int4 *>(a.hdr));      // magic, T, L, kind
+    const int4 h1 = __ldcg(reinterpret_cast<const int4 *>(a.hdr) + 1);  // nactive, ngroups, ntiles
+    int4 tl_next = (int)blockIdx.x < a.max_tiles ? __ldcg(a.tiles + blockIdx.x)
+                                                 : make_int4(-1, 0, 0, -1);
+    if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
             atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
         return;
@@ -95,16 +113,17 @@ expand_kernel(const ExpandArgs a) {
     E *sYl = sYh + kTile * pitch_of(ks_max);              // [kTile][pitch]
     float *sF = reinterpret_cast<float *>(sYl + kTile * pitch_of(ks_max));  // [kTile]
 
-    const int n_tiles = min(a.hdr[LORA_HDR_NTILES], a.max_tiles);
+    const int n_tiles = min(h1.z, a.max_tiles);
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        const int4 tl = a.tiles[tile];
+        const int4 tl = tl_next;
+        if (tile + (int)gridDim.x < n_tiles) tl_next = __ldcg(a.tiles + tile + gridDim.x);
         const int l = tl.x, p0 = tl.y, n = tl.z;
         const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
 
         if (threadIdx.x < kTile) {
             int row = -1;
             if (threadIdx.x < n) {
-                row = a.perm[p0 + threadIdx.x];
+                row = __ldcg(a.perm + p0 + threadIdx.x);
                 if (row < 0 || row >= a.T) row = -1;
             }
             s_rows[threadIdx.x] = row;
@@ -121,7 +140,9 @@ expand_kernel(const ExpandArgs a) {
                     if (VEC) {
                         st_global_v4(p, make_uint4(0, 0, 0, 0));
                     } else {
-                        for (int k = 0; k < 8 && c8 + k < ncols; ++k) p[k] = Elem<E>::from_f(0.f);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            if (c8 + k < ncols) p[k] = Elem<E>::from_f(0.f);
                     }
                 }
             }
@@ -155,49 +176,67 @@ expand_kernel(const ExpandArgs a) {
             uint4 v = make_uint4(0, 0, 0, 0);
             if (j < ncols && c8 < rl) {
                 const E *src = Bl + (int64_t)j * R + c8;
+                const int nv = rl - c8;  // valid elements of this 8-element chunk
                 if (b_vec) {
                     v = __ldg(reinterpret_cast<const uint4 *>(src));
-                    if (c8 + 8 > rl) {
-                        uint16_t *h = reinterpret_cast<uint16_t *>(&v);
-                        for (int k = rl - c8; k < 8; ++k) h[k] = 0;
+                    if (nv < 8) {
+                        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            w[k] &= (2 * k + 1 < nv) ? 0xffffffffu : (2 * k < nv ? 0xffffu : 0u);
                     }
                 } else {
-                    uint16_t *h = reinterpret_cast<uint16_t *>(&v);
                     const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src);
-                    for (int k = 0; k < 8 && c8 + k < rl; ++k) h[k] = __ldg(s16 + k);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t lo16 = 2 * k < nv ? __ldg(s16 + 2 * k) : 0u;
+                        const uint32_t hi16 = 2 * k + 1 < nv ? __ldg(s16 + 2 * k + 1) : 0u;
+                        w[k] = lo16 | (hi16 << 16);
+                    }
+                    v = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
             *reinterpret_cast<uint4 *>(sB + sigma(j) * pitch + c8) = v;
         }
 
-        // 3) stage y rows as scaled hi/lo pairs; one warp per token row
-        for (int i = warp; i < kTile; i += kThreads / 32) {
+        // 3) stage y rows as scaled hi/lo pairs: two threads per token row,
+        //    each owning KS*8 columns, every load of a pass independent.
+        {
+            const int i = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * KS * 8;
             const int row = s_rows[i];
-            float v[4];
+            const float *yr = a.y + (int64_t)(row < 0 ? 0 : row) * a.ldy +
+                              (int64_t)s * a.y_slice_stride;
             float m = 0.f;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = lane + 32 * u;
-                v[u] = (row >= 0 && j < rl) ? a.y[(int64_t)row * a.ldy + (int64_t)s * a.y_slice_stride + j]
-                                             : 0.f;
-                m = fmaxf(m, fabsf(v[u]));
-            }
+            for (int c = 0; c < LORA_MAX_RANK / 16; ++c) {
+                if (c < KS) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    for (int k = 0; k < 8; ++k) {
+                        const int j = c0 + 8 * c + k;
+                        if (row >= 0 && j < rl) m = fmaxf(m, fabsf(yr[j]));
+                    }
+                }
+            }
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
             int e = 0;
             frexpf(m, &e);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = lane + 32 * u;
-                if (j < KS * 16) {
-                    const float vs = ldexpf(v[u], -e);
-                    const E hi = Elem<E>::from_f(vs);
-                    const E lo = Elem<E>::from_f(vs - Elem<E>::to_f(hi));
-                    sYh[i * pitch + j] = hi;
-                    sYl[i * pitch + j] = lo;
+            for (int c = 0; c < LORA_MAX_RANK / 16; ++c) {
+                if (c < KS) {
+                    float vs[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int j = c0 + 8 * c + k;
+                        vs[k] = (row >= 0 && j < rl) ? ldexpf(yr[j], -e) : 0.f;
+                    }
+                    uint4 hi, lo;
+                    split_hilo8<E>(vs, hi, lo);
+                    *reinterpret_cast<uint4 *>(sYh + i * pitch + c0 + 8 * c) = hi;
+                    *reinterpret_cast<uint4 *>(sYl + i * pitch + c0 + 8 * c) = lo;
                 }
             }
-            if (lane == 0) sF[i] = ldexpf(a.scale, e);
+            if ((threadIdx.x & 1) == 0) sF[i] = ldexpf(a.scale, e);
         }
         __syncthreads();
 

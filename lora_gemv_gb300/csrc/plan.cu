@@ -67,8 +67,10 @@ __device__ void write_header(const PlanPtrs &p, int T, int L, int kind, int n_ac
 // a private histogram per warp, a scan over (adapter, warp) gives every warp
 // its first slot per adapter, pass 2 places tokens using match_any ranks so
 // equal ids keep their token order.  Shared memory: kPlanWarps * L ints.
-__global__ void __launch_bounds__(kPlanThreads, 1)
+template <int NW>
+__global__ void __launch_bounds__(NW * 32, 1)
 group_tokens_kernel(const int32_t *__restrict__ idx, int T, int L, PlanPtrs p) {
+    constexpr int kPlanWarps = NW;
     extern __shared__ int hist[];  // [kPlanWarps][L]
     __shared__ int ws[40];
     __shared__ int s_inact[kPlanWarps];
@@ -303,15 +305,26 @@ group_segments_kernel(const int32_t *__restrict__ ss, const int32_t *__restrict_
 
 static_assert(LORA_MAX_ADAPTERS <= kPlanThreads, "one thread per adapter");
 
+// Small batches (decode) use 8 warps: fewer threads make the block-wide
+// scans and barriers of this latency-bound kernel cheaper.
+constexpr int kSmallWarps = 8;
+constexpr int kSmallMaxT = 8192;
+
 cudaError_t configure_plan_kernels() {
-    return cudaFuncSetAttribute(group_tokens_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(group_tokens_kernel<kPlanWarps>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)(sizeof(int) * kPlanWarps * LORA_MAX_ADAPTERS));
 }
 
 cudaError_t launch_group_tokens(const int32_t *idx, int T, int L, const PlanPtrs &p,
                                 cudaStream_t stream) {
-    const size_t smem = sizeof(int) * kPlanWarps * (size_t)L;
-    group_tokens_kernel<<<1, kPlanThreads, smem, stream>>>(idx, T, L, p);
+    if (T <= kSmallMaxT && L <= kSmallWarps * 32) {
+        const size_t smem = sizeof(int) * kSmallWarps * (size_t)L;
+        group_tokens_kernel<kSmallWarps><<<1, kSmallWarps * 32, smem, stream>>>(idx, T, L, p);
+    } else {
+        const size_t smem = sizeof(int) * kPlanWarps * (size_t)L;
+        group_tokens_kernel<kPlanWarps><<<1, kPlanThreads, smem, stream>>>(idx, T, L, p);
+    }
     return cudaGetLastError();
 }
 

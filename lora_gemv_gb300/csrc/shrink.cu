@@ -101,7 +101,12 @@ shrink_kernel(const ShrinkArgs a, int kchunk) {
 
     // Every CTA of a cluster takes the same branch: the plan check reads the
     // same words, and the tile loop depends only on blockIdx.y / blockIdx.z.
-    if (!plan_matches(PlanView{a.hdr, a.perm, a.tiles}, a.T, a.L)) {
+    // The plan header and this CTA's first tile are read together.
+    const int4 h0 = __ldcg(reinterpret_cast<const int4 *>(a.hdr));      // magic, T, L, kind
+    const int4 h1 = __ldcg(reinterpret_cast<const int4 *>(a.hdr) + 1);  // nactive, ngroups, ntiles
+    int4 tl_next = (int)blockIdx.y < a.max_tiles ? __ldcg(a.tiles + blockIdx.y)
+                                                 : make_int4(-1, 0, 0, -1);
+    if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
             atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
         return;
@@ -116,9 +121,10 @@ shrink_kernel(const ShrinkArgs a, int kchunk) {
     E *sA = sX + kStages * kTile * kK;
     float *sRed = reinterpret_cast<float *>(smem);
 
-    const int n_tiles = min(a.hdr[LORA_HDR_NTILES], a.max_tiles);
+    const int n_tiles = min(h1.z, a.max_tiles);
     for (int tile = blockIdx.y; tile < n_tiles; tile += gridDim.y) {
-        const int4 tl = a.tiles[tile];
+        const int4 tl = tl_next;
+        if (tile + (int)gridDim.y < n_tiles) tl_next = __ldcg(a.tiles + tile + gridDim.y);
         const int l = tl.x, p0 = tl.y, n = tl.z;
         const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
 
@@ -139,7 +145,7 @@ shrink_kernel(const ShrinkArgs a, int kchunk) {
         if (threadIdx.x < kTile) {
             int row = -1;
             if (threadIdx.x < n) {
-                row = a.perm[p0 + threadIdx.x];
+                row = __ldcg(a.perm + p0 + threadIdx.x);
                 if (row < 0 || row >= a.T) row = -1;
             }
             s_rows[threadIdx.x] = row;
