@@ -305,6 +305,237 @@ expand_kernel(const ExpandArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming expand (the fast path: 16-byte aligned out columns and B rows).
+//
+// A persistent grid walks "units" (plan tile x 128-column chunk) in a
+// contiguous range per CTA, tile-major, so consecutive units share the
+// tile's token rows and y.  Each unit's out tile (gathered rows) and B tile
+// are copied into shared memory by cp.async, STAGES units ahead, so every
+// SM keeps ~100 KB of HBM reads in flight; results are stored straight from
+// registers with 16-byte stores.  y is converted to scaled hi/lo pairs only
+// when the unit's (tile, slice) changes.
+constexpr int kSThreads = 256;          // 8 warps: 4 column blocks x 2 row halves
+constexpr int kOutPitch = kCols + 8;    // elements per shared row of the out tile (272 B)
+
+__host__ __device__ constexpr int stream_stage_bytes(int ks_max) {
+    return kTile * kOutPitch * 2 + kCols * pitch_of(ks_max) * 2;
+}
+__host__ __device__ constexpr int stream_smem_bytes(int ks_max, int stages) {
+    return stages * stream_stage_bytes(ks_max) + 2 * kTile * pitch_of(ks_max) * 2 +
+           kTile * (int)sizeof(float);
+}
+
+struct UnitInfo {
+    int l, p0, n;        // tile: adapter, first perm position, tokens
+    int s, n0, ncols;    // chunk: slice, first column in the slice, columns
+    int rl;              // adapter rank (0 = nothing to add)
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const ExpandArgs &a, int u, int nchunks) {
+    UnitInfo ui;
+    const int t = u / nchunks, c = u - t * nchunks;
+    const int4 tl = __ldg(a.tiles + t);
+    ui.l = tl.x;
+    ui.p0 = tl.y;
+    ui.n = tl.z;
+    int s = 0;
+    while (s + 1 < a.num_slices && c >= a.chunk_begin[s + 1]) ++s;
+    ui.s = s;
+    ui.n0 = (c - a.chunk_begin[s]) * kCols;
+    ui.ncols = min(kCols, a.N[s] - ui.n0);
+    ui.rl = ui.l >= 0 && ui.l < a.L ? clamp_rank(a.ranks, ui.l, a.R) : 0;
+    return ui;
+}
+
+// (tile, slice) of unit u differs from that of unit u-1 (or u is the first).
+__device__ __forceinline__ bool new_y(const ExpandArgs &a, int u, int u_first, int nchunks) {
+    if (u == u_first) return true;
+    const int t = u / nchunks, c = u - t * nchunks;
+    if (c == 0) return true;
+    for (int s = 1; s < a.num_slices; ++s)
+        if (c == a.chunk_begin[s]) return true;
+    return false;
+}
+
+template <typename E, bool ADD>
+__device__ __forceinline__ void stream_issue(const ExpandArgs &a, const UnitInfo &ui,
+                                             unsigned char *stage, int pitch) {
+    if (ui.rl == 0) return;
+    E *sOut = reinterpret_cast<E *>(stage);
+    E *sB = reinterpret_cast<E *>(stage + kTile * kOutPitch * 2);
+    const E *out = static_cast<const E *>(a.out);
+    const int64_t col0 = (int64_t)a.off[ui.s] + ui.n0;
+    if (ADD) {
+        for (int it = threadIdx.x; it < kTile * (kCols / 8); it += kSThreads) {
+            const int i = it >> 4, ch = it & 15;
+            if (i < ui.n && ch * 8 < ui.ncols) {
+                const int row = __ldg(a.perm + ui.p0 + i);
+                if (row >= 0 && row < a.T)
+                    cp_async16(smem_u32(sOut + i * kOutPitch + ch * 8),
+                               out + (int64_t)row * a.ldo + col0 + ch * 8, 16);
+            }
+        }
+    }
+    const int KS = (ui.rl + 15) / 16;
+    const E *Bl = static_cast<const E *>(a.B[ui.s]) + ((int64_t)ui.l * a.N[ui.s] + ui.n0) * a.R;
+    for (int it = threadIdx.x; it < kCols * 2 * KS; it += kSThreads) {
+        const int j = it / (2 * KS), c8 = (it - j * 2 * KS) * 8;
+        const int nv = j < ui.ncols ? min(8, ui.rl - c8) : 0;
+        const E *src = nv > 0 ? Bl + (int64_t)j * a.R + c8 : Bl;
+        cp_async16(smem_u32(sB + sigma(j) * pitch + c8), src, nv > 0 ? 2 * nv : 0);
+    }
+}
+
+template <typename E, bool ADD, int STAGES>
+__global__ void __launch_bounds__(kSThreads, 1)
+expand_stream_kernel(const ExpandArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, q = lane & 3;
+    const int cb = warp & 3, rh = warp >> 2;  // 32-column block, 32-row half
+
+    const int4 h0 = __ldg(reinterpret_cast<const int4 *>(a.hdr));
+    const int4 h1 = __ldg(reinterpret_cast<const int4 *>(a.hdr) + 1);
+    if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
+        return;
+    }
+    const int nchunks = a.chunk_begin[a.num_slices];
+    const int n_tiles = min(h1.z, a.max_tiles);
+    const int U = n_tiles * nchunks;
+    const int per = (U + gridDim.x - 1) / gridDim.x;
+    const int u0 = blockIdx.x * per, u1 = min(U, u0 + per);
+    if (u0 >= u1) return;
+
+    const int ks_max = (a.R + 15) / 16;
+    const int pitch = pitch_of(ks_max);
+    const int sbytes = stream_stage_bytes(ks_max);
+    E *sYh = reinterpret_cast<E *>(smem + STAGES * sbytes);
+    E *sYl = sYh + kTile * pitch;
+    float *sF = reinterpret_cast<float *>(sYl + kTile * pitch);
+    E *__restrict__ out = static_cast<E *>(a.out);
+
+#pragma unroll
+    for (int k = 0; k < STAGES - 1; ++k) {
+        if (u0 + k < u1) stream_issue<E, ADD>(a, unit_info(a, u0 + k, nchunks), smem + k * sbytes, pitch);
+        cp_async_commit();
+    }
+    for (int u = u0; u < u1; ++u) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        const int nxt = u + STAGES - 1;
+        if (nxt < u1)
+            stream_issue<E, ADD>(a, unit_info(a, nxt, nchunks), smem + ((nxt - u0) % STAGES) * sbytes,
+                                 pitch);
+        cp_async_commit();
+
+        const UnitInfo ui = unit_info(a, u, nchunks);
+        const int64_t col0 = (int64_t)a.off[ui.s] + ui.n0;
+        if (ui.rl == 0) {  // adapter -1 or rank 0: nothing to add; without add_inputs, zeros
+            if (!ADD) {
+                for (int it = threadIdx.x; it < kTile * (kCols / 8); it += kSThreads) {
+                    const int i = it >> 4, ch = it & 15;
+                    if (i < ui.n && ch * 8 < ui.ncols) {
+                        const int row = __ldg(a.perm + ui.p0 + i);
+                        if (row >= 0 && row < a.T)
+                            st_global_v4(out + (int64_t)row * a.ldo + col0 + ch * 8, make_uint4(0, 0, 0, 0));
+                    }
+                }
+            }
+            continue;
+        }
+        const int KS = (ui.rl + 15) / 16;
+        if (new_y(a, u, u0, nchunks)) {
+            // 4 threads per token row: scaled hi/lo pairs of y[row, s*ys : s*ys + r_l)
+            const int i = threadIdx.x >> 2, part = threadIdx.x & 3;
+            const int row = i < ui.n ? __ldg(a.perm + ui.p0 + i) : -1;
+            const bool live = row >= 0 && row < a.T;
+            const float *yr = a.y + (int64_t)(live ? row : 0) * a.ldy + (int64_t)ui.s * a.y_slice_stride;
+            const int j0 = part * KS * 4;
+            float v[LORA_MAX_RANK / 4];
+            float m = 0.f;
+#pragma unroll
+            for (int k = 0; k < LORA_MAX_RANK / 4; ++k) {
+                const int j = j0 + k;
+                v[k] = (k < KS * 4 && live && j < ui.rl) ? yr[j] : 0.f;
+                m = fmaxf(m, fabsf(v[k]));
+            }
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            int e = 0;
+            frexpf(m, &e);
+#pragma unroll
+            for (int k = 0; k < LORA_MAX_RANK / 4; ++k) {
+                if (k < KS * 4) {
+                    const float vs = ldexpf(v[k], -e);
+                    const E hi = Elem<E>::from_f(vs);
+                    sYh[i * pitch + j0 + k] = hi;
+                    sYl[i * pitch + j0 + k] = Elem<E>::from_f(vs - Elem<E>::to_f(hi));
+                }
+            }
+            if (part == 0) sF[i] = ldexpf(a.scale, e);
+            __syncthreads();
+        }
+
+        const unsigned char *stage = smem + ((u - u0) % STAGES) * sbytes;
+        const E *sOut = reinterpret_cast<const E *>(stage);
+        const E *sB = reinterpret_cast<const E *>(stage + kTile * kOutPitch * 2);
+        const int wcol = cb * 32 + q * 8;
+        if (cb * 32 < ui.ncols) {
+#pragma unroll
+            for (int mm = 0; mm < 2; ++mm) {
+                const int mb = rh * 2 + mm;
+                if (mb * 16 >= ui.n) break;
+                float acc[4][4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
+                for (int ks = 0; ks < KS; ++ks) {
+                    uint32_t ah[4], al[4];
+                    const int arow = mb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                    const int acol = ks * 16 + 8 * (lane >> 4);
+                    ldmatrix_x4(ah, smem_u32(sYh + arow * pitch + acol));
+                    ldmatrix_x4(al, smem_u32(sYl + arow * pitch + acol));
+#pragma unroll
+                    for (int np = 0; np < 2; ++np) {
+                        uint32_t b[4];
+                        const int brow = cb * 32 + 8 * (2 * np + (lane >> 4)) + (lane & 7);
+                        const int bcol = ks * 16 + 8 * ((lane >> 3) & 1);
+                        ldmatrix_x4(b, smem_u32(sB + brow * pitch + bcol));
+                        mma16816<E>(acc[2 * np], ah, b[0], b[1]);
+                        mma16816<E>(acc[2 * np], al, b[0], b[1]);
+                        mma16816<E>(acc[2 * np + 1], ah, b[2], b[3]);
+                        mma16816<E>(acc[2 * np + 1], al, b[2], b[3]);
+                    }
+                }
+                if (wcol < ui.ncols) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int i = mb * 16 + g + 8 * h;
+                        if (i >= ui.n) continue;
+                        const int row = __ldg(a.perm + ui.p0 + i);
+                        if (row < 0 || row >= a.T) continue;
+                        const float f = sF[i];
+                        float res[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) res[k] = f * acc[k >> 1][2 * h + (k & 1)];
+                        if (ADD) {
+                            float o[8];
+                            unpack8<E>(*reinterpret_cast<const uint4 *>(sOut + i * kOutPitch + wcol), o);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) res[k] += o[k];
+                        }
+                        st_global_v4(out + (int64_t)row * a.ldo + col0 + wcol, pack8<E>(res));
+                    }
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+}
+
 template <typename E, bool ADD, bool VEC>
 cudaError_t configure_one() {
     const int ks = LORA_MAX_RANK / 16;
@@ -313,13 +544,41 @@ cudaError_t configure_one() {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
+template <typename E, bool ADD, int STAGES>
+cudaError_t configure_stream_one() {
+    // 4 stages serve ranks <= 32, 3 stages any rank (see launch_stream_dtype)
+    return cudaFuncSetAttribute(expand_stream_kernel<E, ADD, STAGES>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                STAGES == 4 ? stream_smem_bytes(2, 4)
+                                            : stream_smem_bytes(LORA_MAX_RANK / 16, 3));
+}
+
 template <typename E>
 cudaError_t configure_dtype() {
     cudaError_t e;
     if ((e = configure_one<E, false, false>()) != cudaSuccess) return e;
     if ((e = configure_one<E, false, true>()) != cudaSuccess) return e;
     if ((e = configure_one<E, true, false>()) != cudaSuccess) return e;
-    return configure_one<E, true, true>();
+    if ((e = configure_one<E, true, true>()) != cudaSuccess) return e;
+    if ((e = configure_stream_one<E, false, 3>()) != cudaSuccess) return e;
+    if ((e = configure_stream_one<E, false, 4>()) != cudaSuccess) return e;
+    if ((e = configure_stream_one<E, true, 3>()) != cudaSuccess) return e;
+    return configure_stream_one<E, true, 4>();
+}
+
+// Stages: 4 for ranks up to 32 (two CTAs per SM fit), else 3 (one CTA per SM).
+template <typename E>
+cudaError_t launch_stream_dtype(const ExpandArgs &a, int ks_max, int grid, cudaStream_t st) {
+    const int stages = ks_max <= 2 ? 4 : 3;
+    const size_t smem = stream_smem_bytes(ks_max, stages);
+    if (a.add) {
+        if (stages == 4) expand_stream_kernel<E, true, 4><<<grid, kSThreads, smem, st>>>(a);
+        else expand_stream_kernel<E, true, 3><<<grid, kSThreads, smem, st>>>(a);
+    } else {
+        if (stages == 4) expand_stream_kernel<E, false, 4><<<grid, kSThreads, smem, st>>>(a);
+        else expand_stream_kernel<E, false, 3><<<grid, kSThreads, smem, st>>>(a);
+    }
+    return cudaGetLastError();
 }
 
 template <typename E>
@@ -345,7 +604,6 @@ cudaError_t configure_expand_kernels() {
 cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceInfo &dev,
                           cudaStream_t stream) {
     ExpandArgs a = a_in;
-    (void)dev;
     a.chunk_begin[0] = 0;
     for (int s = 0; s < a.num_slices; ++s)
         a.chunk_begin[s + 1] = a.chunk_begin[s] + (a.N[s] + kCols - 1) / kCols;
@@ -360,6 +618,21 @@ cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceI
     // Tiles: ceil(T/64) full-or-partial tiles plus at most one ragged tile per
     // adapter and one for the inactive tokens; CTAs loop if a plan has more.
     const long long est = (a.T + kTile - 1) / kTile + (long long)std::min(a.L, a.T) + 1;
+    const int ks_max = (a.R + 15) / 16;
+    const bool b_vec_all = [&] {
+        if (a.R % 8 != 0) return false;
+        for (int s = 0; s < a.num_slices; ++s)
+            if (reinterpret_cast<uintptr_t>(a.B[s]) & 15) return false;
+        return true;
+    }();
+    if (vec && b_vec_all) {
+        // persistent grid: every CTA streams a contiguous range of units
+        const int per_sm = stream_smem_bytes(ks_max, ks_max <= 2 ? 4 : 3) * 2 <= 227 * 1024 ? 2 : 1;
+        const long long units = std::min<long long>(est, a.max_tiles) * chunks;
+        const int grid = (int)std::max<long long>(1, std::min<long long>(units, (long long)per_sm * dev.sm_count));
+        return dt == LORA_F16 ? launch_stream_dtype<__half>(a, ks_max, grid, stream)
+                              : launch_stream_dtype<__nv_bfloat16>(a, ks_max, grid, stream);
+    }
     const int gx = (int)std::min<long long>(est, a.max_tiles);
     dim3 grid(std::max(gx, 1), chunks);
     const int ks = (a.R + 15) / 16;

@@ -36,8 +36,12 @@ constexpr int kRows = 128;     // compacted A rows per CTA (grid.z covers more)
 constexpr int kK = 64;         // H elements per pipeline stage (128 bytes)
 constexpr int kStages = 4;
 constexpr int kRedPitch = kRows + 4;  // floats per reduction row
-constexpr int kSmem = kStages * (kTile + kRows) * kK * 2;
-static_assert(kTile * kRedPitch * 4 <= kSmem, "reduction buffer fits in the stage buffers");
+constexpr int kSmem = kStages * (kTile + kRows) * kK * 2;  // largest configuration
+// Shared memory for A tiles of `rows_cap` rows (a multiple of 16, <= kRows).
+__host__ __device__ constexpr int smem_bytes(int rows_cap) {
+    return kStages * (kTile + rows_cap) * kK * 2;
+}
+static_assert(kTile * kRedPitch * 4 <= smem_bytes(16), "reduction buffer fits in the stage buffers");
 
 // 128-byte rows, 16-byte chunks XOR-swizzled by the row index.
 __device__ __forceinline__ int swz(int row, int chunk) { return row * kK + ((chunk ^ (row & 7)) << 3); }
@@ -89,7 +93,7 @@ __device__ __forceinline__ void load_stage(E *sX, E *sA, const E *__restrict__ x
 
 template <typename E, bool VEC>
 __global__ void __launch_bounds__(kThreads)
-shrink_kernel(const ShrinkArgs a, int kchunk) {
+shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_rows[kTile];
     __shared__ int s_arow[kRows];
@@ -169,7 +173,7 @@ shrink_kernel(const ShrinkArgs a, int kchunk) {
 #pragma unroll
         for (int st = 0; st < kStages - 1; ++st) {
             if (st < nsteps)
-                load_stage<E, VEC>(sX + st * kTile * kK, sA + st * kRows * kK, x, a.ldx, Al, H,
+                load_stage<E, VEC>(sX + st * kTile * kK, sA + st * rows_cap * kK, x, a.ldx, Al, H,
                                    s_rows, s_arow, n, nrows, h_begin + st * kK, h_end);
             cp_async_commit();
         }
@@ -179,14 +183,14 @@ shrink_kernel(const ShrinkArgs a, int kchunk) {
             const int nxt = step + kStages - 1;
             if (nxt < nsteps) {
                 const int b = nxt % kStages;
-                load_stage<E, VEC>(sX + b * kTile * kK, sA + b * kRows * kK, x, a.ldx, Al, H,
+                load_stage<E, VEC>(sX + b * kTile * kK, sA + b * rows_cap * kK, x, a.ldx, Al, H,
                                    s_rows, s_arow, n, nrows, h_begin + nxt * kK, h_end);
             }
             cp_async_commit();
             if (wact) {
                 const int b = step % kStages;
                 const E *bx = sX + b * kTile * kK;
-                const E *ba = sA + b * kRows * kK;
+                const E *ba = sA + b * rows_cap * kK;
 #pragma unroll
                 for (int kk = 0; kk < kK / 16; ++kk) {
                     uint32_t af[4];
@@ -257,12 +261,12 @@ cudaError_t configure_one(int max_cluster) {
 }
 
 template <typename E>
-cudaError_t launch_dtype(const ShrinkArgs &a, bool vec, int ksplit, int kchunk, dim3 grid,
-                         cudaStream_t stream) {
+cudaError_t launch_dtype(const ShrinkArgs &a, bool vec, int ksplit, int kchunk, int rows_cap,
+                         dim3 grid, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmem;
+    cfg.dynamicSmemBytes = smem_bytes(rows_cap);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -271,8 +275,8 @@ cudaError_t launch_dtype(const ShrinkArgs &a, bool vec, int ksplit, int kchunk, 
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (vec) return cudaLaunchKernelEx(&cfg, shrink_kernel<E, true>, a, kchunk);
-    return cudaLaunchKernelEx(&cfg, shrink_kernel<E, false>, a, kchunk);
+    if (vec) return cudaLaunchKernelEx(&cfg, shrink_kernel<E, true>, a, kchunk, rows_cap);
+    return cudaLaunchKernelEx(&cfg, shrink_kernel<E, false>, a, kchunk, rows_cap);
 }
 
 }  // namespace
@@ -322,8 +326,12 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     const long long est = (a.T + kTile - 1) / kTile + (long long)std::min(a.L, a.T) + 1;
     const int gy = (int)std::max<long long>(1, std::min<long long>({est, a.max_tiles, 65535}));
     const int gz = (a.S * a.R + kRows - 1) / kRows;
-    // Split K so that the grid holds about two CTAs per SM, each with >= 2 stages of work.
-    const int target = 2 * dev.sm_count;
+    const int rows_cap = std::min(kRows, (a.S * a.R + 15) / 16 * 16);
+    // CTAs resident per SM (shared memory, and 128 registers x 128 threads)
+    const int per_sm = std::max(1, std::min(4, (227 * 1024) / (smem_bytes(rows_cap) + 1024)));
+    // Split K across a cluster so that the grid fills the resident slots,
+    // each CTA keeping >= 2 pipeline stages of work.
+    const int target = per_sm * dev.sm_count;
     int ksplit = 1;
     while (ksplit < dev.max_cluster && (long long)gy * gz * ksplit * 2 <= target &&
            (a.H + ksplit * 2 * kK - 1) / (ksplit * 2 * kK) >= 2)
@@ -332,8 +340,8 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     while (ksplit > 1 && (long long)(ksplit - 1) * kchunk >= a.H) ksplit /= 2;  // no empty CTAs
     kchunk = ((a.H + ksplit - 1) / ksplit + kK - 1) / kK * kK;
     dim3 grid(ksplit, gy, gz);
-    return dt == LORA_F16 ? launch_dtype<__half>(a, vec, ksplit, kchunk, grid, stream)
-                          : launch_dtype<__nv_bfloat16>(a, vec, ksplit, kchunk, grid, stream);
+    return dt == LORA_F16 ? launch_dtype<__half>(a, vec, ksplit, kchunk, rows_cap, grid, stream)
+                          : launch_dtype<__nv_bfloat16>(a, vec, ksplit, kchunk, rows_cap, grid, stream);
 }
 
 }  // namespace lora
