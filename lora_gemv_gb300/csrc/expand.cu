@@ -326,25 +326,36 @@ __host__ __device__ constexpr int stream_smem_bytes(int ks_max, int stages) {
            kTile * (int)sizeof(float);
 }
 
+constexpr int kWin = 8;  // plan tiles whose metadata a CTA holds in shared memory at once
+
 struct UnitInfo {
+    int w;               // tile slot in the CTA's window
     int l, p0, n;        // tile: adapter, first perm position, tokens
     int s, n0, ncols;    // chunk: slice, first column in the slice, columns
     int rl;              // adapter rank (0 = nothing to add)
 };
 
-__device__ __forceinline__ UnitInfo unit_info(const ExpandArgs &a, int u, int nchunks) {
+// Shared per-window plan metadata: tile records and their token rows.
+struct WinMeta {
+    int4 tile[kWin];          // {adapter, p0, n, rank}
+    int rows[kWin][kTile];    // out row of every token of the tile, -1 if none
+};
+
+__device__ __forceinline__ UnitInfo unit_info(const ExpandArgs &a, const WinMeta &wm, int u,
+                                              int t_first, int nchunks) {
     UnitInfo ui;
     const int t = u / nchunks, c = u - t * nchunks;
-    const int4 tl = __ldg(a.tiles + t);
+    ui.w = t - t_first;
+    const int4 tl = wm.tile[ui.w];
     ui.l = tl.x;
     ui.p0 = tl.y;
     ui.n = tl.z;
+    ui.rl = tl.w;
     int s = 0;
     while (s + 1 < a.num_slices && c >= a.chunk_begin[s + 1]) ++s;
     ui.s = s;
     ui.n0 = (c - a.chunk_begin[s]) * kCols;
     ui.ncols = min(kCols, a.N[s] - ui.n0);
-    ui.rl = ui.l >= 0 && ui.l < a.L ? clamp_rank(a.ranks, ui.l, a.R) : 0;
     return ui;
 }
 
@@ -359,22 +370,22 @@ __device__ __forceinline__ bool new_y(const ExpandArgs &a, int u, int u_first, i
 }
 
 template <typename E, bool ADD>
-__device__ __forceinline__ void stream_issue(const ExpandArgs &a, const UnitInfo &ui,
-                                             unsigned char *stage, int pitch) {
+__device__ __forceinline__ void stream_issue(const ExpandArgs &a, const WinMeta &wm,
+                                             const UnitInfo &ui, unsigned char *stage, int pitch) {
     if (ui.rl == 0) return;
     E *sOut = reinterpret_cast<E *>(stage);
     E *sB = reinterpret_cast<E *>(stage + kTile * kOutPitch * 2);
     const E *out = static_cast<const E *>(a.out);
     const int64_t col0 = (int64_t)a.off[ui.s] + ui.n0;
-    if (ADD) {
-        for (int it = threadIdx.x; it < kTile * (kCols / 8); it += kSThreads) {
-            const int i = it >> 4, ch = it & 15;
-            if (i < ui.n && ch * 8 < ui.ncols) {
-                const int row = __ldg(a.perm + ui.p0 + i);
-                if (row >= 0 && row < a.T)
-                    cp_async16(smem_u32(sOut + i * kOutPitch + ch * 8),
-                               out + (int64_t)row * a.ldo + col0 + ch * 8, 16);
-            }
+    if (ADD) {  // 4 threads per token row, 4 x 16 bytes each
+        const int i = threadIdx.x >> 2, ch0 = (threadIdx.x & 3) * 4;
+        const int row = wm.rows[ui.w][i];
+        if (row >= 0) {
+            const E *src = out + (int64_t)row * a.ldo + col0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if ((ch0 + k) * 8 < ui.ncols)
+                    cp_async16(smem_u32(sOut + i * kOutPitch + (ch0 + k) * 8), src + (ch0 + k) * 8, 16);
         }
     }
     const int KS = (ui.rl + 15) / 16;
@@ -389,24 +400,32 @@ __device__ __forceinline__ void stream_issue(const ExpandArgs &a, const UnitInfo
 
 template <typename E, bool ADD, int STAGES>
 __global__ void __launch_bounds__(kSThreads, 1)
-expand_stream_kernel(const ExpandArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
+expand_stream_kernel(const ExpandArgs a, int tiles_grid) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ WinMeta wm;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
     const int cb = warp & 3, rh = warp >> 2;  // 32-column block, 32-row half
 
+    // Units (tile x chunk, tile-major) are split over the grid by the host's
+    // tile bound, so the first window's tile records load with the header.
+    const int nchunks = a.chunk_begin[a.num_slices];
+    const int U_grid = tiles_grid * nchunks;
+    const int per = (U_grid + gridDim.x - 1) / gridDim.x;
+    const int u_begin = blockIdx.x * per;
     const int4 h0 = __ldg(reinterpret_cast<const int4 *>(a.hdr));
     const int4 h1 = __ldg(reinterpret_cast<const int4 *>(a.hdr) + 1);
+    int4 tl_first = make_int4(-1, 0, 0, 0);
+    if (threadIdx.x < kWin) {
+        const int t = u_begin / nchunks + threadIdx.x;
+        if (t < a.max_tiles) tl_first = __ldg(a.tiles + t);
+    }
     if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
         return;
     }
-    const int nchunks = a.chunk_begin[a.num_slices];
     const int n_tiles = min(h1.z, a.max_tiles);
-    const int U = n_tiles * nchunks;
-    const int per = (U + gridDim.x - 1) / gridDim.x;
-    const int u0 = blockIdx.x * per, u1 = min(U, u0 + per);
-    if (u0 >= u1) return;
+    const int u_end = min(n_tiles * nchunks, u_begin + per);
 
     const int ks_max = (a.R + 15) / 16;
     const int pitch = pitch_of(ks_max);
@@ -416,124 +435,160 @@ expand_stream_kernel(const ExpandArgs a) {
     float *sF = reinterpret_cast<float *>(sYl + kTile * pitch);
     E *__restrict__ out = static_cast<E *>(a.out);
 
-#pragma unroll
-    for (int k = 0; k < STAGES - 1; ++k) {
-        if (u0 + k < u1) stream_issue<E, ADD>(a, unit_info(a, u0 + k, nchunks), smem + k * sbytes, pitch);
-        cp_async_commit();
-    }
-    for (int u = u0; u < u1; ++u) {
-        cp_async_wait<STAGES - 2>();
+    for (int u0 = u_begin; u0 < u_end;) {
+        // ---- window: up to kWin tiles, metadata into shared memory
+        const int t_first = u0 / nchunks;
+        const int u1 = min(u_end, (t_first + kWin) * nchunks);
+        if (threadIdx.x < kWin) {
+            int4 tl = tl_first;
+            if (u0 != u_begin) {
+                const int t = t_first + threadIdx.x;
+                tl = t < n_tiles ? __ldg(a.tiles + t) : make_int4(-1, 0, 0, 0);
+            }
+            const int t = t_first + threadIdx.x;
+            if (t >= n_tiles) tl = make_int4(-1, 0, 0, 0);
+            const int rl = tl.x >= 0 && tl.x < a.L ? clamp_rank(a.ranks, tl.x, a.R) : 0;
+            wm.tile[threadIdx.x] = make_int4(tl.x, tl.y, tl.z, rl);
+        }
         __syncthreads();
-        const int nxt = u + STAGES - 1;
-        if (nxt < u1)
-            stream_issue<E, ADD>(a, unit_info(a, nxt, nchunks), smem + ((nxt - u0) % STAGES) * sbytes,
-                                 pitch);
-        cp_async_commit();
-
-        const UnitInfo ui = unit_info(a, u, nchunks);
-        const int64_t col0 = (int64_t)a.off[ui.s] + ui.n0;
-        if (ui.rl == 0) {  // adapter -1 or rank 0: nothing to add; without add_inputs, zeros
-            if (!ADD) {
-                for (int it = threadIdx.x; it < kTile * (kCols / 8); it += kSThreads) {
-                    const int i = it >> 4, ch = it & 15;
-                    if (i < ui.n && ch * 8 < ui.ncols) {
-                        const int row = __ldg(a.perm + ui.p0 + i);
-                        if (row >= 0 && row < a.T)
-                            st_global_v4(out + (int64_t)row * a.ldo + col0 + ch * 8, make_uint4(0, 0, 0, 0));
-                    }
-                }
+        for (int it = threadIdx.x; it < kWin * kTile; it += kSThreads) {
+            const int w = it / kTile, i = it - w * kTile;
+            const int4 tl = wm.tile[w];
+            int row = -1;
+            if (i < tl.z) {
+                row = __ldg(a.perm + tl.y + i);
+                if (row < 0 || row >= a.T) row = -1;
             }
-            continue;
+            wm.rows[w][i] = row;
         }
-        const int KS = (ui.rl + 15) / 16;
-        if (new_y(a, u, u0, nchunks)) {
-            // 4 threads per token row: scaled hi/lo pairs of y[row, s*ys : s*ys + r_l)
-            const int i = threadIdx.x >> 2, part = threadIdx.x & 3;
-            const int row = i < ui.n ? __ldg(a.perm + ui.p0 + i) : -1;
-            const bool live = row >= 0 && row < a.T;
-            const float *yr = a.y + (int64_t)(live ? row : 0) * a.ldy + (int64_t)ui.s * a.y_slice_stride;
-            const int j0 = part * KS * 4;
-            float v[LORA_MAX_RANK / 4];
-            float m = 0.f;
+        __syncthreads();
+
+        // ---- pipelined units of the window
 #pragma unroll
-            for (int k = 0; k < LORA_MAX_RANK / 4; ++k) {
-                const int j = j0 + k;
-                v[k] = (k < KS * 4 && live && j < ui.rl) ? yr[j] : 0.f;
-                m = fmaxf(m, fabsf(v[k]));
-            }
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-            int e = 0;
-            frexpf(m, &e);
-#pragma unroll
-            for (int k = 0; k < LORA_MAX_RANK / 4; ++k) {
-                if (k < KS * 4) {
-                    const float vs = ldexpf(v[k], -e);
-                    const E hi = Elem<E>::from_f(vs);
-                    sYh[i * pitch + j0 + k] = hi;
-                    sYl[i * pitch + j0 + k] = Elem<E>::from_f(vs - Elem<E>::to_f(hi));
-                }
-            }
-            if (part == 0) sF[i] = ldexpf(a.scale, e);
+        for (int k = 0; k < STAGES - 1; ++k) {
+            if (u0 + k < u1)
+                stream_issue<E, ADD>(a, wm, unit_info(a, wm, u0 + k, t_first, nchunks),
+                                     smem + k * sbytes, pitch);
+            cp_async_commit();
+        }
+        for (int u = u0; u < u1; ++u) {
+            cp_async_wait<STAGES - 2>();
             __syncthreads();
-        }
+            const int nxt = u + STAGES - 1;
+            if (nxt < u1)
+                stream_issue<E, ADD>(a, wm, unit_info(a, wm, nxt, t_first, nchunks),
+                                     smem + ((nxt - u0) % STAGES) * sbytes, pitch);
+            cp_async_commit();
 
-        const unsigned char *stage = smem + ((u - u0) % STAGES) * sbytes;
-        const E *sOut = reinterpret_cast<const E *>(stage);
-        const E *sB = reinterpret_cast<const E *>(stage + kTile * kOutPitch * 2);
-        const int wcol = cb * 32 + q * 8;
-        if (cb * 32 < ui.ncols) {
+            const UnitInfo ui = unit_info(a, wm, u, t_first, nchunks);
+            const int *rows = wm.rows[ui.w];
+            const int64_t col0 = (int64_t)a.off[ui.s] + ui.n0;
+            if (ui.rl == 0) {  // adapter -1 or rank 0: nothing to add; without add_inputs, zeros
+                if (!ADD) {
+                    const int i = threadIdx.x >> 2, ch0 = (threadIdx.x & 3) * 4;
+                    const int row = rows[i];
+                    if (row >= 0) {
 #pragma unroll
-            for (int mm = 0; mm < 2; ++mm) {
-                const int mb = rh * 2 + mm;
-                if (mb * 16 >= ui.n) break;
-                float acc[4][4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
-                for (int ks = 0; ks < KS; ++ks) {
-                    uint32_t ah[4], al[4];
-                    const int arow = mb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-                    const int acol = ks * 16 + 8 * (lane >> 4);
-                    ldmatrix_x4(ah, smem_u32(sYh + arow * pitch + acol));
-                    ldmatrix_x4(al, smem_u32(sYl + arow * pitch + acol));
-#pragma unroll
-                    for (int np = 0; np < 2; ++np) {
-                        uint32_t b[4];
-                        const int brow = cb * 32 + 8 * (2 * np + (lane >> 4)) + (lane & 7);
-                        const int bcol = ks * 16 + 8 * ((lane >> 3) & 1);
-                        ldmatrix_x4(b, smem_u32(sB + brow * pitch + bcol));
-                        mma16816<E>(acc[2 * np], ah, b[0], b[1]);
-                        mma16816<E>(acc[2 * np], al, b[0], b[1]);
-                        mma16816<E>(acc[2 * np + 1], ah, b[2], b[3]);
-                        mma16816<E>(acc[2 * np + 1], al, b[2], b[3]);
+                        for (int k = 0; k < 4; ++k)
+                            if ((ch0 + k) * 8 < ui.ncols)
+                                st_global_v4(out + (int64_t)row * a.ldo + col0 + (ch0 + k) * 8,
+                                             make_uint4(0, 0, 0, 0));
                     }
                 }
-                if (wcol < ui.ncols) {
+                continue;
+            }
+            const int KS = (ui.rl + 15) / 16;
+            if (new_y(a, u, u0, nchunks)) {
+                // 4 threads per token row: scaled hi/lo pairs of y[row, s*ys : s*ys + r_l)
+                const int i = threadIdx.x >> 2, part = threadIdx.x & 3;
+                const int row = rows[i];
+                const bool live = row >= 0;
+                const float *yr = a.y + (int64_t)(live ? row : 0) * a.ldy +
+                                  (int64_t)ui.s * a.y_slice_stride;
+                const int j0 = part * KS * 4;
+                float v[LORA_MAX_RANK / 4];
+                float m = 0.f;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int i = mb * 16 + g + 8 * h;
-                        if (i >= ui.n) continue;
-                        const int row = __ldg(a.perm + ui.p0 + i);
-                        if (row < 0 || row >= a.T) continue;
-                        const float f = sF[i];
-                        float res[8];
+                for (int k = 0; k < LORA_MAX_RANK / 4; ++k) {
+                    const int j = j0 + k;
+                    v[k] = (k < KS * 4 && live && j < ui.rl) ? yr[j] : 0.f;
+                    m = fmaxf(m, fabsf(v[k]));
+                }
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                int e = 0;
+                frexpf(m, &e);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) res[k] = f * acc[k >> 1][2 * h + (k & 1)];
-                        if (ADD) {
-                            float o[8];
-                            unpack8<E>(*reinterpret_cast<const uint4 *>(sOut + i * kOutPitch + wcol), o);
+                for (int k = 0; k < LORA_MAX_RANK / 4; ++k) {
+                    if (k < KS * 4) {
+                        const float vs = ldexpf(v[k], -e);
+                        const E hi = Elem<E>::from_f(vs);
+                        sYh[i * pitch + j0 + k] = hi;
+                        sYl[i * pitch + j0 + k] = Elem<E>::from_f(vs - Elem<E>::to_f(hi));
+                    }
+                }
+                if (part == 0) sF[i] = ldexpf(a.scale, e);
+                __syncthreads();
+            }
+
+            const unsigned char *stage = smem + ((u - u0) % STAGES) * sbytes;
+            const E *sOut = reinterpret_cast<const E *>(stage);
+            const E *sB = reinterpret_cast<const E *>(stage + kTile * kOutPitch * 2);
+            const int wcol = cb * 32 + q * 8;
+            if (cb * 32 < ui.ncols) {
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) res[k] += o[k];
+                for (int mm = 0; mm < 2; ++mm) {
+                    const int mb = rh * 2 + mm;
+                    if (mb * 16 >= ui.n) break;
+                    float acc[4][4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
+                    for (int ks = 0; ks < KS; ++ks) {
+                        uint32_t ah[4], al[4];
+                        const int arow = mb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+                        const int acol = ks * 16 + 8 * (lane >> 4);
+                        ldmatrix_x4(ah, smem_u32(sYh + arow * pitch + acol));
+                        ldmatrix_x4(al, smem_u32(sYl + arow * pitch + acol));
+#pragma unroll
+                        for (int np = 0; np < 2; ++np) {
+                            uint32_t b[4];
+                            const int brow = cb * 32 + 8 * (2 * np + (lane >> 4)) + (lane & 7);
+                            const int bcol = ks * 16 + 8 * ((lane >> 3) & 1);
+                            ldmatrix_x4(b, smem_u32(sB + brow * pitch + bcol));
+                            mma16816<E>(acc[2 * np], ah, b[0], b[1]);
+                            mma16816<E>(acc[2 * np], al, b[0], b[1]);
+                            mma16816<E>(acc[2 * np + 1], ah, b[2], b[3]);
+                            mma16816<E>(acc[2 * np + 1], al, b[2], b[3]);
                         }
-                        st_global_v4(out + (int64_t)row * a.ldo + col0 + wcol, pack8<E>(res));
+                    }
+                    if (wcol < ui.ncols) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int i = mb * 16 + g + 8 * h;
+                            const int row = rows[i];
+                            if (row < 0) continue;
+                            const float f = sF[i];
+                            float res[8];
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) res[k] = f * acc[k >> 1][2 * h + (k & 1)];
+                            if (ADD) {
+                                float o[8];
+                                unpack8<E>(*reinterpret_cast<const uint4 *>(sOut + i * kOutPitch + wcol), o);
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) res[k] += o[k];
+                            }
+                            st_global_v4(out + (int64_t)row * a.ldo + col0 + wcol, pack8<E>(res));
+                        }
                     }
                 }
             }
         }
+        cp_async_wait<0>();
+        __syncthreads();  // the window's shared metadata and stages are free again
+        u0 = u1;
     }
-    cp_async_wait<0>();
 }
 
 template <typename E, bool ADD, bool VEC>
@@ -568,15 +623,16 @@ cudaError_t configure_dtype() {
 
 // Stages: 4 for ranks up to 32 (two CTAs per SM fit), else 3 (one CTA per SM).
 template <typename E>
-cudaError_t launch_stream_dtype(const ExpandArgs &a, int ks_max, int grid, cudaStream_t st) {
+cudaError_t launch_stream_dtype(const ExpandArgs &a, int ks_max, int grid, int tiles_grid,
+                                cudaStream_t st) {
     const int stages = ks_max <= 2 ? 4 : 3;
     const size_t smem = stream_smem_bytes(ks_max, stages);
     if (a.add) {
-        if (stages == 4) expand_stream_kernel<E, true, 4><<<grid, kSThreads, smem, st>>>(a);
-        else expand_stream_kernel<E, true, 3><<<grid, kSThreads, smem, st>>>(a);
+        if (stages == 4) expand_stream_kernel<E, true, 4><<<grid, kSThreads, smem, st>>>(a, tiles_grid);
+        else expand_stream_kernel<E, true, 3><<<grid, kSThreads, smem, st>>>(a, tiles_grid);
     } else {
-        if (stages == 4) expand_stream_kernel<E, false, 4><<<grid, kSThreads, smem, st>>>(a);
-        else expand_stream_kernel<E, false, 3><<<grid, kSThreads, smem, st>>>(a);
+        if (stages == 4) expand_stream_kernel<E, false, 4><<<grid, kSThreads, smem, st>>>(a, tiles_grid);
+        else expand_stream_kernel<E, false, 3><<<grid, kSThreads, smem, st>>>(a, tiles_grid);
     }
     return cudaGetLastError();
 }
@@ -628,10 +684,11 @@ cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceI
     if (vec && b_vec_all) {
         // persistent grid: every CTA streams a contiguous range of units
         const int per_sm = stream_smem_bytes(ks_max, ks_max <= 2 ? 4 : 3) * 2 <= 227 * 1024 ? 2 : 1;
-        const long long units = std::min<long long>(est, a.max_tiles) * chunks;
+        const int tiles_grid = (int)std::min<long long>(est, a.max_tiles);
+        const long long units = (long long)tiles_grid * chunks;
         const int grid = (int)std::max<long long>(1, std::min<long long>(units, (long long)per_sm * dev.sm_count));
-        return dt == LORA_F16 ? launch_stream_dtype<__half>(a, ks_max, grid, stream)
-                              : launch_stream_dtype<__nv_bfloat16>(a, ks_max, grid, stream);
+        return dt == LORA_F16 ? launch_stream_dtype<__half>(a, ks_max, grid, tiles_grid, stream)
+                              : launch_stream_dtype<__nv_bfloat16>(a, ks_max, grid, tiles_grid, stream);
     }
     const int gx = (int)std::min<long long>(est, a.max_tiles);
     dim3 grid(std::max(gx, 1), chunks);

@@ -233,11 +233,20 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
         for (int it = threadIdx.x; it < my_rows * nrows; it += kThreads) {
             const int i = kc + ksplit * (it / nrows), c = it % nrows;
             const int row = s_rows[i];
-            float sum = 0.f;
-            for (int r = 0; r < ksplit; ++r) {
-                const float *src = ksplit > 1 ? cluster.map_shared_rank(sRed, r) : sRed;
-                sum += src[i * kRedPitch + c];
+            // all ranks' partials are loaded at once, then added in rank order
+            float part[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                part[r] = 0.f;
+                if (r < ksplit) {
+                    const float *src = ksplit > 1 ? cluster.map_shared_rank(sRed, r) : sRed;
+                    part[r] = src[i * kRedPitch + c];
+                }
             }
+            float sum = 0.f;
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                if (r < ksplit) sum += part[r];
             if (row >= 0) {
                 float *yp = a.y + (int64_t)row * a.ldy + s_arow[c];
                 const float v = a.scale * sum;
