@@ -169,16 +169,12 @@ def make_pool(dev, rank: int, l2_bytes: int, only_T=None):
     return pool, nsets * per_set
 
 
-def run_step(lg, batches, ev=None):
-    for i, b in enumerate(batches):
+def run_step(lg, batches):
+    for b in batches:
         lg.lora_group_tokens(b["idx"], L, b["plan"])
         lg.lora_shrink(b["x"], b["A"], b["y"], b["plan"], num_slices=len(SLICES))
-        if ev is not None:
-            ev[i][0].record()
         lg.lora_expand_slice(b["y"], b["B"], b["out"], b["plan"], b["case"].slice_offsets,
                              y_slice_stride=R, add_inputs=True)
-        if ev is not None:
-            ev[i][1].record()
 
 
 def e2e_run(lg, dev, steps: int, warmup: int):
@@ -254,37 +250,26 @@ def cpu_baseline(target_s: float = 10.0):
                       f"fp64 C loops, OpenMP over tokens, {el:.1f} s"}
 
 
-def _timing_event(external: bool):
-    if external:
-        return torch.cuda.Event(enable_timing=True, external=True)
-    return torch.cuda.Event(enable_timing=True)
-
-
 def capture_steps(lg, pool):
     """One CUDA graph per pool set holding a whole step (launch overhead off
-    the timed path, as the pages time their kernels).  Timing events bracket
-    every expand_slice inside the graph when torch can record graph event
-    nodes; the last replay of each graph leaves its durations behind."""
+    the timed path, as the pages time their kernels).  The graphs hold no
+    event nodes: on this GPU an event-record node costs several microseconds,
+    far more than the decode kernels themselves."""
     graphs = []
-    try:
-        _timing_event(True)
-        external = True
-    except TypeError:
-        external = False
     stream = torch.cuda.Stream()
     for batches in pool:
         g = torch.cuda.CUDAGraph()
-        ev = [[_timing_event(True), _timing_event(True)] for _ in batches] if external else None
         with torch.cuda.graph(g, stream=stream):
-            run_step(lg, batches, ev)
-        graphs.append((g, ev))
+            run_step(lg, batches)
+        graphs.append(g)
     torch.cuda.synchronize()
-    return graphs, external
+    return graphs
 
 
 def expand_only_ms(lg, pool, reps: int = 20):
-    """Fallback timing of expand_slice alone: a graph of one launch per pool
-    set for every batch size, replayed `reps` times between two events."""
+    """Average duration of expand_slice per batch size: a graph of one launch
+    per pool set (each on a different set, so inputs come from HBM), replayed
+    `reps` times between two events on the launching stream."""
     res = []
     stream = torch.cuda.Stream()
     for i in range(len(li.DECODE_T)):
@@ -322,9 +307,9 @@ def main_ours(args):
     for w in range(max(W, 1)):  # eager warm-up also configures the kernels before capture
         run_step(lg, pool[w % nsets])
     torch.cuda.synchronize()
-    graphs, in_graph_events = capture_steps(lg, pool)
+    graphs = capture_steps(lg, pool)
     for w in range(W):
-        graphs[w % nsets][0].replay()
+        graphs[w % nsets].replay()
     torch.cuda.synchronize()
 
     nb = len(li.DECODE_T)
@@ -340,7 +325,7 @@ def main_ours(args):
     wall0 = time.perf_counter()
     start.record()
     for k in range(K):
-        graphs[(W + k) % nsets][0].replay()
+        graphs[(W + k) % nsets].replay()
     end.record()
     torch.cuda.synchronize()
     if ws > 1:
@@ -349,14 +334,10 @@ def main_ours(args):
     clk = clocks.stop()
 
     ms = start.elapsed_time(end)
-    if in_graph_events:
-        # durations of every batch's expand_slice in the last replay of each pool set
-        ex_ms = [statistics.fmean(graphs[p][1][i][0].elapsed_time(graphs[p][1][i][1])
-                                  for p in range(nsets)) for i in range(nb)]
-        ex_src = f"CUDA events inside the step graphs (last replay of each of {nsets} sets)"
-    else:
-        ex_ms = expand_only_ms(lg, pool)
-        ex_src = "CUDA events around a graph of expand_slice launches over the pool"
+    # dominant kernel, timed right after the step loop on the same stream
+    ex_ms = expand_only_ms(lg, pool)
+    ex_src = (f"CUDA events around graphs of back-to-back expand_slice launches, one per "
+              f"pool set ({nsets} sets, inputs from HBM), per batch size")
     if ws > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
