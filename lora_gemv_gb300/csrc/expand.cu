@@ -306,288 +306,254 @@ expand_kernel(const ExpandArgs a) {
 }
 
 // ---------------------------------------------------------------------------
-// Streaming expand (the fast path: 16-byte aligned out columns and B rows).
+// Warp-streaming expand: the fast path (16-byte aligned out columns, R % 8 == 0).
 //
-// A persistent grid walks "units" (plan tile x 128-column chunk) in a
-// contiguous range per CTA, tile-major, so consecutive units share the
-// tile's token rows and y.  Each unit's out tile (gathered rows) and B tile
-// are copied into shared memory by cp.async, STAGES units ahead, so every
-// SM keeps ~100 KB of HBM reads in flight; results are stored straight from
-// registers with 16-byte stores.  y is converted to scaled hi/lo pairs only
-// when the unit's (tile, slice) changes.
-constexpr int kSThreads = 256;          // 8 warps: 4 column blocks x 2 row halves
-constexpr int kOutPitch = kCols + 8;    // elements per shared row of the out tile (272 B)
+// Every warp works alone: no shared memory, no block barriers.  A warp unit
+// is (plan tile, 32-row half of the tile, 32-column block of one slice); the
+// units are split in contiguous, tile-major ranges over all warps of a
+// persistent grid, so a warp's consecutive units share their token rows and,
+// within one slice, their y fragments (kept in registers).
+//
+// Operands go straight from global memory into mma.sync fragments.  The
+// contraction index is permuted so that each thread's slots of one 16-wide
+// k step, {2q, 2q+1, 2q+8, 2q+9}, are the 4 consecutive ranks 4q..4q+3: the
+// thread reads 8 contiguous bytes of a B row and 16 contiguous bytes of a y
+// row per k step.  The output columns are permuted the same way (n-tile i,
+// column c -> 8*(c/2) + 2i + c%2), so each thread's accumulators are 8
+// contiguous output columns: out is read and written with 16-byte accesses.
+// With ~20 warps per SM, each holding 64 bytes of out reads and the B / y
+// reads of its unit in flight, the SM keeps enough HBM traffic outstanding
+// (plain loads sustain ~7 TB/s on this part; cp.async and small bulk copies
+// measured far lower).
+constexpr int kWThreads = 128;  // 4 independent warps per CTA
+constexpr int kWCols = 32;      // output columns per warp unit
+// Token rows per warp unit: MB m16 blocks, MB = 2 for ranks <= 64 and 1 above
+// (the y fragments of a unit live in registers).
+__host__ __device__ constexpr int warp_mb(int ksmax) { return ksmax >= 8 ? 1 : 2; }
 
-__host__ __device__ constexpr int stream_stage_bytes(int ks_max) {
-    return kTile * kOutPitch * 2 + kCols * pitch_of(ks_max) * 2;
-}
-__host__ __device__ constexpr int stream_smem_bytes(int ks_max, int stages) {
-    return stages * stream_stage_bytes(ks_max) + 2 * kTile * pitch_of(ks_max) * 2 +
-           kTile * (int)sizeof(float);
-}
-
-constexpr int kWin = 8;  // plan tiles whose metadata a CTA holds in shared memory at once
-
-struct UnitInfo {
-    int w;               // tile slot in the CTA's window
-    int l, p0, n;        // tile: adapter, first perm position, tokens
-    int s, n0, ncols;    // chunk: slice, first column in the slice, columns
-    int rl;              // adapter rank (0 = nothing to add)
-};
-
-// Shared per-window plan metadata: tile records and their token rows.
-struct WinMeta {
-    int4 tile[kWin];          // {adapter, p0, n, rank}
-    int rows[kWin][kTile];    // out row of every token of the tile, -1 if none
-};
-
-__device__ __forceinline__ UnitInfo unit_info(const ExpandArgs &a, const WinMeta &wm, int u,
-                                              int t_first, int nchunks) {
-    UnitInfo ui;
-    const int t = u / nchunks, c = u - t * nchunks;
-    ui.w = t - t_first;
-    const int4 tl = wm.tile[ui.w];
-    ui.l = tl.x;
-    ui.p0 = tl.y;
-    ui.n = tl.z;
-    ui.rl = tl.w;
-    int s = 0;
-    while (s + 1 < a.num_slices && c >= a.chunk_begin[s + 1]) ++s;
-    ui.s = s;
-    ui.n0 = (c - a.chunk_begin[s]) * kCols;
-    ui.ncols = min(kCols, a.N[s] - ui.n0);
-    return ui;
+template <typename E>
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+    E lo = Elem<E>::from_f(a), hi = Elem<E>::from_f(b);
+    return (uint32_t)(*reinterpret_cast<uint16_t *>(&lo)) |
+           ((uint32_t)(*reinterpret_cast<uint16_t *>(&hi)) << 16);
 }
 
-// (tile, slice) of unit u differs from that of unit u-1 (or u is the first).
-__device__ __forceinline__ bool new_y(const ExpandArgs &a, int u, int u_first, int nchunks) {
-    if (u == u_first) return true;
-    const int t = u / nchunks, c = u - t * nchunks;
-    if (c == 0) return true;
-    for (int s = 1; s < a.num_slices; ++s)
-        if (c == a.chunk_begin[s]) return true;
-    return false;
+// Power-of-two factor 2^k as a float, k in [-126, 127].
+__device__ __forceinline__ float exp2i(int k) { return __int_as_float((127 + k) << 23); }
+
+// Per-row exponent e with max|y_row| * 2^-e < 1 (frexp-style), clamped.
+__device__ __forceinline__ int row_exponent(float m) {
+    const int be = (__float_as_int(m) >> 23) & 0xff;
+    return min(max(be - 126, -125), 126);
 }
 
-template <typename E, bool ADD>
-__device__ __forceinline__ void stream_issue(const ExpandArgs &a, const WinMeta &wm,
-                                             const UnitInfo &ui, unsigned char *stage, int pitch) {
-    if (ui.rl == 0) return;
-    E *sOut = reinterpret_cast<E *>(stage);
-    E *sB = reinterpret_cast<E *>(stage + kTile * kOutPitch * 2);
-    const E *out = static_cast<const E *>(a.out);
-    const int64_t col0 = (int64_t)a.off[ui.s] + ui.n0;
-    if (ADD) {  // 4 threads per token row, 4 x 16 bytes each
-        const int i = threadIdx.x >> 2, ch0 = (threadIdx.x & 3) * 4;
-        const int row = wm.rows[ui.w][i];
-        if (row >= 0) {
-            const E *src = out + (int64_t)row * a.ldo + col0;
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if ((ch0 + k) * 8 < ui.ncols)
-                    cp_async16(smem_u32(sOut + i * kOutPitch + (ch0 + k) * 8), src + (ch0 + k) * 8, 16);
-        }
-    }
-    const int KS = (ui.rl + 15) / 16;
-    const E *Bl = static_cast<const E *>(a.B[ui.s]) + ((int64_t)ui.l * a.N[ui.s] + ui.n0) * a.R;
-    for (int it = threadIdx.x; it < kCols * 2 * KS; it += kSThreads) {
-        const int j = it / (2 * KS), c8 = (it - j * 2 * KS) * 8;
-        const int nv = j < ui.ncols ? min(8, ui.rl - c8) : 0;
-        const E *src = nv > 0 ? Bl + (int64_t)j * a.R + c8 : Bl;
-        cp_async16(smem_u32(sB + sigma(j) * pitch + c8), src, nv > 0 ? 2 * nv : 0);
-    }
-}
-
-template <typename E, bool ADD, int STAGES>
-__global__ void __launch_bounds__(kSThreads, 1)
-expand_stream_kernel(const ExpandArgs a, int tiles_grid) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ WinMeta wm;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+template <typename E, bool ADD, int KSMAX>
+__global__ void __launch_bounds__(kWThreads)
+expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb) {
+    constexpr int MB = warp_mb(KSMAX);
+    constexpr int kWRows = 16 * MB;
+    constexpr int kParts = kTile / kWRows;  // row parts per tile
+    const int lane = threadIdx.x & 31;
     const int g = lane >> 2, q = lane & 3;
-    const int cb = warp & 3, rh = warp >> 2;  // 32-column block, 32-row half
+    const int gwarp = blockIdx.x * (kWThreads / 32) + (threadIdx.x >> 5);
+    const int nwarps = gridDim.x * (kWThreads / 32);
 
-    // Units (tile x chunk, tile-major) are split over the grid by the host's
-    // tile bound, so the first window's tile records load with the header.
-    const int nchunks = a.chunk_begin[a.num_slices];
-    const int U_grid = tiles_grid * nchunks;
-    const int per = (U_grid + gridDim.x - 1) / gridDim.x;
-    const int u_begin = blockIdx.x * per;
+    // units (tile, row part, column block), tile-major; ranges use the host's
+    // tile bound so the first tile record loads together with the header
+    const int per_tile = kParts * ncb;
+    const int U_grid = tiles_grid * per_tile;
+    const int per = (U_grid + nwarps - 1) / nwarps;
+    const int u_begin = gwarp * per;
     const int4 h0 = __ldg(reinterpret_cast<const int4 *>(a.hdr));
     const int4 h1 = __ldg(reinterpret_cast<const int4 *>(a.hdr) + 1);
-    int4 tl_first = make_int4(-1, 0, 0, 0);
-    if (threadIdx.x < kWin) {
-        const int t = u_begin / nchunks + threadIdx.x;
-        if (t < a.max_tiles) tl_first = __ldg(a.tiles + t);
-    }
+    int4 tl = u_begin / per_tile < a.max_tiles ? __ldg(a.tiles + u_begin / per_tile)
+                                               : make_int4(-1, 0, 0, 0);
     if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
         return;
     }
     const int n_tiles = min(h1.z, a.max_tiles);
-    const int u_end = min(n_tiles * nchunks, u_begin + per);
-
-    const int ks_max = (a.R + 15) / 16;
-    const int pitch = pitch_of(ks_max);
-    const int sbytes = stream_stage_bytes(ks_max);
-    E *sYh = reinterpret_cast<E *>(smem + STAGES * sbytes);
-    E *sYl = sYh + kTile * pitch;
-    float *sF = reinterpret_cast<float *>(sYl + kTile * pitch);
+    const int u_end = min(n_tiles * per_tile, u_begin + per);
     E *__restrict__ out = static_cast<E *>(a.out);
+    const int R = a.R;
 
-    for (int u0 = u_begin; u0 < u_end;) {
-        // ---- window: up to kWin tiles, metadata into shared memory
-        const int t_first = u0 / nchunks;
-        const int u1 = min(u_end, (t_first + kWin) * nchunks);
-        if (threadIdx.x < kWin) {
-            int4 tl = tl_first;
-            if (u0 != u_begin) {
-                const int t = t_first + threadIdx.x;
-                tl = t < n_tiles ? __ldg(a.tiles + t) : make_int4(-1, 0, 0, 0);
-            }
-            const int t = t_first + threadIdx.x;
-            if (t >= n_tiles) tl = make_int4(-1, 0, 0, 0);
-            const int rl = tl.x >= 0 && tl.x < a.L ? clamp_rank(a.ranks, tl.x, a.R) : 0;
-            wm.tile[threadIdx.x] = make_int4(tl.x, tl.y, tl.z, rl);
-        }
-        __syncthreads();
-        for (int it = threadIdx.x; it < kWin * kTile; it += kSThreads) {
-            const int w = it / kTile, i = it - w * kTile;
-            const int4 tl = wm.tile[w];
-            int row = -1;
-            if (i < tl.z) {
-                row = __ldg(a.perm + tl.y + i);
-                if (row < 0 || row >= a.T) row = -1;
-            }
-            wm.rows[w][i] = row;
-        }
-        __syncthreads();
+    int cur_t = -1, cur_half = -1, cur_s = -1;
+    int rows[MB][2];         // [m16 block][g / g+8] out row, -1 if none
+    int rl = 0, KS = 0, nrow = 0;
+    float fscale[MB][2];     // scale * 2^e per row
+    uint32_t ah[MB][KSMAX][4], al[MB][KSMAX][4];  // y fragments (hi, lo)
 
-        // ---- pipelined units of the window
+    for (int u = u_begin; u < u_end; ++u) {
+        const int t = u / per_tile, rem = u - t * per_tile;
+        const int half = rem / ncb, cbi = rem - half * ncb;
+        if (t != cur_t) {
+            if (cur_t >= 0) tl = __ldg(a.tiles + t);
+            rl = tl.x >= 0 && tl.x < a.L ? clamp_rank(a.ranks, tl.x, R) : 0;
+            KS = (rl + 15) / 16;
+            cur_half = -1;
+        }
+        // column block -> slice and columns
+        int s = 0;
+        while (s + 1 < a.num_slices && cbi >= a.chunk_begin[s + 1]) ++s;
+        const int c0 = (cbi - a.chunk_begin[s]) * kWCols;       // first column within the slice
+        const int Ns = a.N[s];
+        const int64_t col = (int64_t)a.off[s] + c0 + 8 * q;     // this thread's 8 columns
+        const bool col_ok = c0 + 8 * q < Ns;
+        if (t != cur_t || half != cur_half) {
+            nrow = min(kWRows, tl.z - half * kWRows);
 #pragma unroll
-        for (int k = 0; k < STAGES - 1; ++k) {
-            if (u0 + k < u1)
-                stream_issue<E, ADD>(a, wm, unit_info(a, wm, u0 + k, t_first, nchunks),
-                                     smem + k * sbytes, pitch);
-            cp_async_commit();
-        }
-        for (int u = u0; u < u1; ++u) {
-            cp_async_wait<STAGES - 2>();
-            __syncthreads();
-            const int nxt = u + STAGES - 1;
-            if (nxt < u1)
-                stream_issue<E, ADD>(a, wm, unit_info(a, wm, nxt, t_first, nchunks),
-                                     smem + ((nxt - u0) % STAGES) * sbytes, pitch);
-            cp_async_commit();
-
-            const UnitInfo ui = unit_info(a, wm, u, t_first, nchunks);
-            const int *rows = wm.rows[ui.w];
-            const int64_t col0 = (int64_t)a.off[ui.s] + ui.n0;
-            if (ui.rl == 0) {  // adapter -1 or rank 0: nothing to add; without add_inputs, zeros
-                if (!ADD) {
-                    const int i = threadIdx.x >> 2, ch0 = (threadIdx.x & 3) * 4;
-                    const int row = rows[i];
-                    if (row >= 0) {
+            for (int mm = 0; mm < MB; ++mm)
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            if ((ch0 + k) * 8 < ui.ncols)
-                                st_global_v4(out + (int64_t)row * a.ldo + col0 + (ch0 + k) * 8,
-                                             make_uint4(0, 0, 0, 0));
+                for (int h = 0; h < 2; ++h) {
+                    const int i = half * kWRows + mm * 16 + g + 8 * h;
+                    int row = -1;
+                    if (i < tl.z) {
+                        row = __ldg(a.perm + tl.y + i);
+                        if (row < 0 || row >= a.T) row = -1;
                     }
+                    rows[mm][h] = row;
                 }
-                continue;
+            cur_s = -1;
+        }
+        cur_t = t;
+        cur_half = half;
+        if (nrow <= 0) continue;  // half without tokens
+
+        if (rl == 0) {  // adapter -1 or rank 0: untouched with add_inputs, zeros without
+            if (!ADD && col_ok) {
+#pragma unroll
+                for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (rows[mm][h] >= 0)
+                            st_global_v4(out + (int64_t)rows[mm][h] * a.ldo + col, make_uint4(0, 0, 0, 0));
             }
-            const int KS = (ui.rl + 15) / 16;
-            if (new_y(a, u, u0, nchunks)) {
-                // 4 threads per token row: scaled hi/lo pairs of y[row, s*ys : s*ys + r_l)
-                const int i = threadIdx.x >> 2, part = threadIdx.x & 3;
-                const int row = rows[i];
-                const bool live = row >= 0;
-                const float *yr = a.y + (int64_t)(live ? row : 0) * a.ldy +
-                                  (int64_t)ui.s * a.y_slice_stride;
-                const int j0 = part * KS * 4;
-                float v[LORA_MAX_RANK / 4];
-                float m = 0.f;
+            continue;
+        }
+
+        // 1) reads of out for this unit (issued first, consumed last)
+        uint4 old[MB][2];
+        if (ADD && col_ok) {
 #pragma unroll
-                for (int k = 0; k < LORA_MAX_RANK / 4; ++k) {
-                    const int j = j0 + k;
-                    v[k] = (k < KS * 4 && live && j < ui.rl) ? yr[j] : 0.f;
-                    m = fmaxf(m, fabsf(v[k]));
-                }
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                int e = 0;
-                frexpf(m, &e);
+            for (int mm = 0; mm < MB; ++mm)
 #pragma unroll
-                for (int k = 0; k < LORA_MAX_RANK / 4; ++k) {
-                    if (k < KS * 4) {
-                        const float vs = ldexpf(v[k], -e);
-                        const E hi = Elem<E>::from_f(vs);
-                        sYh[i * pitch + j0 + k] = hi;
-                        sYl[i * pitch + j0 + k] = Elem<E>::from_f(vs - Elem<E>::to_f(hi));
+                for (int h = 0; h < 2; ++h)
+                    if (rows[mm][h] >= 0) old[mm][h] = ld_global_v4(out + (int64_t)rows[mm][h] * a.ldo + col);
+        }
+
+        // 2) B fragments: row n = c0 + 8*(g/2) + 2i + g%2 of this slice, ranks 16ks + 4q .. +3
+        const E *Bs = static_cast<const E *>(a.B[s]);
+        uint2 bf[KSMAX][4];
+#pragma unroll
+        for (int ks = 0; ks < KSMAX; ++ks)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                bf[ks][i] = make_uint2(0, 0);
+                const int n = c0 + 8 * (g >> 1) + 2 * i + (g & 1);
+                const int k = ks * 16 + 4 * q;
+                if (ks < KS && n < Ns && k < rl) {
+                    uint2 v = __ldg(reinterpret_cast<const uint2 *>(Bs + ((int64_t)tl.x * Ns + n) * R + k));
+                    const int nv = rl - k;  // valid ranks among these 4
+                    if (nv < 4) {
+                        if (nv < 2) v.x &= 0xffffu;
+                        v.y = nv < 3 ? 0u : (v.y & 0xffffu);
+                        if (nv < 1) v.x = 0u;
                     }
+                    bf[ks][i] = v;
                 }
-                if (part == 0) sF[i] = ldexpf(a.scale, e);
-                __syncthreads();
             }
 
-            const unsigned char *stage = smem + ((u - u0) % STAGES) * sbytes;
-            const E *sOut = reinterpret_cast<const E *>(stage);
-            const E *sB = reinterpret_cast<const E *>(stage + kTile * kOutPitch * 2);
-            const int wcol = cb * 32 + q * 8;
-            if (cb * 32 < ui.ncols) {
+        // 3) y fragments for (tile, half, slice), scaled per row by a power of two
+        if (s != cur_s) {
+            cur_s = s;
+            const float *yb = a.y + (int64_t)s * a.y_slice_stride;
+            float yv[MB][2][KSMAX][4];
+            float m[MB][2];
 #pragma unroll
-                for (int mm = 0; mm < 2; ++mm) {
-                    const int mb = rh * 2 + mm;
-                    if (mb * 16 >= ui.n) break;
-                    float acc[4][4];
+            for (int mm = 0; mm < MB; ++mm)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
+                for (int h = 0; h < 2; ++h) {
+                    m[mm][h] = 0.f;
+                    const int row = rows[mm][h];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
-                    for (int ks = 0; ks < KS; ++ks) {
-                        uint32_t ah[4], al[4];
-                        const int arow = mb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-                        const int acol = ks * 16 + 8 * (lane >> 4);
-                        ldmatrix_x4(ah, smem_u32(sYh + arow * pitch + acol));
-                        ldmatrix_x4(al, smem_u32(sYl + arow * pitch + acol));
+                    for (int ks = 0; ks < KSMAX; ++ks)
 #pragma unroll
-                        for (int np = 0; np < 2; ++np) {
-                            uint32_t b[4];
-                            const int brow = cb * 32 + 8 * (2 * np + (lane >> 4)) + (lane & 7);
-                            const int bcol = ks * 16 + 8 * ((lane >> 3) & 1);
-                            ldmatrix_x4(b, smem_u32(sB + brow * pitch + bcol));
-                            mma16816<E>(acc[2 * np], ah, b[0], b[1]);
-                            mma16816<E>(acc[2 * np], al, b[0], b[1]);
-                            mma16816<E>(acc[2 * np + 1], ah, b[2], b[3]);
-                            mma16816<E>(acc[2 * np + 1], al, b[2], b[3]);
+                        for (int j = 0; j < 4; ++j) {
+                            const int k = ks * 16 + 4 * q + j;
+                            const float v = (row >= 0 && ks < KS && k < rl)
+                                                ? __ldg(yb + (int64_t)row * a.ldy + k) : 0.f;
+                            yv[mm][h][ks][j] = v;
+                            m[mm][h] = fmaxf(m[mm][h], fabsf(v));
                         }
+                }
+#pragma unroll
+            for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float mx = m[mm][h];
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                    const int e = row_exponent(mx);
+                    fscale[mm][h] = a.scale * exp2i(e);
+                    const float inv = exp2i(-e);
+#pragma unroll
+                    for (int ks = 0; ks < KSMAX; ++ks)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) yv[mm][h][ks][j] *= inv;
+                }
+#pragma unroll
+            for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+                for (int ks = 0; ks < KSMAX; ++ks)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        // a0: (row g, ranks 4q, 4q+1)  a1: (row g+8, 4q, 4q+1)
+                        // a2: (row g, 4q+2, 4q+3)     a3: (row g+8, 4q+2, 4q+3)
+                        const int h = r & 1, j = (r >> 1) * 2;
+                        const float v0 = yv[mm][h][ks][j], v1 = yv[mm][h][ks][j + 1];
+                        const float h0f = Elem<E>::to_f(Elem<E>::from_f(v0));
+                        const float h1f = Elem<E>::to_f(Elem<E>::from_f(v1));
+                        ah[mm][ks][r] = pack2<E>(h0f, h1f);
+                        al[mm][ks][r] = pack2<E>(v0 - h0f, v1 - h1f);
                     }
-                    if (wcol < ui.ncols) {
+        }
+
+        // 4) MMAs and epilogue, per 16-row block
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int i = mb * 16 + g + 8 * h;
-                            const int row = rows[i];
-                            if (row < 0) continue;
-                            const float f = sF[i];
-                            float res[8];
+        for (int mm = 0; mm < MB; ++mm) {
+            if (mm * 16 >= nrow) break;
+            float acc[4][4];
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) res[k] = f * acc[k >> 1][2 * h + (k & 1)];
-                            if (ADD) {
-                                float o[8];
-                                unpack8<E>(*reinterpret_cast<const uint4 *>(sOut + i * kOutPitch + wcol), o);
+            for (int i = 0; i < 4; ++i)
 #pragma unroll
-                                for (int k = 0; k < 8; ++k) res[k] += o[k];
-                            }
-                            st_global_v4(out + (int64_t)row * a.ldo + col0 + wcol, pack8<E>(res));
-                        }
+                for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KSMAX; ++ks) {
+                if (ks < KS) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        mma16816<E>(acc[i], ah[mm][ks], bf[ks][i].x, bf[ks][i].y);
+                        mma16816<E>(acc[i], al[mm][ks], bf[ks][i].x, bf[ks][i].y);
                     }
                 }
             }
+            if (!col_ok) continue;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int row = rows[mm][h];
+                if (row < 0) continue;
+                float res[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) res[k] = fscale[mm][h] * acc[k >> 1][2 * h + (k & 1)];
+                if (ADD) {
+                    float o[8];
+                    unpack8<E>(old[mm][h], o);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) res[k] += o[k];
+                }
+                st_global_v4(out + (int64_t)row * a.ldo + col, pack8<E>(res));
+            }
         }
-        cp_async_wait<0>();
-        __syncthreads();  // the window's shared metadata and stages are free again
-        u0 = u1;
     }
 }
 
@@ -599,53 +565,34 @@ cudaError_t configure_one() {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
-template <typename E, bool ADD, int STAGES>
-cudaError_t configure_stream_one() {
-    // 4 stages serve ranks <= 32, 3 stages any rank (see launch_stream_dtype)
-    return cudaFuncSetAttribute(expand_stream_kernel<E, ADD, STAGES>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                STAGES == 4 ? stream_smem_bytes(2, 4)
-                                            : stream_smem_bytes(LORA_MAX_RANK / 16, 3));
-}
-
 template <typename E>
 cudaError_t configure_dtype() {
     cudaError_t e;
     if ((e = configure_one<E, false, false>()) != cudaSuccess) return e;
-    if ((e = configure_one<E, false, true>()) != cudaSuccess) return e;
-    if ((e = configure_one<E, true, false>()) != cudaSuccess) return e;
-    if ((e = configure_one<E, true, true>()) != cudaSuccess) return e;
-    if ((e = configure_stream_one<E, false, 3>()) != cudaSuccess) return e;
-    if ((e = configure_stream_one<E, false, 4>()) != cudaSuccess) return e;
-    if ((e = configure_stream_one<E, true, 3>()) != cudaSuccess) return e;
-    return configure_stream_one<E, true, 4>();
+    return configure_one<E, true, false>();
 }
 
-// Stages: 4 for ranks up to 32 (two CTAs per SM fit), else 3 (one CTA per SM).
-template <typename E>
-cudaError_t launch_stream_dtype(const ExpandArgs &a, int ks_max, int grid, int tiles_grid,
-                                cudaStream_t st) {
-    const int stages = ks_max <= 2 ? 4 : 3;
-    const size_t smem = stream_smem_bytes(ks_max, stages);
-    if (a.add) {
-        if (stages == 4) expand_stream_kernel<E, true, 4><<<grid, kSThreads, smem, st>>>(a, tiles_grid);
-        else expand_stream_kernel<E, true, 3><<<grid, kSThreads, smem, st>>>(a, tiles_grid);
-    } else {
-        if (stages == 4) expand_stream_kernel<E, false, 4><<<grid, kSThreads, smem, st>>>(a, tiles_grid);
-        else expand_stream_kernel<E, false, 3><<<grid, kSThreads, smem, st>>>(a, tiles_grid);
-    }
+template <typename E, int KSMAX>
+cudaError_t launch_warp_ks(const ExpandArgs &a, int grid, int tiles_grid, int ncb, cudaStream_t st) {
+    if (a.add) expand_warp_kernel<E, true, KSMAX><<<grid, kWThreads, 0, st>>>(a, tiles_grid, ncb);
+    else expand_warp_kernel<E, false, KSMAX><<<grid, kWThreads, 0, st>>>(a, tiles_grid, ncb);
     return cudaGetLastError();
 }
 
 template <typename E>
-cudaError_t launch_dtype(const ExpandArgs &a, bool vec, dim3 grid, size_t smem, cudaStream_t st) {
-    if (a.add) {
-        if (vec) expand_kernel<E, true, true><<<grid, kThreads, smem, st>>>(a);
-        else expand_kernel<E, true, false><<<grid, kThreads, smem, st>>>(a);
-    } else {
-        if (vec) expand_kernel<E, false, true><<<grid, kThreads, smem, st>>>(a);
-        else expand_kernel<E, false, false><<<grid, kThreads, smem, st>>>(a);
-    }
+cudaError_t launch_warp_dtype(const ExpandArgs &a, int grid, int tiles_grid, int ncb,
+                              cudaStream_t st) {
+    const int ks = (a.R + 15) / 16;
+    if (ks <= 1) return launch_warp_ks<E, 1>(a, grid, tiles_grid, ncb, st);
+    if (ks <= 2) return launch_warp_ks<E, 2>(a, grid, tiles_grid, ncb, st);
+    if (ks <= 4) return launch_warp_ks<E, 4>(a, grid, tiles_grid, ncb, st);
+    return launch_warp_ks<E, 8>(a, grid, tiles_grid, ncb, st);
+}
+
+template <typename E>
+cudaError_t launch_dtype(const ExpandArgs &a, dim3 grid, size_t smem, cudaStream_t st) {
+    if (a.add) expand_kernel<E, true, false><<<grid, kThreads, smem, st>>>(a);
+    else expand_kernel<E, false, false><<<grid, kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -660,42 +607,45 @@ cudaError_t configure_expand_kernels() {
 cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceInfo &dev,
                           cudaStream_t stream) {
     ExpandArgs a = a_in;
+    if (a.T == 0) return cudaSuccess;
+    // Tiles: ceil(T/64) full-or-partial tiles plus at most one ragged tile per
+    // adapter and one for the inactive tokens; kernels loop if a plan has more.
+    const long long est = (a.T + kTile - 1) / kTile + (long long)std::min(a.L, a.T) + 1;
+    const int tiles_grid = (int)std::max<long long>(1, std::min<long long>(est, a.max_tiles));
+
+    // Fast path: every 8-column group of every slice 16-byte aligned, B rows 16-byte aligned.
+    bool vec = (reinterpret_cast<uintptr_t>(a.out) & 15) == 0 && a.ldo % 8 == 0 && a.R % 8 == 0;
+    for (int s = 0; s < a.num_slices; ++s)
+        vec = vec && a.off[s] % 8 == 0 && a.N[s] % 8 == 0 &&
+              (reinterpret_cast<uintptr_t>(a.B[s]) & 15) == 0;
+    if (vec) {
+        // 32-column blocks per slice (prefix sums in chunk_begin)
+        a.chunk_begin[0] = 0;
+        for (int s = 0; s < a.num_slices; ++s)
+            a.chunk_begin[s + 1] = a.chunk_begin[s] + (a.N[s] + kWCols - 1) / kWCols;
+        for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s];
+        const int ncb = a.chunk_begin[a.num_slices];
+        if (ncb == 0) return cudaSuccess;
+        const long long units = (long long)tiles_grid * (kTile / (16 * warp_mb((a.R + 15) / 16 > 4 ? 8 : 1))) * ncb;
+        const long long warps_max = (long long)dev.sm_count * 20;  // ~20 resident warps per SM
+        const long long warps = std::min(units, warps_max);
+        const int grid = (int)std::max<long long>(1, (warps + 3) / 4);
+        return dt == LORA_F16 ? launch_warp_dtype<__half>(a, grid, tiles_grid, ncb, stream)
+                              : launch_warp_dtype<__nv_bfloat16>(a, grid, tiles_grid, ncb, stream);
+    }
+
+    // Generic path: 128-column chunks per slice
     a.chunk_begin[0] = 0;
     for (int s = 0; s < a.num_slices; ++s)
         a.chunk_begin[s + 1] = a.chunk_begin[s] + (a.N[s] + kCols - 1) / kCols;
     for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s];
     const int chunks = a.chunk_begin[a.num_slices];
-    if (chunks == 0 || a.T == 0) return cudaSuccess;
-
-    // Vector path: every 8-column group of every slice is 16-byte aligned.
-    bool vec = (reinterpret_cast<uintptr_t>(a.out) & 15) == 0 && a.ldo % 8 == 0;
-    for (int s = 0; s < a.num_slices; ++s) vec = vec && a.off[s] % 8 == 0 && a.N[s] % 8 == 0;
-
-    // Tiles: ceil(T/64) full-or-partial tiles plus at most one ragged tile per
-    // adapter and one for the inactive tokens; CTAs loop if a plan has more.
-    const long long est = (a.T + kTile - 1) / kTile + (long long)std::min(a.L, a.T) + 1;
-    const int ks_max = (a.R + 15) / 16;
-    const bool b_vec_all = [&] {
-        if (a.R % 8 != 0) return false;
-        for (int s = 0; s < a.num_slices; ++s)
-            if (reinterpret_cast<uintptr_t>(a.B[s]) & 15) return false;
-        return true;
-    }();
-    if (vec && b_vec_all) {
-        // persistent grid: every CTA streams a contiguous range of units
-        const int per_sm = stream_smem_bytes(ks_max, ks_max <= 2 ? 4 : 3) * 2 <= 227 * 1024 ? 2 : 1;
-        const int tiles_grid = (int)std::min<long long>(est, a.max_tiles);
-        const long long units = (long long)tiles_grid * chunks;
-        const int grid = (int)std::max<long long>(1, std::min<long long>(units, (long long)per_sm * dev.sm_count));
-        return dt == LORA_F16 ? launch_stream_dtype<__half>(a, ks_max, grid, tiles_grid, stream)
-                              : launch_stream_dtype<__nv_bfloat16>(a, ks_max, grid, tiles_grid, stream);
-    }
-    const int gx = (int)std::min<long long>(est, a.max_tiles);
-    dim3 grid(std::max(gx, 1), chunks);
+    if (chunks == 0) return cudaSuccess;
+    dim3 grid(tiles_grid, chunks);
     const int ks = (a.R + 15) / 16;
     const size_t smem = (size_t)(kCols + 2 * kTile) * pitch_of(ks) * 2 + kTile * sizeof(float);
-    return dt == LORA_F16 ? launch_dtype<__half>(a, vec, grid, smem, stream)
-                          : launch_dtype<__nv_bfloat16>(a, vec, grid, smem, stream);
+    return dt == LORA_F16 ? launch_dtype<__half>(a, grid, smem, stream)
+                          : launch_dtype<__nv_bfloat16>(a, grid, smem, stream);
 }
 
 }  // namespace lora
