@@ -347,9 +347,69 @@ __device__ __forceinline__ int row_exponent(float m) {
     return min(max(be - 126, -125), 126);
 }
 
+template <typename E> struct Pack;
+template <> struct Pack<__half> {
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    static __device__ __forceinline__ float2 unpack(uint32_t w) {
+        return __half22float2(*reinterpret_cast<__half2 *>(&w));
+    }
+};
+template <> struct Pack<__nv_bfloat16> {
+    static __device__ __forceinline__ uint32_t pack(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    static __device__ __forceinline__ float2 unpack(uint32_t w) {
+        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w));
+    }
+};
+
+// Loads of one warp unit that are issued a unit ahead.
+template <int MB, int KSMAX>
+struct UnitLoads {
+    uint4 old[MB][2];     // out[row][8 columns] for rows g, g+8 of each m16 block
+    uint2 bf[KSMAX][4];   // B fragments per k step and n-tile
+};
+
+template <typename E, bool ADD, int MB, int KSMAX>
+__device__ __forceinline__ void issue_unit(const ExpandArgs &a, UnitLoads<MB, KSMAX> &ld,
+                                           const int (&rows)[MB][2], int l, int rl, int KS,
+                                           int s, int c0, int64_t col, bool col_ok, int g, int q) {
+    const E *out = static_cast<const E *>(a.out);
+    if (ADD && col_ok) {
+#pragma unroll
+        for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (rows[mm][h] >= 0) ld.old[mm][h] = ld_global_v4(out + (int64_t)rows[mm][h] * a.ldo + col);
+    }
+    const int Ns = a.N[s];
+    const E *Bl = static_cast<const E *>(a.B[s]) + (int64_t)l * Ns * a.R;
+#pragma unroll
+    for (int ks = 0; ks < KSMAX; ++ks)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ld.bf[ks][i] = make_uint2(0, 0);
+            const int n = c0 + 8 * (g >> 1) + 2 * i + (g & 1);
+            const int k = ks * 16 + 4 * q;
+            if (ks < KS && n < Ns && k < rl) {
+                uint2 v = __ldg(reinterpret_cast<const uint2 *>(Bl + (int64_t)n * a.R + k));
+                const int nv = rl - k;  // valid ranks among these 4
+                if (nv < 4) {
+                    v.y = nv <= 2 ? 0u : (v.y & 0xffffu);
+                    if (nv < 2) v.x &= 0xffffu;
+                }
+                ld.bf[ks][i] = v;
+            }
+        }
+}
+
 template <typename E, bool ADD, int KSMAX>
 __global__ void __launch_bounds__(kWThreads)
-expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb) {
+expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     constexpr int MB = warp_mb(KSMAX);
     constexpr int kWRows = 16 * MB;
     constexpr int kParts = kTile / kWRows;  // row parts per tile
@@ -366,194 +426,237 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb) {
     const int u_begin = gwarp * per;
     const int4 h0 = __ldg(reinterpret_cast<const int4 *>(a.hdr));
     const int4 h1 = __ldg(reinterpret_cast<const int4 *>(a.hdr) + 1);
-    int4 tl = u_begin / per_tile < a.max_tiles ? __ldg(a.tiles + u_begin / per_tile)
-                                               : make_int4(-1, 0, 0, 0);
+    int t = u_begin / per_tile;
+    int4 tl = t < a.max_tiles ? __ldg(a.tiles + t) : make_int4(-1, 0, 0, 0);
     if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
         if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
         return;
     }
     const int n_tiles = min(h1.z, a.max_tiles);
     const int u_end = min(n_tiles * per_tile, u_begin + per);
+    if (u_begin >= u_end) return;
     E *__restrict__ out = static_cast<E *>(a.out);
-    const int R = a.R;
 
-    int cur_t = -1, cur_half = -1, cur_s = -1;
-    int rows[MB][2];         // [m16 block][g / g+8] out row, -1 if none
+    // position of the current unit
+    int part = (u_begin - t * per_tile) / ncb;
+    int cbi = u_begin - t * per_tile - part * ncb;
+
+    // per (tile, part) state
+    int rows[MB][2];
     int rl = 0, KS = 0, nrow = 0;
-    float fscale[MB][2];     // scale * 2^e per row
-    uint32_t ah[MB][KSMAX][4], al[MB][KSMAX][4];  // y fragments (hi, lo)
-
-    for (int u = u_begin; u < u_end; ++u) {
-        const int t = u / per_tile, rem = u - t * per_tile;
-        const int half = rem / ncb, cbi = rem - half * ncb;
-        if (t != cur_t) {
-            if (cur_t >= 0) tl = __ldg(a.tiles + t);
-            rl = tl.x >= 0 && tl.x < a.L ? clamp_rank(a.ranks, tl.x, R) : 0;
-            KS = (rl + 15) / 16;
-            cur_half = -1;
-        }
-        // column block -> slice and columns
-        int s = 0;
-        while (s + 1 < a.num_slices && cbi >= a.chunk_begin[s + 1]) ++s;
-        const int c0 = (cbi - a.chunk_begin[s]) * kWCols;       // first column within the slice
-        const int Ns = a.N[s];
-        const int64_t col = (int64_t)a.off[s] + c0 + 8 * q;     // this thread's 8 columns
-        const bool col_ok = c0 + 8 * q < Ns;
-        if (t != cur_t || half != cur_half) {
-            nrow = min(kWRows, tl.z - half * kWRows);
+    auto load_rows = [&](const int4 &tile, int pt, int (&r)[MB][2]) {
 #pragma unroll
-            for (int mm = 0; mm < MB; ++mm)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int i = half * kWRows + mm * 16 + g + 8 * h;
-                    int row = -1;
-                    if (i < tl.z) {
-                        row = __ldg(a.perm + tl.y + i);
-                        if (row < 0 || row >= a.T) row = -1;
-                    }
-                    rows[mm][h] = row;
-                }
-            cur_s = -1;
-        }
-        cur_t = t;
-        cur_half = half;
-        if (nrow <= 0) continue;  // half without tokens
-
-        if (rl == 0) {  // adapter -1 or rank 0: untouched with add_inputs, zeros without
-            if (!ADD && col_ok) {
-#pragma unroll
-                for (int mm = 0; mm < MB; ++mm)
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        if (rows[mm][h] >= 0)
-                            st_global_v4(out + (int64_t)rows[mm][h] * a.ldo + col, make_uint4(0, 0, 0, 0));
-            }
-            continue;
-        }
-
-        // 1) reads of out for this unit (issued first, consumed last)
-        uint4 old[MB][2];
-        if (ADD && col_ok) {
-#pragma unroll
-            for (int mm = 0; mm < MB; ++mm)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    if (rows[mm][h] >= 0) old[mm][h] = ld_global_v4(out + (int64_t)rows[mm][h] * a.ldo + col);
-        }
-
-        // 2) B fragments: row n = c0 + 8*(g/2) + 2i + g%2 of this slice, ranks 16ks + 4q .. +3
-        const E *Bs = static_cast<const E *>(a.B[s]);
-        uint2 bf[KSMAX][4];
-#pragma unroll
-        for (int ks = 0; ks < KSMAX; ++ks)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                bf[ks][i] = make_uint2(0, 0);
-                const int n = c0 + 8 * (g >> 1) + 2 * i + (g & 1);
-                const int k = ks * 16 + 4 * q;
-                if (ks < KS && n < Ns && k < rl) {
-                    uint2 v = __ldg(reinterpret_cast<const uint2 *>(Bs + ((int64_t)tl.x * Ns + n) * R + k));
-                    const int nv = rl - k;  // valid ranks among these 4
-                    if (nv < 4) {
-                        if (nv < 2) v.x &= 0xffffu;
-                        v.y = nv < 3 ? 0u : (v.y & 0xffffu);
-                        if (nv < 1) v.x = 0u;
-                    }
-                    bf[ks][i] = v;
-                }
-            }
-
-        // 3) y fragments for (tile, half, slice), scaled per row by a power of two
-        if (s != cur_s) {
-            cur_s = s;
-            const float *yb = a.y + (int64_t)s * a.y_slice_stride;
-            float yv[MB][2][KSMAX][4];
-            float m[MB][2];
-#pragma unroll
-            for (int mm = 0; mm < MB; ++mm)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    m[mm][h] = 0.f;
-                    const int row = rows[mm][h];
-#pragma unroll
-                    for (int ks = 0; ks < KSMAX; ++ks)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const int k = ks * 16 + 4 * q + j;
-                            const float v = (row >= 0 && ks < KS && k < rl)
-                                                ? __ldg(yb + (int64_t)row * a.ldy + k) : 0.f;
-                            yv[mm][h][ks][j] = v;
-                            m[mm][h] = fmaxf(m[mm][h], fabsf(v));
-                        }
-                }
-#pragma unroll
-            for (int mm = 0; mm < MB; ++mm)
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    float mx = m[mm][h];
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                    const int e = row_exponent(mx);
-                    fscale[mm][h] = a.scale * exp2i(e);
-                    const float inv = exp2i(-e);
-#pragma unroll
-                    for (int ks = 0; ks < KSMAX; ++ks)
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) yv[mm][h][ks][j] *= inv;
-                }
-#pragma unroll
-            for (int mm = 0; mm < MB; ++mm)
-#pragma unroll
-                for (int ks = 0; ks < KSMAX; ++ks)
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        // a0: (row g, ranks 4q, 4q+1)  a1: (row g+8, 4q, 4q+1)
-                        // a2: (row g, 4q+2, 4q+3)     a3: (row g+8, 4q+2, 4q+3)
-                        const int h = r & 1, j = (r >> 1) * 2;
-                        const float v0 = yv[mm][h][ks][j], v1 = yv[mm][h][ks][j + 1];
-                        const float h0f = Elem<E>::to_f(Elem<E>::from_f(v0));
-                        const float h1f = Elem<E>::to_f(Elem<E>::from_f(v1));
-                        ah[mm][ks][r] = pack2<E>(h0f, h1f);
-                        al[mm][ks][r] = pack2<E>(v0 - h0f, v1 - h1f);
-                    }
-        }
-
-        // 4) MMAs and epilogue, per 16-row block
-#pragma unroll
-        for (int mm = 0; mm < MB; ++mm) {
-            if (mm * 16 >= nrow) break;
-            float acc[4][4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < KSMAX; ++ks) {
-                if (ks < KS) {
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        mma16816<E>(acc[i], ah[mm][ks], bf[ks][i].x, bf[ks][i].y);
-                        mma16816<E>(acc[i], al[mm][ks], bf[ks][i].x, bf[ks][i].y);
-                    }
-                }
-            }
-            if (!col_ok) continue;
+        for (int mm = 0; mm < MB; ++mm)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int row = rows[mm][h];
-                if (row < 0) continue;
-                float res[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) res[k] = fscale[mm][h] * acc[k >> 1][2 * h + (k & 1)];
-                if (ADD) {
-                    float o[8];
-                    unpack8<E>(old[mm][h], o);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) res[k] += o[k];
+                const int i = pt * kWRows + mm * 16 + g + 8 * h;
+                int row = -1;
+                if (i < tile.z) {
+                    row = __ldg(a.perm + tile.y + i);
+                    if (row < 0 || row >= a.T) row = -1;
                 }
-                st_global_v4(out + (int64_t)row * a.ldo + col, pack8<E>(res));
+                r[mm][h] = row;
+            }
+    };
+    auto slice_of = [&](int c, int &s, int &c0) {
+        s = 0;
+        while (s + 1 < a.num_slices && c >= a.chunk_begin[s + 1]) ++s;
+        c0 = (c - a.chunk_begin[s]) * kWCols;
+    };
+    load_rows(tl, part, rows);
+    rl = tl.x >= 0 && tl.x < a.L ? clamp_rank(a.ranks, tl.x, a.R) : 0;
+    KS = (rl + 15) / 16;
+    nrow = min(kWRows, tl.z - part * kWRows);
+
+    int s, c0;
+    slice_of(cbi, s, c0);
+    int64_t col = (int64_t)a.off[s] + c0 + 8 * q;
+    bool col_ok = c0 + 8 * q < a.N[s];
+    UnitLoads<MB, KSMAX> cur, nxt;
+    if (nrow > 0 && rl > 0) issue_unit<E, ADD, MB, KSMAX>(a, cur, rows, tl.x, rl, KS, s, c0, col, col_ok, g, q);
+
+    int y_s = -1;  // slice whose y fragments are held (same tile and part)
+    float fscale[MB][2];
+    uint32_t ah[MB][KSMAX][4], al[MB][KSMAX][4];
+
+    for (int u = u_begin; u < u_end; ++u) {
+        // ---- the next unit: position, and its loads issued now
+        int nt = t, npart = part, ncbi = cbi + 1;
+        if (ncbi == ncb) {
+            ncbi = 0;
+            if (++npart == kParts) {
+                npart = 0;
+                ++nt;
             }
         }
+        const bool has_next = u + 1 < u_end;
+        int4 ntl = tl;
+        int nrows_[MB][2];
+        int nrl = rl, nKS = KS, nnrow = nrow;
+        bool new_rows = has_next && (nt != t || npart != part);
+        if (new_rows) {
+            if (nt != t) {
+                ntl = __ldg(a.tiles + nt);
+                nrl = ntl.x >= 0 && ntl.x < a.L ? clamp_rank(a.ranks, ntl.x, a.R) : 0;
+                nKS = (nrl + 15) / 16;
+            }
+            load_rows(ntl, npart, nrows_);
+            nnrow = min(kWRows, ntl.z - npart * kWRows);
+        }
+        int ns = s, nc0 = c0;
+        int64_t ncol = col;
+        bool ncol_ok = col_ok;
+        if (has_next) {
+            slice_of(ncbi, ns, nc0);
+            ncol = (int64_t)a.off[ns] + nc0 + 8 * q;
+            ncol_ok = nc0 + 8 * q < a.N[ns];
+            if (nnrow > 0 && nrl > 0) {
+                if (new_rows) issue_unit<E, ADD, MB, KSMAX>(a, nxt, nrows_, ntl.x, nrl, nKS, ns, nc0, ncol, ncol_ok, g, q);
+                else issue_unit<E, ADD, MB, KSMAX>(a, nxt, rows, ntl.x, nrl, nKS, ns, nc0, ncol, ncol_ok, g, q);
+            }
+        }
+
+        // ---- the current unit
+        if (nrow > 0) {
+            if (rl == 0) {  // adapter -1 or rank 0: untouched with add_inputs, zeros without
+                if (!ADD && col_ok) {
+#pragma unroll
+                    for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (rows[mm][h] >= 0)
+                                st_global_v4(out + (int64_t)rows[mm][h] * a.ldo + col, make_uint4(0, 0, 0, 0));
+                }
+            } else {
+                if (s != y_s) {
+                    // y fragments of (tile, part, slice), scaled per row by a power of two
+                    y_s = s;
+                    const float *yb = a.y + (int64_t)s * a.y_slice_stride;
+                    float yv[MB][2][KSMAX][4];
+#pragma unroll
+                    for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int row = rows[mm][h];
+                            const float *yr = yb + (int64_t)(row < 0 ? 0 : row) * a.ldy;
+#pragma unroll
+                            for (int ks = 0; ks < KSMAX; ++ks) {
+                                const int k = ks * 16 + 4 * q;
+                                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                                if (row >= 0 && ks < KS && k < rl) {
+                                    if (y_vec && k + 4 <= rl) {
+                                        v = __ldg(reinterpret_cast<const float4 *>(yr + k));
+                                    } else {
+                                        v.x = __ldg(yr + k);
+                                        if (k + 1 < rl) v.y = __ldg(yr + k + 1);
+                                        if (k + 2 < rl) v.z = __ldg(yr + k + 2);
+                                        if (k + 3 < rl) v.w = __ldg(yr + k + 3);
+                                    }
+                                }
+                                yv[mm][h][ks][0] = v.x;
+                                yv[mm][h][ks][1] = v.y;
+                                yv[mm][h][ks][2] = v.z;
+                                yv[mm][h][ks][3] = v.w;
+                            }
+                        }
+#pragma unroll
+                    for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            float mx = 0.f;
+#pragma unroll
+                            for (int ks = 0; ks < KSMAX; ++ks)
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(yv[mm][h][ks][j]));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                            const int e = row_exponent(mx);
+                            fscale[mm][h] = a.scale * exp2i(e);
+                            const float inv = exp2i(-e);
+#pragma unroll
+                            for (int ks = 0; ks < KSMAX; ++ks)
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) yv[mm][h][ks][j] *= inv;
+                        }
+#pragma unroll
+                    for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+                        for (int ks = 0; ks < KSMAX; ++ks)
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                // a0: (row g, ranks 4q, 4q+1)  a1: (row g+8, 4q, 4q+1)
+                                // a2: (row g, 4q+2, 4q+3)     a3: (row g+8, 4q+2, 4q+3)
+                                const int h = r & 1, j = (r >> 1) * 2;
+                                const float v0 = yv[mm][h][ks][j], v1 = yv[mm][h][ks][j + 1];
+                                const uint32_t hw = Pack<E>::pack(v0, v1);
+                                const float2 hf = Pack<E>::unpack(hw);
+                                ah[mm][ks][r] = hw;
+                                al[mm][ks][r] = Pack<E>::pack(v0 - hf.x, v1 - hf.y);
+                            }
+                }
+#pragma unroll
+                for (int mm = 0; mm < MB; ++mm) {
+                    if (mm * 16 >= nrow) break;
+                    float acc[4][4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
+#pragma unroll
+                    for (int ks = 0; ks < KSMAX; ++ks) {
+                        if (ks < KS) {
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                mma16816<E>(acc[i], ah[mm][ks], cur.bf[ks][i].x, cur.bf[ks][i].y);
+                                mma16816<E>(acc[i], al[mm][ks], cur.bf[ks][i].x, cur.bf[ks][i].y);
+                            }
+                        }
+                    }
+                    if (!col_ok) continue;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int row = rows[mm][h];
+                        if (row < 0) continue;
+                        const float f = fscale[mm][h];
+                        uint32_t w[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            float r0 = f * acc[k][2 * h], r1 = f * acc[k][2 * h + 1];
+                            if (ADD) {
+                                const float2 o = Pack<E>::unpack(
+                                    reinterpret_cast<const uint32_t *>(&cur.old[mm][h])[k]);
+                                r0 = fmaf(f, acc[k][2 * h], o.x);
+                                r1 = fmaf(f, acc[k][2 * h + 1], o.y);
+                            }
+                            w[k] = Pack<E>::pack(r0, r1);
+                        }
+                        st_global_v4(out + (int64_t)row * a.ldo + col, make_uint4(w[0], w[1], w[2], w[3]));
+                    }
+                }
+            }
+        }
+
+        // ---- advance
+        if (!has_next) break;
+        if (new_rows) {
+#pragma unroll
+            for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) rows[mm][h] = nrows_[mm][h];
+            y_s = -1;
+        }
+        t = nt;
+        part = npart;
+        cbi = ncbi;
+        tl = ntl;
+        rl = nrl;
+        KS = nKS;
+        nrow = nnrow;
+        s = ns;
+        c0 = nc0;
+        col = ncol;
+        col_ok = ncol_ok;
+        cur = nxt;
     }
 }
 
@@ -572,10 +675,38 @@ cudaError_t configure_dtype() {
     return configure_one<E, true, false>();
 }
 
+// Resident CTAs per SM of each warp-kernel instantiation [dtype][add][ks class],
+// filled once per process by configure_expand_kernels.
+int g_warp_occ[2][2][4] = {};
+
+template <typename E, bool ADD, int KSMAX>
+cudaError_t query_occ(int &occ) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, expand_warp_kernel<E, ADD, KSMAX>,
+                                                         kWThreads, 0);
+}
+
+template <typename E>
+cudaError_t query_occ_dtype(int (&occ)[2][4]) {
+    cudaError_t e;
+    if ((e = query_occ<E, false, 1>(occ[0][0])) != cudaSuccess) return e;
+    if ((e = query_occ<E, false, 2>(occ[0][1])) != cudaSuccess) return e;
+    if ((e = query_occ<E, false, 4>(occ[0][2])) != cudaSuccess) return e;
+    if ((e = query_occ<E, false, 8>(occ[0][3])) != cudaSuccess) return e;
+    if ((e = query_occ<E, true, 1>(occ[1][0])) != cudaSuccess) return e;
+    if ((e = query_occ<E, true, 2>(occ[1][1])) != cudaSuccess) return e;
+    if ((e = query_occ<E, true, 4>(occ[1][2])) != cudaSuccess) return e;
+    return query_occ<E, true, 8>(occ[1][3]);
+}
+
+int ks_class(int ks) { return ks <= 1 ? 0 : ks <= 2 ? 1 : ks <= 4 ? 2 : 3; }
+
 template <typename E, int KSMAX>
 cudaError_t launch_warp_ks(const ExpandArgs &a, int grid, int tiles_grid, int ncb, cudaStream_t st) {
-    if (a.add) expand_warp_kernel<E, true, KSMAX><<<grid, kWThreads, 0, st>>>(a, tiles_grid, ncb);
-    else expand_warp_kernel<E, false, KSMAX><<<grid, kWThreads, 0, st>>>(a, tiles_grid, ncb);
+    // 16-byte y loads when every slice's y block starts 16-byte aligned
+    const int y_vec = (reinterpret_cast<uintptr_t>(a.y) & 15) == 0 && a.ldy % 4 == 0 &&
+                      a.y_slice_stride % 4 == 0;
+    if (a.add) expand_warp_kernel<E, true, KSMAX><<<grid, kWThreads, 0, st>>>(a, tiles_grid, ncb, y_vec);
+    else expand_warp_kernel<E, false, KSMAX><<<grid, kWThreads, 0, st>>>(a, tiles_grid, ncb, y_vec);
     return cudaGetLastError();
 }
 
@@ -601,7 +732,9 @@ cudaError_t launch_dtype(const ExpandArgs &a, dim3 grid, size_t smem, cudaStream
 cudaError_t configure_expand_kernels() {
     cudaError_t e = configure_dtype<__half>();
     if (e != cudaSuccess) return e;
-    return configure_dtype<__nv_bfloat16>();
+    if ((e = configure_dtype<__nv_bfloat16>()) != cudaSuccess) return e;
+    if ((e = query_occ_dtype<__half>(g_warp_occ[LORA_F16])) != cudaSuccess) return e;
+    return query_occ_dtype<__nv_bfloat16>(g_warp_occ[LORA_BF16]);
 }
 
 cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceInfo &dev,
@@ -627,7 +760,8 @@ cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceI
         const int ncb = a.chunk_begin[a.num_slices];
         if (ncb == 0) return cudaSuccess;
         const long long units = (long long)tiles_grid * (kTile / (16 * warp_mb((a.R + 15) / 16 > 4 ? 8 : 1))) * ncb;
-        const long long warps_max = (long long)dev.sm_count * 20;  // ~20 resident warps per SM
+        const int occ = std::max(1, g_warp_occ[dt][a.add ? 1 : 0][ks_class((a.R + 15) / 16)]);
+        const long long warps_max = (long long)dev.sm_count * occ * (kWThreads / 32);
         const long long warps = std::min(units, warps_max);
         const int grid = (int)std::max<long long>(1, (warps + 3) / 4);
         return dt == LORA_F16 ? launch_warp_dtype<__half>(a, grid, tiles_grid, ncb, stream)
