@@ -266,6 +266,28 @@ def capture_steps(lg, pool):
     return graphs
 
 
+def op_only_ms(pool, launch, reps: int = 20):
+    """Average duration of one operator per batch size: a graph of one launch
+    per pool set (each on a different set, so inputs come from HBM), replayed
+    `reps` times between two events on the launching stream."""
+    res = []
+    stream = torch.cuda.Stream()
+    for i in range(len(li.DECODE_T)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for batches in pool:
+                launch(batches[i])
+        g.replay()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            g.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        res.append(t0.elapsed_time(t1) / (reps * len(pool)))
+    return res
+
+
 def expand_only_ms(lg, pool, reps: int = 20):
     """Average duration of expand_slice per batch size: a graph of one launch
     per pool set (each on a different set, so inputs come from HBM), replayed
@@ -336,6 +358,9 @@ def main_ours(args):
     ms = start.elapsed_time(end)
     # dominant kernel, timed right after the step loop on the same stream
     ex_ms = expand_only_ms(lg, pool)
+    sh_ms = op_only_ms(pool, lambda b: lg.lora_shrink(b["x"], b["A"], b["y"], b["plan"],
+                                                      num_slices=len(SLICES)))
+    gr_ms = op_only_ms(pool, lambda b: lg.lora_group_tokens(b["idx"], L, b["plan"]))
     ex_src = (f"CUDA events around graphs of back-to-back expand_slice launches, one per "
               f"pool set ({nsets} sets, inputs from HBM), per batch size")
     if ws > 1:
@@ -356,6 +381,9 @@ def main_ours(args):
         ex_time += ex_ms[i] / 1e3
         per_T[str(T)] = {"expand_us": ex_ms[i] * 1e3,
                          "expand_GBps": eb / (ex_ms[i] / 1e3) / 1e9,
+                         "shrink_us": sh_ms[i] * 1e3,
+                         "shrink_GBps": sb / (sh_ms[i] / 1e3) / 1e9,
+                         "group_us": gr_ms[i] * 1e3,
                          "expand_bytes": eb, "shrink_bytes": sb}
     hbm, tf, src = peaks()
     achieved = ex_bytes / ex_time / 1e9          # bytes of the 5 launches / their summed time
