@@ -223,6 +223,31 @@ lora_status_t lora_expand_slice(lora_dtype_t dtype, const float *y, int64_t ldy,
                                 float scale, int add_inputs, lora_stream_t stream);
 
 /*
+ * Shrink followed by expand_slice in one call (vLLM PR #15655's shrink and
+ * expand variants of the LoRA kernel, chained through the fp32 rank buffer
+ * of vLLM PR #11579), the decode-path form used once per LoRA layer:
+ *   y   = scale_shrink * x . A[l]^T         (as lora_shrink with add_inputs = 0,
+ *                                             A = [L, num_slices*R, H])
+ *   out = (add_inputs ? out : 0) + scale_expand * y_s . B_s[l]^T for every slice
+ *                                            (as lora_expand_slice with y_slice_stride = R)
+ * y [T, ldy >= num_slices*R] is written in full (it is also the fp32 output of
+ * the shrink).  When the shapes allow it (R <= 64, num_slices*R <= 128, H, ldx,
+ * ldo, R, slice offsets and sizes multiples of 8, 16-byte aligned x, A, out
+ * and B_s) one kernel does both steps, a thread-block cluster per plan tile;
+ * otherwise the call runs the two operators back to back.  Results agree
+ * with the two-operator sequence within fp32 accumulation accuracy.
+ * Errors: those of lora_shrink and lora_expand_slice.
+ */
+lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_t ldx, int32_t T,
+                                       int32_t H, const void *A, int32_t L, int32_t R,
+                                       const int32_t *ranks, float *y, int64_t ldy,
+                                       int32_t num_slices, const void *const *B_slices,
+                                       const int32_t *slice_N, const int32_t *slice_offset,
+                                       void *out, int64_t ldo, const void *plan,
+                                       float scale_shrink, float scale_expand, int add_inputs,
+                                       lora_stream_t stream);
+
+/*
  * Reads the plan's device-side error words.  SYNCHRONISES `stream` (a
  * device-to-host copy); for tests and debugging, not for the hot path.
  * *bad_ids <- LORA_HDR_BAD_IDS, *err_flags <- LORA_HDR_ERR (either may be NULL).

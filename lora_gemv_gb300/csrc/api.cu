@@ -37,7 +37,8 @@ cudaError_t init_device(int dev, lora::DeviceInfo *info) {
     if (e != cudaSuccess) return e;
     if ((e = lora::configure_plan_kernels()) != cudaSuccess) return e;
     if ((e = lora::configure_shrink_kernels(info)) != cudaSuccess) return e;
-    return lora::configure_expand_kernels();
+    if ((e = lora::configure_expand_kernels()) != cudaSuccess) return e;
+    return lora::configure_fused_kernels(*info);
 }
 
 // Per-device kernel attributes are set once, on the first call on that device.
@@ -155,10 +156,13 @@ lora_status_t lora_group_segments(const int32_t *seg_start, const int32_t *seg_l
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "group_segments launch");
 }
 
-lora_status_t lora_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_t T, int32_t H,
-                          const void *A, int32_t L, int32_t R, int32_t num_slices,
-                          const int32_t *ranks, float *y, int64_t ldy, const void *plan,
-                          float scale, int add_inputs, lora_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+lora_status_t check_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_t T, int32_t H,
+                           const void *A, int32_t L, int32_t R, int32_t num_slices,
+                           const int32_t *ranks, const float *y, int64_t ldy, const void *plan) {
     if (!valid_dtype(dtype)) return fail(LORA_ERR_INVALID_ARG, "dtype %d", (int)dtype);
     if (T < 0 || H < 1 || L < 1) return fail(LORA_ERR_INVALID_ARG, "T=%d H=%d L=%d", T, H, L);
     if (R < 1 || R > LORA_MAX_RANK) return fail(LORA_ERR_INVALID_ARG, "R = %d", R);
@@ -171,6 +175,63 @@ lora_status_t lora_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_
     if (!aligned(x, 2) || !aligned(A, 2) || !aligned(y, 4) || !aligned(ranks, 4))
         return fail(LORA_ERR_INVALID_ARG, "misaligned pointer");
     if (!aligned(plan, 16)) return fail(LORA_ERR_WORKSPACE, "plan is not 16-byte aligned");
+    lora_plan_layout_t lay;
+    return lora_plan_layout(T, L, &lay);
+}
+
+lora_status_t check_expand(lora_dtype_t dtype, const float *y, int64_t ldy, int32_t T,
+                           int32_t num_slices, const void *const *B_slices,
+                           const int32_t *slice_N, const int32_t *slice_offset,
+                           int32_t y_slice_stride, int32_t L, int32_t R, const int32_t *ranks,
+                           const void *out, int64_t ldo, const void *plan) {
+    if (!valid_dtype(dtype)) return fail(LORA_ERR_INVALID_ARG, "dtype %d", (int)dtype);
+    if (T < 0 || L < 1) return fail(LORA_ERR_INVALID_ARG, "T=%d L=%d", T, L);
+    if (R < 1 || R > LORA_MAX_RANK) return fail(LORA_ERR_INVALID_ARG, "R = %d", R);
+    if (num_slices < 1 || num_slices > LORA_MAX_SLICES)
+        return fail(LORA_ERR_INVALID_ARG, "num_slices = %d", num_slices);
+    if (!B_slices || !slice_N || !slice_offset)
+        return fail(LORA_ERR_INVALID_ARG, "slice arrays are NULL");
+    if (y_slice_stride < 0) return fail(LORA_ERR_INVALID_ARG, "y_slice_stride < 0");
+    if ((int64_t)(num_slices - 1) * y_slice_stride + R > ldy)
+        return fail(LORA_ERR_INVALID_ARG, "y columns of the last slice exceed ldy");
+    if (!plan || (T > 0 && (!y || !out))) return fail(LORA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(y, 4) || !aligned(out, 2) || !aligned(ranks, 4))
+        return fail(LORA_ERR_INVALID_ARG, "misaligned pointer");
+    if (!aligned(plan, 16)) return fail(LORA_ERR_WORKSPACE, "plan is not 16-byte aligned");
+    int order[LORA_MAX_SLICES];
+    for (int s = 0; s < num_slices; ++s) {
+        if (slice_N[s] < 0 || slice_offset[s] < 0)
+            return fail(LORA_ERR_INVALID_ARG, "slice %d: N=%d offset=%d", s, slice_N[s],
+                        slice_offset[s]);
+        if ((int64_t)slice_offset[s] + slice_N[s] > ldo)
+            return fail(LORA_ERR_INVALID_ARG, "slice %d ends past ldo", s);
+        if (slice_N[s] > 0 && (B_slices[s] == nullptr || !aligned(B_slices[s], 2)))
+            return fail(LORA_ERR_INVALID_ARG, "slice %d weights NULL or misaligned", s);
+        order[s] = s;
+    }
+    std::sort(order, order + num_slices,
+              [&](int i, int j) { return slice_offset[i] < slice_offset[j]; });
+    for (int k = 0; k + 1 < num_slices; ++k) {
+        const int i = order[k], j = order[k + 1];
+        if (slice_N[i] > 0 && slice_N[j] > 0 && slice_offset[i] + slice_N[i] > slice_offset[j])
+            return fail(LORA_ERR_INVALID_ARG, "slices %d and %d overlap", i, j);
+    }
+    lora_plan_layout_t lay;
+    return lora_plan_layout(T, L, &lay);
+}
+
+}  // namespace
+
+extern "C" {
+
+lora_status_t lora_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_t T, int32_t H,
+                          const void *A, int32_t L, int32_t R, int32_t num_slices,
+                          const int32_t *ranks, float *y, int64_t ldy, const void *plan,
+                          float scale, int add_inputs, lora_stream_t stream) {
+    {
+        lora_status_t st = check_shrink(dtype, x, ldx, T, H, A, L, R, num_slices, ranks, y, ldy, plan);
+        if (st != LORA_OK) return st;
+    }
     lora_plan_layout_t lay;
     lora_status_t s = lora_plan_layout(T, L, &lay);
     if (s != LORA_OK) return s;
@@ -206,37 +267,10 @@ lora_status_t lora_expand_slice(lora_dtype_t dtype, const float *y, int64_t ldy,
                                 int32_t y_slice_stride, int32_t L, int32_t R,
                                 const int32_t *ranks, void *out, int64_t ldo, const void *plan,
                                 float scale, int add_inputs, lora_stream_t stream) {
-    if (!valid_dtype(dtype)) return fail(LORA_ERR_INVALID_ARG, "dtype %d", (int)dtype);
-    if (T < 0 || L < 1) return fail(LORA_ERR_INVALID_ARG, "T=%d L=%d", T, L);
-    if (R < 1 || R > LORA_MAX_RANK) return fail(LORA_ERR_INVALID_ARG, "R = %d", R);
-    if (num_slices < 1 || num_slices > LORA_MAX_SLICES)
-        return fail(LORA_ERR_INVALID_ARG, "num_slices = %d", num_slices);
-    if (!B_slices || !slice_N || !slice_offset)
-        return fail(LORA_ERR_INVALID_ARG, "slice arrays are NULL");
-    if (y_slice_stride < 0) return fail(LORA_ERR_INVALID_ARG, "y_slice_stride < 0");
-    if ((int64_t)(num_slices - 1) * y_slice_stride + R > ldy)
-        return fail(LORA_ERR_INVALID_ARG, "y columns of the last slice exceed ldy");
-    if (!plan || (T > 0 && (!y || !out))) return fail(LORA_ERR_INVALID_ARG, "NULL pointer");
-    if (!aligned(y, 4) || !aligned(out, 2) || !aligned(ranks, 4))
-        return fail(LORA_ERR_INVALID_ARG, "misaligned pointer");
-    if (!aligned(plan, 16)) return fail(LORA_ERR_WORKSPACE, "plan is not 16-byte aligned");
-    int order[LORA_MAX_SLICES];
-    for (int s = 0; s < num_slices; ++s) {
-        if (slice_N[s] < 0 || slice_offset[s] < 0)
-            return fail(LORA_ERR_INVALID_ARG, "slice %d: N=%d offset=%d", s, slice_N[s],
-                        slice_offset[s]);
-        if ((int64_t)slice_offset[s] + slice_N[s] > ldo)
-            return fail(LORA_ERR_INVALID_ARG, "slice %d ends past ldo", s);
-        if (slice_N[s] > 0 && (B_slices[s] == nullptr || !aligned(B_slices[s], 2)))
-            return fail(LORA_ERR_INVALID_ARG, "slice %d weights NULL or misaligned", s);
-        order[s] = s;
-    }
-    std::sort(order, order + num_slices,
-              [&](int i, int j) { return slice_offset[i] < slice_offset[j]; });
-    for (int k = 0; k + 1 < num_slices; ++k) {
-        const int i = order[k], j = order[k + 1];
-        if (slice_N[i] > 0 && slice_N[j] > 0 && slice_offset[i] + slice_N[i] > slice_offset[j])
-            return fail(LORA_ERR_INVALID_ARG, "slices %d and %d overlap", i, j);
+    {
+        lora_status_t st = check_expand(dtype, y, ldy, T, num_slices, B_slices, slice_N,
+                                        slice_offset, y_slice_stride, L, R, ranks, out, ldo, plan);
+        if (st != LORA_OK) return st;
     }
     lora_plan_layout_t lay;
     lora_status_t s = lora_plan_layout(T, L, &lay);
@@ -280,6 +314,64 @@ lora_status_t lora_expand(lora_dtype_t dtype, const float *y, int64_t ldy, int32
     const int32_t offs[1] = {0};
     return lora_expand_slice(dtype, y, ldy, T, 1, Bs, Ns, offs, 0, L, R, ranks, out, ldo, plan,
                              scale, add_inputs, stream);
+}
+
+lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_t ldx, int32_t T,
+                                       int32_t H, const void *A, int32_t L, int32_t R,
+                                       const int32_t *ranks, float *y, int64_t ldy,
+                                       int32_t num_slices, const void *const *B_slices,
+                                       const int32_t *slice_N, const int32_t *slice_offset,
+                                       void *out, int64_t ldo, const void *plan,
+                                       float scale_shrink, float scale_expand, int add_inputs,
+                                       lora_stream_t stream) {
+    lora_status_t st = check_shrink(dtype, x, ldx, T, H, A, L, R, num_slices, ranks, y, ldy, plan);
+    if (st != LORA_OK) return st;
+    st = check_expand(dtype, y, ldy, T, num_slices, B_slices, slice_N, slice_offset, R, L, R, ranks,
+                      out, ldo, plan);
+    if (st != LORA_OK) return st;
+    if (T == 0) return LORA_OK;
+    const lora::DeviceInfo *dev;
+    if ((st = device_info(&dev)) != LORA_OK) return st;
+    lora_plan_layout_t lay;
+    lora_plan_layout(T, L, &lay);
+    lora::PlanPtrs p = plan_ptrs(const_cast<void *>(plan), lay);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    lora::FusedArgs f{};
+    f.x = x;
+    f.ldx = ldx;
+    f.T = T;
+    f.H = H;
+    f.A = A;
+    f.L = L;
+    f.R = R;
+    f.S = num_slices;
+    f.ranks = ranks;
+    f.y = y;
+    f.ldy = ldy;
+    f.scale_s = scale_shrink;
+    f.num_slices = num_slices;
+    for (int k = 0; k < num_slices; ++k) {
+        f.B[k] = B_slices[k];
+        f.N[k] = slice_N[k];
+        f.off[k] = slice_offset[k];
+    }
+    f.out = out;
+    f.ldo = ldo;
+    f.scale = scale_expand;
+    f.add = add_inputs ? 1 : 0;
+    f.hdr = p.hdr;
+    f.perm = p.perm;
+    f.tiles = p.tiles;
+    f.max_tiles = (int)lay.max_tiles;
+    cudaError_t e = lora::launch_fused(dtype, f, *dev, cs);
+    if (e == cudaErrorNotSupported) {  // shapes outside the fused kernel: two launches
+        if ((st = lora_shrink(dtype, x, ldx, T, H, A, L, R, num_slices, ranks, y, ldy, plan,
+                              scale_shrink, 0, stream)) != LORA_OK)
+            return st;
+        return lora_expand_slice(dtype, y, ldy, T, num_slices, B_slices, slice_N, slice_offset, R,
+                                 L, R, ranks, out, ldo, plan, scale_expand, add_inputs, stream);
+    }
+    return e == cudaSuccess ? LORA_OK : cuda_fail(e, "shrink_expand_slice launch");
 }
 
 lora_status_t lora_get_error(const void *plan, int32_t *bad_ids, int32_t *err_flags,

@@ -20,6 +20,7 @@
 //  - tiles with adapter -1 and adapters of rank 0 load nothing (block
 //    skipping) and, without add_inputs, only store zeros.
 #include "common.cuh"
+#include "frag.cuh"
 #include "kernels.h"
 
 namespace lora {
@@ -331,42 +332,6 @@ constexpr int kWCols = 32;      // output columns per warp unit
 // (the y fragments of a unit live in registers).
 __host__ __device__ constexpr int warp_mb(int ksmax) { return ksmax >= 8 ? 1 : 2; }
 
-template <typename E>
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-    E lo = Elem<E>::from_f(a), hi = Elem<E>::from_f(b);
-    return (uint32_t)(*reinterpret_cast<uint16_t *>(&lo)) |
-           ((uint32_t)(*reinterpret_cast<uint16_t *>(&hi)) << 16);
-}
-
-// Power-of-two factor 2^k as a float, k in [-126, 127].
-__device__ __forceinline__ float exp2i(int k) { return __int_as_float((127 + k) << 23); }
-
-// Per-row exponent e with max|y_row| * 2^-e < 1 (frexp-style), clamped.
-__device__ __forceinline__ int row_exponent(float m) {
-    const int be = (__float_as_int(m) >> 23) & 0xff;
-    return min(max(be - 126, -125), 126);
-}
-
-template <typename E> struct Pack;
-template <> struct Pack<__half> {
-    static __device__ __forceinline__ uint32_t pack(float a, float b) {
-        __half2 h = __floats2half2_rn(a, b);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-    static __device__ __forceinline__ float2 unpack(uint32_t w) {
-        return __half22float2(*reinterpret_cast<__half2 *>(&w));
-    }
-};
-template <> struct Pack<__nv_bfloat16> {
-    static __device__ __forceinline__ uint32_t pack(float a, float b) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-        return *reinterpret_cast<uint32_t *>(&h);
-    }
-    static __device__ __forceinline__ float2 unpack(uint32_t w) {
-        return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w));
-    }
-};
-
 // Loads of one warp unit that are issued a unit ahead.
 template <int MB, int KSMAX>
 struct UnitLoads {
@@ -387,24 +352,8 @@ __device__ __forceinline__ void issue_unit(const ExpandArgs &a, UnitLoads<MB, KS
                 if (rows[mm][h] >= 0) ld.old[mm][h] = ld_global_v4(out + (int64_t)rows[mm][h] * a.ldo + col);
     }
     const int Ns = a.N[s];
-    const E *Bl = static_cast<const E *>(a.B[s]) + (int64_t)l * Ns * a.R;
-#pragma unroll
-    for (int ks = 0; ks < KSMAX; ++ks)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            ld.bf[ks][i] = make_uint2(0, 0);
-            const int n = c0 + 8 * (g >> 1) + 2 * i + (g & 1);
-            const int k = ks * 16 + 4 * q;
-            if (ks < KS && n < Ns && k < rl) {
-                uint2 v = __ldg(reinterpret_cast<const uint2 *>(Bl + (int64_t)n * a.R + k));
-                const int nv = rl - k;  // valid ranks among these 4
-                if (nv < 4) {
-                    v.y = nv <= 2 ? 0u : (v.y & 0xffffu);
-                    if (nv < 2) v.x &= 0xffffu;
-                }
-                ld.bf[ks][i] = v;
-            }
-        }
+    load_bfrags<E, KSMAX>(ld.bf, static_cast<const E *>(a.B[s]) + (int64_t)l * Ns * a.R, Ns, a.R,
+                          c0, rl, KS, g, q);
 }
 
 template <typename E, bool ADD, int KSMAX>
@@ -493,7 +442,7 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
         int4 ntl = tl;
         int nrows_[MB][2];
         int nrl = rl, nKS = KS, nnrow = nrow;
-        bool new_rows = has_next && (nt != t || npart != part);
+        const bool new_rows = has_next && (nt != t || npart != part);
         if (new_rows) {
             if (nt != t) {
                 ntl = __ldg(a.tiles + nt);
@@ -528,110 +477,17 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
                                 st_global_v4(out + (int64_t)rows[mm][h] * a.ldo + col, make_uint4(0, 0, 0, 0));
                 }
             } else {
-                if (s != y_s) {
-                    // y fragments of (tile, part, slice), scaled per row by a power of two
+                if (s != y_s) {  // y fragments of (tile, part, slice)
                     y_s = s;
-                    const float *yb = a.y + (int64_t)s * a.y_slice_stride;
-                    float yv[MB][2][KSMAX][4];
-#pragma unroll
-                    for (int mm = 0; mm < MB; ++mm)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int row = rows[mm][h];
-                            const float *yr = yb + (int64_t)(row < 0 ? 0 : row) * a.ldy;
-#pragma unroll
-                            for (int ks = 0; ks < KSMAX; ++ks) {
-                                const int k = ks * 16 + 4 * q;
-                                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-                                if (row >= 0 && ks < KS && k < rl) {
-                                    if (y_vec && k + 4 <= rl) {
-                                        v = __ldg(reinterpret_cast<const float4 *>(yr + k));
-                                    } else {
-                                        v.x = __ldg(yr + k);
-                                        if (k + 1 < rl) v.y = __ldg(yr + k + 1);
-                                        if (k + 2 < rl) v.z = __ldg(yr + k + 2);
-                                        if (k + 3 < rl) v.w = __ldg(yr + k + 3);
-                                    }
-                                }
-                                yv[mm][h][ks][0] = v.x;
-                                yv[mm][h][ks][1] = v.y;
-                                yv[mm][h][ks][2] = v.z;
-                                yv[mm][h][ks][3] = v.w;
-                            }
-                        }
-#pragma unroll
-                    for (int mm = 0; mm < MB; ++mm)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            float mx = 0.f;
-#pragma unroll
-                            for (int ks = 0; ks < KSMAX; ++ks)
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(yv[mm][h][ks][j]));
-                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                            const int e = row_exponent(mx);
-                            fscale[mm][h] = a.scale * exp2i(e);
-                            const float inv = exp2i(-e);
-#pragma unroll
-                            for (int ks = 0; ks < KSMAX; ++ks)
-#pragma unroll
-                                for (int j = 0; j < 4; ++j) yv[mm][h][ks][j] *= inv;
-                        }
-#pragma unroll
-                    for (int mm = 0; mm < MB; ++mm)
-#pragma unroll
-                        for (int ks = 0; ks < KSMAX; ++ks)
-#pragma unroll
-                            for (int r = 0; r < 4; ++r) {
-                                // a0: (row g, ranks 4q, 4q+1)  a1: (row g+8, 4q, 4q+1)
-                                // a2: (row g, 4q+2, 4q+3)     a3: (row g+8, 4q+2, 4q+3)
-                                const int h = r & 1, j = (r >> 1) * 2;
-                                const float v0 = yv[mm][h][ks][j], v1 = yv[mm][h][ks][j + 1];
-                                const uint32_t hw = Pack<E>::pack(v0, v1);
-                                const float2 hf = Pack<E>::unpack(hw);
-                                ah[mm][ks][r] = hw;
-                                al[mm][ks][r] = Pack<E>::pack(v0 - hf.x, v1 - hf.y);
-                            }
+                    build_yfrags<E, MB, KSMAX, false>(ah, al, fscale, rows,
+                                                      a.y + (int64_t)s * a.y_slice_stride, a.ldy,
+                                                      rl, KS, a.scale, y_vec != 0, q);
                 }
 #pragma unroll
                 for (int mm = 0; mm < MB; ++mm) {
                     if (mm * 16 >= nrow) break;
-                    float acc[4][4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
-#pragma unroll
-                    for (int ks = 0; ks < KSMAX; ++ks) {
-                        if (ks < KS) {
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                mma16816<E>(acc[i], ah[mm][ks], cur.bf[ks][i].x, cur.bf[ks][i].y);
-                                mma16816<E>(acc[i], al[mm][ks], cur.bf[ks][i].x, cur.bf[ks][i].y);
-                            }
-                        }
-                    }
-                    if (!col_ok) continue;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int row = rows[mm][h];
-                        if (row < 0) continue;
-                        const float f = fscale[mm][h];
-                        uint32_t w[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            float r0 = f * acc[k][2 * h], r1 = f * acc[k][2 * h + 1];
-                            if (ADD) {
-                                const float2 o = Pack<E>::unpack(
-                                    reinterpret_cast<const uint32_t *>(&cur.old[mm][h])[k]);
-                                r0 = fmaf(f, acc[k][2 * h], o.x);
-                                r1 = fmaf(f, acc[k][2 * h + 1], o.y);
-                            }
-                            w[k] = Pack<E>::pack(r0, r1);
-                        }
-                        st_global_v4(out + (int64_t)row * a.ldo + col, make_uint4(w[0], w[1], w[2], w[3]));
-                    }
+                    expand_block<E, ADD, KSMAX>(out, a.ldo, col, rows[mm], ah[mm], al[mm], cur.bf,
+                                                fscale[mm], cur.old[mm], KS, col_ok);
                 }
             }
         }

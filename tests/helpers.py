@@ -78,3 +78,19 @@ def oracle_run(case, rows=None):
     o = oracle.expand_slice(y, [f64(b) for b in case.B], case.slice_offsets, lo, f64(out),
                             y_stride=case.R, ranks=ranks, scale=case.scale, add=case.add)
     return y, o
+
+
+def gpu_run_fused(lg, case, dev="cuda"):
+    """plan + fused shrink/expand_slice on the GPU.  Returns (y, out, plan)."""
+    plan = gpu_plan(lg, case, dev)
+    x, A = case.x.to(dev), case.A.to(dev)
+    Bs = [b.to(dev) for b in case.B]
+    out = case.out.to(dev)
+    y = torch.full((case.T, case.num_slices * case.R), float("nan"), dtype=torch.float32,
+                   device=dev)
+    ranks = case.ranks.to(dev) if case.ranks is not None else None
+    lg.lora_shrink_expand_slice(x, A, y, Bs, out, plan, case.slice_offsets, ranks=ranks,
+                                scale_shrink=case.shrink_scale, scale_expand=case.scale,
+                                add_inputs=case.add)
+    torch.cuda.synchronize()
+    return y.cpu(), out.cpu(), plan
