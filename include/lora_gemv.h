@@ -114,9 +114,13 @@ enum {
  *                     tokens, then the inactive tokens likewise:
  *                     {adapter (-1 for inactive), first perm position,
  *                      token count, group number (-1 for inactive)}
+ *   tile_rows[max_tiles][LORA_TILE_TOKENS]  the tokens of each tile
+ *                     (perm[first .. first + count)), -1 past the count, so
+ *                     an operator reads a tile's rows without first reading
+ *                     its record
  */
 typedef struct {
-    int64_t header, count, offset, perm, group_lora, group_start, group_count, tiles;
+    int64_t header, count, offset, perm, group_lora, group_start, group_count, tiles, tile_rows;
     int64_t max_tiles;
     int64_t bytes; /* total size of the buffer */
 } lora_plan_layout_t;

@@ -52,7 +52,7 @@ class LoraError(RuntimeError):
 
 class _Layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("header", "count", "offset", "perm", "group_lora",
-                                             "group_start", "group_count", "tiles",
+                                             "group_start", "group_count", "tiles", "tile_rows",
                                              "max_tiles", "bytes")]
 
 
@@ -195,6 +195,7 @@ def plan_view(plan: torch.Tensor, T: int, L: int) -> dict:
         "group_start": seg(lay["group_start"], T + 1),
         "group_count": seg(lay["group_count"], T + 1),
         "tiles": seg(lay["tiles"], 4 * lay["max_tiles"]).view(-1, 4),
+        "tile_rows": seg(lay["tile_rows"], TILE_TOKENS * lay["max_tiles"]).view(-1, TILE_TOKENS),
     }
 
 

@@ -79,6 +79,7 @@ lora::PlanPtrs plan_ptrs(void *plan, const lora_plan_layout_t &lay) {
     p.group_start = reinterpret_cast<int32_t *>(b + lay.group_start);
     p.group_count = reinterpret_cast<int32_t *>(b + lay.group_count);
     p.tiles = reinterpret_cast<int4 *>(b + lay.tiles);
+    p.tile_rows = reinterpret_cast<int32_t *>(b + lay.tile_rows);
     return p;
 }
 
@@ -114,6 +115,8 @@ lora_status_t lora_plan_layout(int32_t T, int32_t L, lora_plan_layout_t *lay) {
     lay->tiles = off;
     lay->max_tiles = (int64_t)T + T / LORA_TILE_TOKENS + 2;
     off += lay->max_tiles * 16;
+    lay->tile_rows = off;
+    off += lay->max_tiles * LORA_TILE_TOKENS * 4;
     lay->bytes = off;
     return LORA_OK;
 }
@@ -256,6 +259,7 @@ lora_status_t lora_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_
     a.hdr = p.hdr;
     a.perm = p.perm;
     a.tiles = p.tiles;
+    a.tile_rows = p.tile_rows;
     a.max_tiles = (int)lay.max_tiles;
     cudaError_t e = lora::launch_shrink(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "shrink launch");
@@ -300,6 +304,7 @@ lora_status_t lora_expand_slice(lora_dtype_t dtype, const float *y, int64_t ldy,
     a.hdr = p.hdr;
     a.perm = p.perm;
     a.tiles = p.tiles;
+    a.tile_rows = p.tile_rows;
     a.max_tiles = (int)lay.max_tiles;
     cudaError_t e = lora::launch_expand(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "expand launch");
@@ -362,6 +367,7 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
     f.hdr = p.hdr;
     f.perm = p.perm;
     f.tiles = p.tiles;
+    f.tile_rows = p.tile_rows;
     f.max_tiles = (int)lay.max_tiles;
     cudaError_t e = lora::launch_fused(dtype, f, *dev, cs);
     if (e == cudaErrorNotSupported) {  // shapes outside the fused kernel: two launches

@@ -118,15 +118,12 @@ expand_kernel(const ExpandArgs a) {
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
         const int4 tl = tl_next;
         if (tile + (int)gridDim.x < n_tiles) tl_next = __ldcg(a.tiles + tile + gridDim.x);
-        const int l = tl.x, p0 = tl.y, n = tl.z;
+        const int l = tl.x, n = tl.z;
         const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
 
         if (threadIdx.x < kTile) {
-            int row = -1;
-            if (threadIdx.x < n) {
-                row = __ldcg(a.perm + p0 + threadIdx.x);
-                if (row < 0 || row >= a.T) row = -1;
-            }
+            int row = __ldcg(a.tile_rows + (int64_t)tile * kTile + threadIdx.x);
+            if (row >= a.T) row = -1;
             s_rows[threadIdx.x] = row;
         }
         __syncthreads();
@@ -393,18 +390,14 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     // per (tile, part) state
     int rows[MB][2];
     int rl = 0, KS = 0, nrow = 0;
-    auto load_rows = [&](const int4 &tile, int pt, int (&r)[MB][2]) {
+    // a tile's token rows come from the plan's per-tile row lists (-1 padded)
+    auto load_rows = [&](int tt, int pt, int (&r)[MB][2]) {
 #pragma unroll
         for (int mm = 0; mm < MB; ++mm)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const int i = pt * kWRows + mm * 16 + g + 8 * h;
-                int row = -1;
-                if (i < tile.z) {
-                    row = __ldg(a.perm + tile.y + i);
-                    if (row < 0 || row >= a.T) row = -1;
-                }
-                r[mm][h] = row;
+                int row = __ldg(a.tile_rows + (int64_t)tt * kTile + pt * kWRows + mm * 16 + g + 8 * h);
+                r[mm][h] = row >= a.T ? -1 : row;
             }
     };
     auto slice_of = [&](int c, int &s, int &c0) {
@@ -412,7 +405,7 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
         while (s + 1 < a.num_slices && c >= a.chunk_begin[s + 1]) ++s;
         c0 = (c - a.chunk_begin[s]) * kWCols;
     };
-    load_rows(tl, part, rows);
+    load_rows(t < a.max_tiles ? t : 0, part, rows);
     rl = tl.x >= 0 && tl.x < a.L ? clamp_rank(a.ranks, tl.x, a.R) : 0;
     KS = (rl + 15) / 16;
     nrow = min(kWRows, tl.z - part * kWRows);
@@ -449,7 +442,7 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
                 nrl = ntl.x >= 0 && ntl.x < a.L ? clamp_rank(a.ranks, ntl.x, a.R) : 0;
                 nKS = (nrl + 15) / 16;
             }
-            load_rows(ntl, npart, nrows_);
+            load_rows(nt, npart, nrows_);
             nnrow = min(kWRows, ntl.z - npart * kWRows);
         }
         int ns = s, nc0 = c0;

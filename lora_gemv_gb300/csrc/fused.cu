@@ -78,16 +78,12 @@ fused_kernel(const FusedArgs a, int hchunk, int y_vec) {
     for (int tile = blockIdx.y; tile < n_tiles; tile += gridDim.y) {
         const int4 tl = tl_next;
         if (tile + (int)gridDim.y < n_tiles) tl_next = __ldg(a.tiles + tile + gridDim.y);
-        const int l = tl.x, p0 = tl.y, n = tl.z;
+        const int l = tl.x, n = tl.z;
         const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
 
         if (threadIdx.x < kTile) {
-            int row = -1;
-            if ((int)threadIdx.x < n) {
-                row = __ldg(a.perm + p0 + threadIdx.x);
-                if (row < 0 || row >= a.T) row = -1;
-            }
-            s_rows[threadIdx.x] = row;
+            int row = __ldg(a.tile_rows + (int64_t)tile * kTile + threadIdx.x);
+            s_rows[threadIdx.x] = row >= a.T ? -1 : row;
         }
         __syncthreads();
 

@@ -12,6 +12,7 @@ namespace lora {
 struct PlanPtrs {
     int32_t *hdr, *count, *offset, *perm, *group_lora, *group_start, *group_count;
     int4 *tiles;
+    int32_t *tile_rows;  // [max_tiles][kTile]
 };
 
 struct ShrinkArgs {
@@ -28,6 +29,7 @@ struct ShrinkArgs {
     int32_t *hdr;
     const int32_t *perm;
     const int4 *tiles;
+    const int32_t *tile_rows;
     int max_tiles;
 };
 
@@ -50,6 +52,7 @@ struct ExpandArgs {
     int32_t *hdr;
     const int32_t *perm;
     const int4 *tiles;
+    const int32_t *tile_rows;
     int max_tiles;
 };
 
@@ -76,6 +79,7 @@ struct FusedArgs {
     int32_t *hdr;
     const int32_t *perm;
     const int4 *tiles;
+    const int32_t *tile_rows;
     int max_tiles;
 };
 

@@ -45,6 +45,14 @@ __device__ void emit_tiles(const PlanPtrs &p, int T, int n_active, int G, int *w
         p.tiles[carry + k] = make_int4(-1, p0, min(kTile, T - p0), -1);
     }
     if (threadIdx.x == 0) p.hdr[LORA_HDR_NTILES] = carry + nti;
+    // every tile's token rows, -1 past its count
+    __syncthreads();
+    const int ntl = carry + nti;
+    for (int it = threadIdx.x; it < ntl * kTile; it += blockDim.x) {
+        const int k = it / kTile, i = it - k * kTile;
+        const int4 t = p.tiles[k];
+        p.tile_rows[it] = i < t.z ? p.perm[t.y + i] : -1;
+    }
 }
 
 __device__ void write_header(const PlanPtrs &p, int T, int L, int kind, int n_active, int G,

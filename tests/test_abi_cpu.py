@@ -51,7 +51,8 @@ def test_plan_layout(lib):
     assert lay["offset"] == 64 + 16 and lay["perm"] == 64 + 16 + 20
     assert lay["tiles"] % 16 == 0
     assert lay["max_tiles"] == 1000 + 1000 // 64 + 2
-    assert lay["bytes"] == lay["tiles"] + 16 * lay["max_tiles"]
+    assert lay["tile_rows"] == lay["tiles"] + 16 * lay["max_tiles"]
+    assert lay["bytes"] == lay["tile_rows"] + 4 * 64 * lay["max_tiles"]
     assert lg.lora_workspace_size(1000, 4) == lay["bytes"]
     assert lg.lora_workspace_size(-1, 4) == 0
     assert lg.lora_workspace_size(10, 0) == 0

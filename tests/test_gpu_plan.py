@@ -33,6 +33,11 @@ def check_plan(lg, plan, T, L, ref, by_adapter, bad_ref=0, err_ref=0):
     np.testing.assert_array_equal(v["group_start"][:G], ref["group_start"])
     np.testing.assert_array_equal(v["group_count"][:G], ref["group_count"])
     np.testing.assert_array_equal(v["tiles"][:nt], ref["tiles"])
+    # per-tile row lists: perm[first : first + count], -1 padded
+    for k, (l, p0, n, grp) in enumerate(ref["tiles"].tolist()):
+        exp = np.full(lg.TILE_TOKENS, -1)
+        exp[:n] = ref["perm"][p0:p0 + n]
+        np.testing.assert_array_equal(v["tile_rows"][k], exp)
     assert lg.lora_get_error(plan) == (bad_ref, err_ref)
 
 
