@@ -235,11 +235,11 @@ lora_status_t lora_expand_slice(lora_dtype_t dtype, const float *y, int64_t ldy,
  *   out = (add_inputs ? out : 0) + scale_expand * y_s . B_s[l]^T for every slice
  *                                            (as lora_expand_slice with y_slice_stride = R)
  * y [T, ldy >= num_slices*R] is written in full (it is also the fp32 output of
- * the shrink).  When the shapes allow it (R <= 64, num_slices*R <= 128, H, ldx,
- * ldo, R, slice offsets and sizes multiples of 8, 16-byte aligned x, A, out
- * and B_s) one kernel does both steps, a thread-block cluster per plan tile;
- * otherwise the call runs the two operators back to back.  Results agree
- * with the two-operator sequence within fp32 accumulation accuracy.
+ * the shrink).  The two kernels are chained with programmatic dependent
+ * launch: the expand starts while the shrink finishes, reading the plan, out
+ * and B_s early and y only once the shrink's results are visible, so the
+ * pair costs close to one launch.  Results are those of the two-operator
+ * sequence.
  * Errors: those of lora_shrink and lora_expand_slice.
  */
 lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_t ldx, int32_t T,

@@ -37,8 +37,7 @@ cudaError_t init_device(int dev, lora::DeviceInfo *info) {
     if (e != cudaSuccess) return e;
     if ((e = lora::configure_plan_kernels()) != cudaSuccess) return e;
     if ((e = lora::configure_shrink_kernels(info)) != cudaSuccess) return e;
-    if ((e = lora::configure_expand_kernels()) != cudaSuccess) return e;
-    return lora::configure_fused_kernels(*info);
+    return lora::configure_expand_kernels();
 }
 
 // Per-device kernel attributes are set once, on the first call on that device.
@@ -341,42 +340,53 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
     lora_plan_layout(T, L, &lay);
     lora::PlanPtrs p = plan_ptrs(const_cast<void *>(plan), lay);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    lora::FusedArgs f{};
-    f.x = x;
-    f.ldx = ldx;
-    f.T = T;
-    f.H = H;
-    f.A = A;
-    f.L = L;
-    f.R = R;
-    f.S = num_slices;
-    f.ranks = ranks;
-    f.y = y;
-    f.ldy = ldy;
-    f.scale_s = scale_shrink;
-    f.num_slices = num_slices;
+    lora::ShrinkArgs sa;
+    sa.x = x;
+    sa.ldx = ldx;
+    sa.T = T;
+    sa.H = H;
+    sa.A = A;
+    sa.L = L;
+    sa.R = R;
+    sa.S = num_slices;
+    sa.ranks = ranks;
+    sa.y = y;
+    sa.ldy = ldy;
+    sa.scale = scale_shrink;
+    sa.add = 0;
+    sa.hdr = p.hdr;
+    sa.perm = p.perm;
+    sa.tiles = p.tiles;
+    sa.tile_rows = p.tile_rows;
+    sa.max_tiles = (int)lay.max_tiles;
+    lora::ExpandArgs ea{};
+    ea.y = y;
+    ea.ldy = ldy;
+    ea.T = T;
+    ea.out = out;
+    ea.ldo = ldo;
+    ea.L = L;
+    ea.R = R;
+    ea.ranks = ranks;
+    ea.y_slice_stride = R;
+    ea.scale = scale_expand;
+    ea.add = add_inputs ? 1 : 0;
+    ea.num_slices = num_slices;
     for (int k = 0; k < num_slices; ++k) {
-        f.B[k] = B_slices[k];
-        f.N[k] = slice_N[k];
-        f.off[k] = slice_offset[k];
+        ea.B[k] = B_slices[k];
+        ea.N[k] = slice_N[k];
+        ea.off[k] = slice_offset[k];
     }
-    f.out = out;
-    f.ldo = ldo;
-    f.scale = scale_expand;
-    f.add = add_inputs ? 1 : 0;
-    f.hdr = p.hdr;
-    f.perm = p.perm;
-    f.tiles = p.tiles;
-    f.tile_rows = p.tile_rows;
-    f.max_tiles = (int)lay.max_tiles;
-    cudaError_t e = lora::launch_fused(dtype, f, *dev, cs);
-    if (e == cudaErrorNotSupported) {  // shapes outside the fused kernel: two launches
-        if ((st = lora_shrink(dtype, x, ldx, T, H, A, L, R, num_slices, ranks, y, ldy, plan,
-                              scale_shrink, 0, stream)) != LORA_OK)
-            return st;
-        return lora_expand_slice(dtype, y, ldy, T, num_slices, B_slices, slice_N, slice_offset, R,
-                                 L, R, ranks, out, ldo, plan, scale_expand, add_inputs, stream);
-    }
+    ea.hdr = p.hdr;
+    ea.perm = p.perm;
+    ea.tiles = p.tiles;
+    ea.tile_rows = p.tile_rows;
+    ea.max_tiles = (int)lay.max_tiles;
+    // The shrink waits for the caller's previous kernels, then lets the
+    // expand launch early; the expand reads plan, out and B (none written by
+    // the shrink) before its own wait and y after it.
+    cudaError_t e = lora::launch_shrink(dtype, sa, *dev, cs, true);
+    if (e == cudaSuccess) e = lora::launch_expand(dtype, ea, *dev, cs, true);
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "shrink_expand_slice launch");
 }
 

@@ -94,6 +94,11 @@ __device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
                  : "memory");
 }
 
+// Programmatic dependent launch: wait for the previous grid's results; let
+// the next grid start launching.  Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n"); }
+
 __device__ __forceinline__ int clamp_rank(const int32_t *ranks, int l, int R) {
     if (ranks == nullptr) return R;
     int r = __ldg(ranks + l);

@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kThreads)
 expand_kernel(const ExpandArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
+    grid_dep_wait();  // y (and anything else) may come from the previous kernel
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -421,6 +422,10 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     float fscale[MB][2];
     uint32_t ah[MB][KSMAX][4], al[MB][KSMAX][4];
 
+    // As a programmatic dependent of the shrink, everything above (plan, out,
+    // B) overlaps the shrink's tail; y is read only after this wait.
+    grid_dep_wait();
+
     for (int u = u_begin; u < u_end; ++u) {
         // ---- the next unit: position, and its loads issued now
         int nt = t, npart = part, ncbi = cbi + 1;
@@ -550,23 +555,32 @@ cudaError_t query_occ_dtype(int (&occ)[2][4]) {
 int ks_class(int ks) { return ks <= 1 ? 0 : ks <= 2 ? 1 : ks <= 4 ? 2 : 3; }
 
 template <typename E, int KSMAX>
-cudaError_t launch_warp_ks(const ExpandArgs &a, int grid, int tiles_grid, int ncb, cudaStream_t st) {
+cudaError_t launch_warp_ks(const ExpandArgs &a, int grid, int tiles_grid, int ncb, cudaStream_t st,
+                           bool pdl) {
     // 16-byte y loads when every slice's y block starts 16-byte aligned
     const int y_vec = (reinterpret_cast<uintptr_t>(a.y) & 15) == 0 && a.ldy % 4 == 0 &&
                       a.y_slice_stride % 4 == 0;
-    if (a.add) expand_warp_kernel<E, true, KSMAX><<<grid, kWThreads, 0, st>>>(a, tiles_grid, ncb, y_vec);
-    else expand_warp_kernel<E, false, KSMAX><<<grid, kWThreads, 0, st>>>(a, tiles_grid, ncb, y_vec);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kWThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (a.add) return cudaLaunchKernelEx(&cfg, expand_warp_kernel<E, true, KSMAX>, a, tiles_grid, ncb, y_vec);
+    return cudaLaunchKernelEx(&cfg, expand_warp_kernel<E, false, KSMAX>, a, tiles_grid, ncb, y_vec);
 }
 
 template <typename E>
 cudaError_t launch_warp_dtype(const ExpandArgs &a, int grid, int tiles_grid, int ncb,
-                              cudaStream_t st) {
+                              cudaStream_t st, bool pdl) {
     const int ks = (a.R + 15) / 16;
-    if (ks <= 1) return launch_warp_ks<E, 1>(a, grid, tiles_grid, ncb, st);
-    if (ks <= 2) return launch_warp_ks<E, 2>(a, grid, tiles_grid, ncb, st);
-    if (ks <= 4) return launch_warp_ks<E, 4>(a, grid, tiles_grid, ncb, st);
-    return launch_warp_ks<E, 8>(a, grid, tiles_grid, ncb, st);
+    if (ks <= 1) return launch_warp_ks<E, 1>(a, grid, tiles_grid, ncb, st, pdl);
+    if (ks <= 2) return launch_warp_ks<E, 2>(a, grid, tiles_grid, ncb, st, pdl);
+    if (ks <= 4) return launch_warp_ks<E, 4>(a, grid, tiles_grid, ncb, st, pdl);
+    return launch_warp_ks<E, 8>(a, grid, tiles_grid, ncb, st, pdl);
 }
 
 template <typename E>
@@ -587,7 +601,7 @@ cudaError_t configure_expand_kernels() {
 }
 
 cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceInfo &dev,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool pdl) {
     ExpandArgs a = a_in;
     if (a.T == 0) return cudaSuccess;
     // Tiles: ceil(T/64) full-or-partial tiles plus at most one ragged tile per
@@ -613,8 +627,8 @@ cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceI
         const long long warps_max = (long long)dev.sm_count * occ * (kWThreads / 32);
         const long long warps = std::min(units, warps_max);
         const int grid = (int)std::max<long long>(1, (warps + 3) / 4);
-        return dt == LORA_F16 ? launch_warp_dtype<__half>(a, grid, tiles_grid, ncb, stream)
-                              : launch_warp_dtype<__nv_bfloat16>(a, grid, tiles_grid, ncb, stream);
+        return dt == LORA_F16 ? launch_warp_dtype<__half>(a, grid, tiles_grid, ncb, stream, pdl)
+                              : launch_warp_dtype<__nv_bfloat16>(a, grid, tiles_grid, ncb, stream, pdl);
     }
 
     // Generic path: 128-column chunks per slice

@@ -56,33 +56,6 @@ struct ExpandArgs {
     int max_tiles;
 };
 
-// Fused shrink + expand_slice (one thread-block cluster per plan tile).
-struct FusedArgs {
-    const void *x;
-    int64_t ldx;
-    int T, H;
-    const void *A;
-    int L, R, S;
-    const int32_t *ranks;
-    float *y;
-    int64_t ldy;
-    float scale_s;
-    int num_slices;  // expand slices (the shrink stacks S = num_slices slices of R rows)
-    const void *B[LORA_MAX_SLICES];
-    int N[LORA_MAX_SLICES];
-    int off[LORA_MAX_SLICES];
-    int cb_begin[LORA_MAX_SLICES + 1];  // first 32-column block of each slice (prefix sums)
-    void *out;
-    int64_t ldo;
-    float scale;
-    int add;
-    int32_t *hdr;
-    const int32_t *perm;
-    const int4 *tiles;
-    const int32_t *tile_rows;
-    int max_tiles;
-};
-
 struct DeviceInfo {
     int sm_count;
     int max_cluster;  // largest split-K cluster the shrink kernel can be launched with
@@ -96,13 +69,12 @@ cudaError_t launch_group_tokens(const int32_t *idx, int T, int L, const PlanPtrs
                                 cudaStream_t stream);
 cudaError_t launch_group_segments(const int32_t *ss, const int32_t *sl, const int32_t *slo, int S,
                                   int T, int L, const PlanPtrs &p, cudaStream_t stream);
+// pdl: launch as a programmatic dependent of the previous kernel in the
+// stream (the kernel's own griddepcontrol.wait guards every read of data the
+// previous kernels produce).  Only for launches whose predecessor is known.
 cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo &dev,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool pdl = false);
 cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a, const DeviceInfo &dev,
-                          cudaStream_t stream);
-cudaError_t configure_fused_kernels(const DeviceInfo &dev);
-// Returns cudaErrorNotSupported when the shapes need the two-kernel path.
-cudaError_t launch_fused(lora_dtype_t dt, const FusedArgs &a, const DeviceInfo &dev,
-                         cudaStream_t stream);
+                          cudaStream_t stream, bool pdl = false);
 
 }  // namespace lora

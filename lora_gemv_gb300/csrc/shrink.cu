@@ -123,6 +123,12 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
     const int kc = blockIdx.x, ksplit = gridDim.x, rc = blockIdx.z;
     cg::cluster_group cluster = cg::this_cluster();
 
+    // Everything this kernel reads may come from the previous kernels; once
+    // they are done, a dependent expand may start (it reads y only after its
+    // own wait, i.e. after this grid completes).
+    grid_dep_wait();
+    grid_dep_launch();
+
     // Every CTA of a cluster takes the same branches: the plan check reads the
     // same words, and the tile loop depends only on blockIdx.y / blockIdx.z.
     // The plan header and this CTA's first tile are read together.
@@ -303,32 +309,57 @@ cudaError_t configure_vec(int max_cluster) {
     return configure_one<E, VEC, 16>(max_cluster);
 }
 
+// Resident CTAs per SM of each instantiation at its largest shared memory,
+// [dtype][vec][n-tile class], filled by configure_shrink_kernels.
+int g_occ[2][2][4] = {};
+
+template <typename E, bool VEC, int NTMAX>
+cudaError_t occ_one(int &occ) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, shrink_kernel<E, VEC, NTMAX>, kThreads, smem_bytes(NTMAX * 8 < kRows ? NTMAX * 8 : kRows, NTMAX));
+}
+
+template <typename E>
+cudaError_t occ_dtype(int (&occ)[2][4]) {
+    cudaError_t e;
+    if ((e = occ_one<E, false, 2>(occ[0][0])) != cudaSuccess) return e;
+    if ((e = occ_one<E, false, 4>(occ[0][1])) != cudaSuccess) return e;
+    if ((e = occ_one<E, false, 8>(occ[0][2])) != cudaSuccess) return e;
+    if ((e = occ_one<E, false, 16>(occ[0][3])) != cudaSuccess) return e;
+    if ((e = occ_one<E, true, 2>(occ[1][0])) != cudaSuccess) return e;
+    if ((e = occ_one<E, true, 4>(occ[1][1])) != cudaSuccess) return e;
+    if ((e = occ_one<E, true, 8>(occ[1][2])) != cudaSuccess) return e;
+    return occ_one<E, true, 16>(occ[1][3]);
+}
+
 template <typename E, bool VEC, int NTMAX>
 cudaError_t launch_nt(const ShrinkArgs &a, int ksplit, int kchunk, int rows_cap, dim3 grid,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem_bytes(rows_cap, NTMAX);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = ksplit;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, shrink_kernel<E, VEC, NTMAX>, a, kchunk, rows_cap);
 }
 
 template <typename E, bool VEC>
 cudaError_t launch_vec(const ShrinkArgs &a, int ksplit, int kchunk, int rows_cap, dim3 grid,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, bool pdl) {
     const int nt = rows_cap / 8;
-    if (nt <= 2) return launch_nt<E, VEC, 2>(a, ksplit, kchunk, rows_cap, grid, stream);
-    if (nt <= 4) return launch_nt<E, VEC, 4>(a, ksplit, kchunk, rows_cap, grid, stream);
-    if (nt <= 8) return launch_nt<E, VEC, 8>(a, ksplit, kchunk, rows_cap, grid, stream);
-    return launch_nt<E, VEC, 16>(a, ksplit, kchunk, rows_cap, grid, stream);
+    if (nt <= 2) return launch_nt<E, VEC, 2>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
+    if (nt <= 4) return launch_nt<E, VEC, 4>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
+    if (nt <= 8) return launch_nt<E, VEC, 8>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
+    return launch_nt<E, VEC, 16>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
 }
 
 }  // namespace
@@ -365,11 +396,13 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
     if ((e = configure_vec<__half, true>(max_cluster)) != cudaSuccess) return e;
     if ((e = configure_vec<__half, false>(max_cluster)) != cudaSuccess) return e;
     if ((e = configure_vec<__nv_bfloat16, true>(max_cluster)) != cudaSuccess) return e;
-    return configure_vec<__nv_bfloat16, false>(max_cluster);
+    if ((e = configure_vec<__nv_bfloat16, false>(max_cluster)) != cudaSuccess) return e;
+    if ((e = occ_dtype<__half>(g_occ[LORA_F16])) != cudaSuccess) return e;
+    return occ_dtype<__nv_bfloat16>(g_occ[LORA_BF16]);
 }
 
 cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo &dev,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool pdl) {
     if (a.T == 0) return cudaSuccess;
     const bool vec = (reinterpret_cast<uintptr_t>(a.x) & 15) == 0 &&
                      (reinterpret_cast<uintptr_t>(a.A) & 15) == 0 && a.ldx % 8 == 0 &&
@@ -381,13 +414,15 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     const int gz = (a.S * a.R + kRows - 1) / kRows;
     const int rows_cap = std::min(kRows, (a.S * a.R + 15) / 16 * 16);
     const int ntmax = rows_cap / 8 <= 2 ? 2 : rows_cap / 8 <= 4 ? 4 : rows_cap / 8 <= 8 ? 8 : 16;
-    // CTAs resident per SM (shared memory; 256 threads)
-    const int per_sm = std::max(1, std::min(4, (227 * 1024) / (smem_bytes(rows_cap, ntmax) + 1024)));
-    // Split K across a cluster so that the grid fills the resident slots,
-    // each CTA keeping >= 2 stages of work.
-    const int target = per_sm * dev.sm_count;
+    // CTAs resident per SM (registers and shared memory)
+    const int ntc = ntmax == 2 ? 0 : ntmax == 4 ? 1 : ntmax == 8 ? 2 : 3;
+    const int per_sm = std::max(1, g_occ[dt][vec ? 1 : 0][ntc]);
+    // Split K across a cluster so that the whole grid is resident at once
+    // (one wave; a cluster needs all its CTAs placed together, so keep some
+    // slack), each CTA keeping >= 2 stages of work.
+    const long long slots = (long long)per_sm * dev.sm_count * 3 / 4;
     int ksplit = 1;
-    while (ksplit < dev.max_cluster && (long long)gy * gz * ksplit * 2 <= target &&
+    while (ksplit < dev.max_cluster && (long long)gy * gz * ksplit * 2 <= slots &&
            a.H / (ksplit * 2) >= 2 * kK)
         ksplit *= 2;
     int kchunk = ((a.H + ksplit - 1) / ksplit + kK - 1) / kK * kK;
@@ -395,10 +430,10 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     kchunk = ((a.H + ksplit - 1) / ksplit + kK - 1) / kK * kK;
     dim3 grid(ksplit, gy, gz);
     if (dt == LORA_F16)
-        return vec ? launch_vec<__half, true>(a, ksplit, kchunk, rows_cap, grid, stream)
-                   : launch_vec<__half, false>(a, ksplit, kchunk, rows_cap, grid, stream);
-    return vec ? launch_vec<__nv_bfloat16, true>(a, ksplit, kchunk, rows_cap, grid, stream)
-               : launch_vec<__nv_bfloat16, false>(a, ksplit, kchunk, rows_cap, grid, stream);
+        return vec ? launch_vec<__half, true>(a, ksplit, kchunk, rows_cap, grid, stream, pdl)
+                   : launch_vec<__half, false>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
+    return vec ? launch_vec<__nv_bfloat16, true>(a, ksplit, kchunk, rows_cap, grid, stream, pdl)
+               : launch_vec<__nv_bfloat16, false>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
 }
 
 }  // namespace lora
