@@ -110,69 +110,6 @@ __device__ __forceinline__ void store_stage(const uint4 (&ld)[kMaxLd], unsigned 
     }
 }
 
-// Tile epilogue shared by the shrink kernels: warp partials -> P[warp], the
-// CTA partial Ct (sum over the warps that split a 16-row block, in warp
-// order), then the cluster sum through distributed shared memory in rank
-// order, CTA kc finishing a 1/ksplit share of the tile's elements into y.
-template <int NTMAX, int NWARPS>
-__device__ __forceinline__ void reduce_tile(const ShrinkArgs &a, cg::cluster_group &cluster,
-                                            float *P, const float (&acc)[NTMAX][4], bool wact,
-                                            int warp, int g, int q, int NT, int n, int nrows,
-                                            int nmbp, int kparts, int kc, int ksplit,
-                                            const int *s_rows, const int *s_arow) {
-    constexpr int PP = part_pitch(NTMAX);
-    float *Ct = P + NWARPS * 16 * PP;
-    if (wact) {
-        float *pw = P + warp * 16 * PP;
-#pragma unroll
-        for (int nt = 0; nt < NTMAX; ++nt) {
-            if (nt < NT) {
-                const int cc = nt * 8 + 2 * q;
-                pw[g * PP + cc] = acc[nt][0];
-                pw[g * PP + cc + 1] = acc[nt][1];
-                pw[(g + 8) * PP + cc] = acc[nt][2];
-                pw[(g + 8) * PP + cc + 1] = acc[nt][3];
-            }
-        }
-    }
-    __syncthreads();
-    for (int it = threadIdx.x; it < n * nrows; it += NWARPS * 32) {
-        const int i = it / nrows, j = it - i * nrows;
-        const int m = i >> 4, r = i & 15;
-        float sum = 0.f;
-        for (int k = 0; k < kparts; ++k) sum += P[((k * nmbp + m) * 16 + r) * PP + j];
-        Ct[i * PP + j] = sum;
-    }
-    if (ksplit > 1) cluster.sync();
-    else __syncthreads();
-    const int E_ = n * nrows;
-    const int e0 = (int)((long long)E_ * kc / ksplit), e1 = (int)((long long)E_ * (kc + 1) / ksplit);
-    for (int it = e0 + threadIdx.x; it < e1; it += NWARPS * 32) {
-        const int i = it / nrows, c = it - i * nrows;
-        float part[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            part[r] = 0.f;
-            if (r < ksplit) {
-                const float *src = ksplit > 1 ? cluster.map_shared_rank(Ct, r) : Ct;
-                part[r] = src[i * PP + c];
-            }
-        }
-        float sum = 0.f;
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-            if (r < ksplit) sum += part[r];
-        const int row = s_rows[i];
-        if (row >= 0) {
-            float *yp = a.y + (int64_t)row * a.ldy + s_arow[c];
-            const float v = a.scale * sum;
-            *yp = a.add ? *yp + v : v;
-        }
-    }
-    if (ksplit > 1) cluster.sync();
-    else __syncthreads();
-}
-
 template <typename E, bool VEC, int NTMAX>
 __global__ void __launch_bounds__(kThreads)
 shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
@@ -211,7 +148,8 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
     const int h_end = min(H, h_begin + kchunk);
     const int nstages = h_end > h_begin ? (h_end - h_begin + kK - 1) / kK : 0;
     const int stage_bytes = (kTile + rows_cap) * kK * 2;
-    float *P = reinterpret_cast<float *>(smem);             // [kWarps][16][PP], then Ct [64][PP]
+    float *P = reinterpret_cast<float *>(smem);             // [kWarps][16][PP]
+    float *Ct = P + kWarps * 16 * PP;                        // [64][PP]
 
     const int n_tiles = min(h1.z, a.max_tiles);
     for (int tile = blockIdx.y; tile < n_tiles; tile += gridDim.y) {
@@ -293,185 +231,61 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
             __syncthreads();
         }
 
-        reduce_tile<NTMAX, kWarps>(a, cluster, P, acc, wact, warp, g, q, NT, n, nrows, nmbp, kparts,
-                                    kc, ksplit, s_rows, s_arow);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// TMA shrink (aligned rows: H, ldx multiples of 8, 16-byte aligned x and A).
-// Each stage of a CTA's H range is one bulk copy per x row and per live A
-// row (kTK elements), issued by one warp and completed on an mbarrier, two
-// stages in flight: a CTA's whole H range is requested at once for the
-// decode split-K shapes, and no registers are spent on data in flight.
-constexpr int kTThreads = 128;           // 4 warps
-constexpr int kTWarps = kTThreads / 32;
-constexpr int kTK = 128;                 // H elements per stage
-constexpr int kTPitch = kTK + 8;         // elements per shared row: 272 B, conflict-free ldmatrix
-
-__host__ __device__ constexpr int tma_buf_bytes(int rows_cap) { return (kTile + rows_cap) * kTPitch * 2; }
-__host__ __device__ constexpr int tma_smem_bytes(int rows_cap, int ntmax) {
-    const int bufs = 2 * tma_buf_bytes(rows_cap);
-    const int parts = (kTWarps * 16 + kTile) * part_pitch(ntmax) * 4;
-    return bufs > parts ? bufs : parts;
-}
-
-template <typename E, int NTMAX>
-__global__ void __launch_bounds__(kTThreads)
-shrink_tma_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
-    extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ int s_rows[kTile];
-    __shared__ int s_arow[kRows];
-    __shared__ __align__(8) uint64_t bars[2];
-    __shared__ int s_fail;
-
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, q = lane & 3;
-    const int kc = blockIdx.x, ksplit = gridDim.x, rc = blockIdx.z;
-    cg::cluster_group cluster = cg::this_cluster();
-
-    grid_dep_wait();
-    grid_dep_launch();
-
-    const int4 h0 = __ldcg(reinterpret_cast<const int4 *>(a.hdr));
-    const int4 h1 = __ldcg(reinterpret_cast<const int4 *>(a.hdr) + 1);
-    int4 tl_next = (int)blockIdx.y < a.max_tiles ? __ldcg(a.tiles + blockIdx.y)
-                                                 : make_int4(-1, 0, 0, -1);
-    if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
-        if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
-            atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
-        return;
-    }
-    if (threadIdx.x == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        s_fail = 0;
-        mbar_init_fence();
-    }
-    __syncthreads();
-
-    const E *__restrict__ x = static_cast<const E *>(a.x);
-    const int H = a.H, R = a.R, S = a.S;
-    const int h_begin = kc * kchunk;
-    const int h_end = min(H, h_begin + kchunk);
-    const int nstages = h_end > h_begin ? (h_end - h_begin + kTK - 1) / kTK : 0;
-    const int bbytes = tma_buf_bytes(rows_cap);
-    float *P = reinterpret_cast<float *>(smem);  // after the stages: partials
-    uint32_t uses0 = 0, uses1 = 0;               // completed phases of each buffer's barrier
-
-    const int n_tiles = min(h1.z, a.max_tiles);
-    for (int tile = blockIdx.y; tile < n_tiles; tile += gridDim.y) {
-        const int4 tl = tl_next;
-        if (tile + (int)gridDim.y < n_tiles) tl_next = __ldcg(a.tiles + tile + gridDim.y);
-        const int l = tl.x, n = tl.z;
-        const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
-        int my_row = threadIdx.x < kTile ? __ldcg(a.tile_rows + (int64_t)tile * kTile + threadIdx.x) : -1;
-        if (my_row >= a.T) my_row = -1;
-
-        if (!a.add && kc == 0 && rc == 0 && rl < R) {
-            for (int it = threadIdx.x; it < n * S * R; it += kTThreads) {
-                const int i = it / (S * R), j = it % (S * R);
-                if (j % R < rl) continue;
-                const int row = __ldcg(a.tile_rows + (int64_t)tile * kTile + i);
-                if (row >= 0 && row < a.T) a.y[(int64_t)row * a.ldy + j] = 0.f;
+        // warp partials -> P[warp], then the CTA partial summed in warp order
+        if (wact) {
+            float *pw = P + warp * 16 * PP;
+#pragma unroll
+            for (int nt = 0; nt < NTMAX; ++nt) {
+                if (nt < NT) {
+                    const int cc = nt * 8 + 2 * q;
+                    pw[g * PP + cc] = acc[nt][0];
+                    pw[g * PP + cc + 1] = acc[nt][1];
+                    pw[(g + 8) * PP + cc] = acc[nt][2];
+                    pw[(g + 8) * PP + cc + 1] = acc[nt][3];
+                }
             }
-        }
-        const int row0 = rc * kRows;
-        const int nrows = min(kRows, S * rl - row0);
-        if (nrows <= 0) continue;
-
-        if (threadIdx.x < kTile) s_rows[threadIdx.x] = threadIdx.x < n ? my_row : -1;
-        for (int t = threadIdx.x; t < kRows; t += kTThreads) {
-            const int c = row0 + t;
-            s_arow[t] = t < nrows ? (c / rl) * R + c % rl : 0;
         }
         __syncthreads();
-        const E *Al = static_cast<const E *>(a.A) + (int64_t)l * S * R * H;
-
-        // Stage st -> buffer st & 1.  The 16-byte chunk after a stage's last
-        // element is zeroed (generic stores, before the copy is issued) when
-        // the stage length is not a multiple of 16, so the last k step reads zeros.
-        auto issue = [&](int st) {
-            unsigned char *buf = smem + (st & 1) * bbytes;
-            uint64_t *bar = &bars[st & 1];
-            const int hs = h_begin + st * kTK;
-            const int len = min(kTK, h_end - hs);
-            if (len % 16 != 0) {
-                for (int r = threadIdx.x; r < kTile + nrows; r += kTThreads) {
-                    E *rowp = reinterpret_cast<E *>(buf) + r * kTPitch + len;
-                    *reinterpret_cast<uint4 *>(rowp) = make_uint4(0, 0, 0, 0);
-                }
-            }
-            fence_proxy_async();
-            __syncthreads();
-            if (warp == 0) {
-                int nx = 0;
-                for (int r = 0; r < kTile; ++r) nx += s_rows[r] >= 0;  // uniform over the warp
-                if (lane == 0) mbar_expect_tx(bar, (uint32_t)(nx + nrows) * len * 2);
-                __syncwarp();
-                for (int r = lane; r < kTile + nrows; r += 32) {
-                    if (r < kTile) {
-                        const int row = s_rows[r];
-                        if (row >= 0)
-                            bulk_g2s(buf + r * kTPitch * 2, x + (int64_t)row * a.ldx + hs, len * 2, bar);
-                    } else {
-                        const int ar = r - kTile;
-                        bulk_g2s(buf + r * kTPitch * 2, Al + (int64_t)s_arow[ar] * H + hs, len * 2, bar);
-                    }
-                }
-            }
-        };
-
-        const int NT = (nrows + 7) / 8;
-        const int nmb = (n + 15) / 16;
-        const int nmbp = nmb <= 1 ? 1 : (nmb <= 2 ? 2 : 4);
-        const int kparts = kTWarps / nmbp;
-        const int mb = warp % nmbp, kp = warp / nmbp;
-        const bool wact = mb < nmb && warp < nmbp * kparts;
-
-        float acc[NTMAX][4];
-#pragma unroll
-        for (int i = 0; i < NTMAX; ++i)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
-
-        if (nstages > 0) issue(0);
-        if (nstages > 1) issue(1);
-        for (int st = 0; st < nstages; ++st) {
-            const int b = st & 1;
-            const uint32_t parity = (b ? uses1 : uses0) & 1;
-            if (!mbar_wait_bounded(&bars[b], parity)) s_fail = 1;
-            if (b) ++uses1;
-            else ++uses0;
-            const int len = min(kTK, h_end - (h_begin + st * kTK));
-            const int KK = (len + 15) / 16;
-            const int kk0 = kp * KK / kparts, kk1 = (kp + 1) * KK / kparts;
-            if (wact) {
-                const E *bx = reinterpret_cast<const E *>(smem + b * bbytes);
-                const E *ba = bx + kTile * kTPitch;
-                for (int kk = kk0; kk < kk1; ++kk) {
-                    uint32_t af[4];
-                    const int ar = mb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-                    ldmatrix_x4(af, smem_u32(bx + ar * kTPitch + kk * 16 + 8 * (lane >> 4)));
-#pragma unroll
-                    for (int np = 0; np < NTMAX / 2; ++np) {
-                        if (2 * np < NT) {
-                            uint32_t bf[4];
-                            const int br = 8 * (2 * np + (lane >> 4)) + (lane & 7);
-                            ldmatrix_x4(bf, smem_u32(ba + br * kTPitch + kk * 16 + 8 * ((lane >> 3) & 1)));
-                            mma16816<E>(acc[2 * np], af, bf[0], bf[1]);
-                            if (2 * np + 1 < NT) mma16816<E>(acc[2 * np + 1], af, bf[2], bf[3]);
-                        }
-                    }
-                }
-            }
-            __syncthreads();  // buffer b is free again
-            if (st + 2 < nstages) issue(st + 2);
+        for (int it = threadIdx.x; it < n * nrows; it += kThreads) {
+            const int i = it / nrows, j = it - i * nrows;
+            const int m = i >> 4, r = i & 15;
+            float sum = 0.f;
+            for (int k = 0; k < kparts; ++k) sum += P[((k * nmbp + m) * 16 + r) * PP + j];
+            Ct[i * PP + j] = sum;
         }
-        reduce_tile<NTMAX, kTWarps>(a, cluster, P, acc, wact, warp, g, q, NT, n, nrows, nmbp,
-                                    kparts, kc, ksplit, s_rows, s_arow);
+        if (ksplit > 1) cluster.sync();
+        else __syncthreads();
+
+        // fixed-order reduction over the cluster; CTA kc finishes a 1/ksplit share
+        {
+            const int E_ = n * nrows;
+            const int e0 = (int)((long long)E_ * kc / ksplit), e1 = (int)((long long)E_ * (kc + 1) / ksplit);
+            for (int it = e0 + threadIdx.x; it < e1; it += kThreads) {
+                const int i = it / nrows, c = it - i * nrows;
+                float part[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    part[r] = 0.f;
+                    if (r < ksplit) {
+                        const float *src = ksplit > 1 ? cluster.map_shared_rank(Ct, r) : Ct;
+                        part[r] = src[i * PP + c];
+                    }
+                }
+                float sum = 0.f;
+#pragma unroll
+                for (int r = 0; r < 16; ++r)
+                    if (r < ksplit) sum += part[r];
+                const int row = s_rows[i];
+                if (row >= 0) {
+                    float *yp = a.y + (int64_t)row * a.ldy + s_arow[c];
+                    const float v = a.scale * sum;
+                    *yp = a.add ? *yp + v : v;
+                }
+            }
+        }
+        if (ksplit > 1) cluster.sync();
+        else __syncthreads();
     }
-    if (threadIdx.x == 0 && s_fail) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
 }
 
 template <typename E, bool VEC, int NTMAX>
@@ -486,32 +300,13 @@ cudaError_t configure_one(int max_cluster) {
     return e;
 }
 
-template <typename E, int NTMAX>
-cudaError_t configure_tma_one(int max_cluster) {
-    cudaError_t e = cudaFuncSetAttribute(shrink_tma_kernel<E, NTMAX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         tma_smem_bytes(kRows, NTMAX));
-    if (e != cudaSuccess) return e;
-    if (max_cluster > 8)
-        e = cudaFuncSetAttribute(shrink_tma_kernel<E, NTMAX>,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    return e;
-}
-
-// VEC = true: the TMA kernel; VEC = false: the register-staged generic kernel.
 template <typename E, bool VEC>
 cudaError_t configure_vec(int max_cluster) {
     cudaError_t e;
-    if (VEC) {
-        if ((e = configure_tma_one<E, 2>(max_cluster)) != cudaSuccess) return e;
-        if ((e = configure_tma_one<E, 4>(max_cluster)) != cudaSuccess) return e;
-        if ((e = configure_tma_one<E, 8>(max_cluster)) != cudaSuccess) return e;
-        return configure_tma_one<E, 16>(max_cluster);
-    }
-    if ((e = configure_one<E, false, 2>(max_cluster)) != cudaSuccess) return e;
-    if ((e = configure_one<E, false, 4>(max_cluster)) != cudaSuccess) return e;
-    if ((e = configure_one<E, false, 8>(max_cluster)) != cudaSuccess) return e;
-    return configure_one<E, false, 16>(max_cluster);
+    if ((e = configure_one<E, VEC, 2>(max_cluster)) != cudaSuccess) return e;
+    if ((e = configure_one<E, VEC, 4>(max_cluster)) != cudaSuccess) return e;
+    if ((e = configure_one<E, VEC, 8>(max_cluster)) != cudaSuccess) return e;
+    return configure_one<E, VEC, 16>(max_cluster);
 }
 
 // Resident CTAs per SM of each instantiation at its largest shared memory,
@@ -520,12 +315,8 @@ int g_occ[2][2][4] = {};
 
 template <typename E, bool VEC, int NTMAX>
 cudaError_t occ_one(int &occ) {
-    const int rc = NTMAX * 8 < kRows ? NTMAX * 8 : kRows;
-    if (VEC)
-        return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, shrink_tma_kernel<E, NTMAX>,
-                                                             kTThreads, tma_smem_bytes(rc, NTMAX));
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, shrink_kernel<E, false, NTMAX>,
-                                                         kThreads, smem_bytes(rc, NTMAX));
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, shrink_kernel<E, VEC, NTMAX>, kThreads, smem_bytes(NTMAX * 8 < kRows ? NTMAX * 8 : kRows, NTMAX));
 }
 
 template <typename E>
@@ -546,8 +337,8 @@ cudaError_t launch_nt(const ShrinkArgs &a, int ksplit, int kchunk, int rows_cap,
                       cudaStream_t stream, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(VEC ? kTThreads : kThreads);
-    cfg.dynamicSmemBytes = VEC ? tma_smem_bytes(rows_cap, NTMAX) : smem_bytes(rows_cap, NTMAX);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes(rows_cap, NTMAX);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -558,8 +349,7 @@ cudaError_t launch_nt(const ShrinkArgs &a, int ksplit, int kchunk, int rows_cap,
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    if (VEC) return cudaLaunchKernelEx(&cfg, shrink_tma_kernel<E, NTMAX>, a, kchunk, rows_cap);
-    return cudaLaunchKernelEx(&cfg, shrink_kernel<E, false, NTMAX>, a, kchunk, rows_cap);
+    return cudaLaunchKernelEx(&cfg, shrink_kernel<E, VEC, NTMAX>, a, kchunk, rows_cap);
 }
 
 template <typename E, bool VEC>
@@ -578,10 +368,10 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
     // Largest cluster the GPU can hold with this kernel's largest shared memory.
     int max_cluster = 8;
     {
-        cudaError_t e = cudaFuncSetAttribute(shrink_kernel<__half, false, 16>,
+        cudaError_t e = cudaFuncSetAttribute(shrink_kernel<__half, true, 16>,
                                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(shrink_kernel<__half, false, 16>,
+            e = cudaFuncSetAttribute(shrink_kernel<__half, true, 16>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(kRows, 16));
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
@@ -596,7 +386,7 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, shrink_kernel<__half, false, 16>, &cfg) == cudaSuccess &&
+        if (cudaOccupancyMaxActiveClusters(&n, shrink_kernel<__half, true, 16>, &cfg) == cudaSuccess &&
             n > 0)
             max_cluster = 16;
         cudaGetLastError();  // a refused query is not an error: fall back to 8
@@ -632,13 +422,12 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     // slack), each CTA keeping >= 2 stages of work.
     const long long slots = (long long)per_sm * dev.sm_count * 3 / 4;
     int ksplit = 1;
-    const int kgran = vec ? kTK : kK;  // H per stage
     while (ksplit < dev.max_cluster && (long long)gy * gz * ksplit * 2 <= slots &&
-           a.H / (ksplit * 2) >= 2 * kgran)
+           a.H / (ksplit * 2) >= 2 * kK)
         ksplit *= 2;
-    int kchunk = ((a.H + ksplit - 1) / ksplit + kgran - 1) / kgran * kgran;
+    int kchunk = ((a.H + ksplit - 1) / ksplit + kK - 1) / kK * kK;
     while (ksplit > 1 && (long long)(ksplit - 1) * kchunk >= a.H) ksplit /= 2;  // no empty CTAs
-    kchunk = ((a.H + ksplit - 1) / ksplit + kgran - 1) / kgran * kgran;
+    kchunk = ((a.H + ksplit - 1) / ksplit + kK - 1) / kK * kK;
     dim3 grid(ksplit, gy, gz);
     if (dt == LORA_F16)
         return vec ? launch_vec<__half, true>(a, ksplit, kchunk, rows_cap, grid, stream, pdl)
