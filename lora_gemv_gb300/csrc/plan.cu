@@ -11,6 +11,8 @@
 //
 // Both kernels run as ONE block of 1024 threads: the inputs are at most a few
 // hundred KB of int32 and the result feeds every LoRA layer of a step.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -22,8 +24,11 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPlanWarps = kPlanThreads / 32;
 
 // Cut groups [0, G) into tiles of <= kTile tokens, then the inactive tokens
-// perm[n_active, T).  Group arrays must be visible to the whole block.
-__device__ void emit_tiles(const PlanPtrs &p, int T, int n_active, int G, int *ws) {
+// perm[n_active, T), and write each tile's token rows.  Group arrays must be
+// visible to the whole block.  With perm_s / tiles_s (shared copies of perm
+// and room for the tile records) the row lists are built from shared memory.
+__device__ void emit_tiles(const PlanPtrs &p, int T, int n_active, int G, int *ws,
+                           const int *perm_s = nullptr, int4 *tiles_s = nullptr) {
     int carry = 0;
     for (int base = 0; base < G; base += blockDim.x) {  // block-uniform loop
         const int g = base + threadIdx.x;
@@ -33,8 +38,11 @@ __device__ void emit_tiles(const PlanPtrs &p, int T, int n_active, int G, int *w
         const int ex = block_exclusive_scan(nt, ws, &total);
         if (g < G) {
             const int st = p.group_start[g], lo = p.group_lora[g];
-            for (int k = 0; k < nt; ++k)
-                p.tiles[carry + ex + k] = make_int4(lo, st + k * kTile, min(kTile, cnt - k * kTile), g);
+            for (int k = 0; k < nt; ++k) {
+                const int4 tr = make_int4(lo, st + k * kTile, min(kTile, cnt - k * kTile), g);
+                p.tiles[carry + ex + k] = tr;
+                if (tiles_s) tiles_s[carry + ex + k] = tr;
+            }
         }
         carry += total;
     }
@@ -42,7 +50,9 @@ __device__ void emit_tiles(const PlanPtrs &p, int T, int n_active, int G, int *w
     const int nti = (n_in + kTile - 1) / kTile;
     for (int k = threadIdx.x; k < nti; k += blockDim.x) {
         const int p0 = n_active + k * kTile;
-        p.tiles[carry + k] = make_int4(-1, p0, min(kTile, T - p0), -1);
+        const int4 tr = make_int4(-1, p0, min(kTile, T - p0), -1);
+        p.tiles[carry + k] = tr;
+        if (tiles_s) tiles_s[carry + k] = tr;
     }
     if (threadIdx.x == 0) p.hdr[LORA_HDR_NTILES] = carry + nti;
     // every tile's token rows, -1 past its count
@@ -50,8 +60,8 @@ __device__ void emit_tiles(const PlanPtrs &p, int T, int n_active, int G, int *w
     const int ntl = carry + nti;
     for (int it = threadIdx.x; it < ntl * kTile; it += blockDim.x) {
         const int k = it / kTile, i = it - k * kTile;
-        const int4 t = p.tiles[k];
-        p.tile_rows[it] = i < t.z ? p.perm[t.y + i] : -1;
+        const int4 t = tiles_s ? tiles_s[k] : p.tiles[k];
+        p.tile_rows[it] = i < t.z ? (perm_s ? perm_s[t.y + i] : p.perm[t.y + i]) : -1;
     }
 }
 
@@ -75,16 +85,25 @@ __device__ void write_header(const PlanPtrs &p, int T, int L, int kind, int n_ac
 // a private histogram per warp, a scan over (adapter, warp) gives every warp
 // its first slot per adapter, pass 2 places tokens using match_any ranks so
 // equal ids keep their token order.  Shared memory: kPlanWarps * L ints.
-template <int NW>
+// STAGED (small batches): idx and perm live in shared memory (one coalesced
+// read of idx, no dependent global reads afterwards); shared layout
+// [kPlanWarps][L] histogram, idx[T], perm[T], tile records.
+template <int NW, bool STAGED>
 __global__ void __launch_bounds__(NW * 32, 1)
-group_tokens_kernel(const int32_t *__restrict__ idx, int T, int L, PlanPtrs p) {
+group_tokens_kernel(const int32_t *__restrict__ idx_g, int T, int L, PlanPtrs p) {
     constexpr int kPlanWarps = NW;
     extern __shared__ int hist[];  // [kPlanWarps][L]
     __shared__ int ws[40];
     __shared__ int s_inact[kPlanWarps];
     __shared__ int s_bad;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int *idx_s = hist + kPlanWarps * L;  // STAGED only
+    int *perm_s = idx_s + T;
+    int4 *tiles_s = reinterpret_cast<int4 *>(perm_s + T + ((T & 3) ? 4 - (T & 3) : 0));
+    const int32_t *idx = STAGED ? idx_s : idx_g;
 
+    if (STAGED)
+        for (int t = threadIdx.x; t < T; t += blockDim.x) idx_s[t] = __ldg(idx_g + t);
     for (int i = threadIdx.x; i < kPlanWarps * L; i += blockDim.x) hist[i] = 0;
     if (threadIdx.x == 0) s_bad = 0;
     __syncthreads();
@@ -99,7 +118,7 @@ group_tokens_kernel(const int32_t *__restrict__ idx, int T, int L, PlanPtrs p) {
         const bool live = t < t_end;
         int id = -1;
         if (live) {
-            const int v = __ldg(idx + t);
+            const int v = STAGED ? idx[t] : __ldg(idx + t);
             if (v >= 0 && v < L) id = v;
             else if (v != -1) bad++;
         }
@@ -147,7 +166,7 @@ group_tokens_kernel(const int32_t *__restrict__ idx, int T, int L, PlanPtrs p) {
         const bool live = t < t_end;
         int id = -1;
         if (live) {
-            const int v = __ldg(idx + t);
+            const int v = STAGED ? idx[t] : __ldg(idx + t);
             if (v >= 0 && v < L) id = v;
         }
         const unsigned peers = __match_any_sync(0xffffffffu, live ? id : -2);
@@ -155,6 +174,7 @@ group_tokens_kernel(const int32_t *__restrict__ idx, int T, int L, PlanPtrs p) {
         if (live) {
             const int pos = id >= 0 ? my_hist[id] + __popc(peers & lt) : ibase + __popc(inact & lt);
             p.perm[pos] = t;
+            if (STAGED) perm_s[pos] = t;
         }
         __syncwarp();
         if (live && id >= 0 && lane == __ffs(peers) - 1) my_hist[id] += __popc(peers);
@@ -172,7 +192,8 @@ group_tokens_kernel(const int32_t *__restrict__ idx, int T, int L, PlanPtrs p) {
         p.group_count[gi] = cnt;
     }
     __syncthreads();
-    emit_tiles(p, T, n_active, G, ws);
+    if (STAGED) emit_tiles(p, T, n_active, G, ws, perm_s, tiles_s);
+    else emit_tiles(p, T, n_active, G, ws);
     write_header(p, T, L, 1, n_active, G, s_bad, 0);
 }
 
@@ -318,20 +339,30 @@ static_assert(LORA_MAX_ADAPTERS <= kPlanThreads, "one thread per adapter");
 constexpr int kSmallWarps = 8;
 constexpr int kSmallMaxT = 8192;
 
+// Shared memory of the staged variant: histogram, idx, perm, tile records.
+size_t staged_smem(int T, int L) {
+    const size_t tiles = (size_t)(T / kTile + std::min(L, T) + 2);
+    return sizeof(int) * ((size_t)kSmallWarps * L + 2 * (size_t)T + 4) + 16 * tiles;
+}
+
 cudaError_t configure_plan_kernels() {
-    return cudaFuncSetAttribute(group_tokens_kernel<kPlanWarps>,
+    cudaError_t e = cudaFuncSetAttribute(group_tokens_kernel<kPlanWarps, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(int) * kPlanWarps * LORA_MAX_ADAPTERS));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(group_tokens_kernel<kSmallWarps, true>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)(sizeof(int) * kPlanWarps * LORA_MAX_ADAPTERS));
+                                (int)staged_smem(kSmallMaxT, kSmallWarps * 32));
 }
 
 cudaError_t launch_group_tokens(const int32_t *idx, int T, int L, const PlanPtrs &p,
                                 cudaStream_t stream) {
     if (T <= kSmallMaxT && L <= kSmallWarps * 32) {
-        const size_t smem = sizeof(int) * kSmallWarps * (size_t)L;
-        group_tokens_kernel<kSmallWarps><<<1, kSmallWarps * 32, smem, stream>>>(idx, T, L, p);
+        group_tokens_kernel<kSmallWarps, true>
+            <<<1, kSmallWarps * 32, staged_smem(T, L), stream>>>(idx, T, L, p);
     } else {
         const size_t smem = sizeof(int) * kPlanWarps * (size_t)L;
-        group_tokens_kernel<kPlanWarps><<<1, kPlanThreads, smem, stream>>>(idx, T, L, p);
+        group_tokens_kernel<kPlanWarps, false><<<1, kPlanThreads, smem, stream>>>(idx, T, L, p);
     }
     return cudaGetLastError();
 }
