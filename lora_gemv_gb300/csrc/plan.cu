@@ -92,14 +92,15 @@ template <int NW, bool STAGED>
 __global__ void __launch_bounds__(NW * 32, 1)
 group_tokens_kernel(const int32_t *__restrict__ idx_g, int T, int L, PlanPtrs p) {
     constexpr int kPlanWarps = NW;
-    extern __shared__ int hist[];  // [kPlanWarps][L]
+    extern __shared__ __align__(16) int hist[];  // [kPlanWarps][L]
     __shared__ int ws[40];
     __shared__ int s_inact[kPlanWarps];
     __shared__ int s_bad;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int *idx_s = hist + kPlanWarps * L;  // STAGED only
     int *perm_s = idx_s + T;
-    int4 *tiles_s = reinterpret_cast<int4 *>(perm_s + T + ((T & 3) ? 4 - (T & 3) : 0));
+    // tile records start at a multiple of 4 ints (16 bytes): kPlanWarps*L is one
+    int4 *tiles_s = reinterpret_cast<int4 *>(perm_s + T + ((4 - ((2 * T) & 3)) & 3));
     const int32_t *idx = STAGED ? idx_s : idx_g;
 
     if (STAGED)
