@@ -60,6 +60,21 @@ def dist_env():
     return ws, rank, local
 
 
+def aggregate(ms_local: float, tokens_local: int, ws: int, device=None):
+    """Whole-job figures over ranks that run independent batches (replicas,
+    no data-path collective): the slowest rank's time and every rank's
+    tokens.  Returns (ms, tokens, tokens_per_s)."""
+    ms, tokens = float(ms_local), float(tokens_local)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        n = torch.tensor([tokens], dtype=torch.float64, device=device)
+        dist.all_reduce(n, op=dist.ReduceOp.SUM)
+        ms, tokens = float(t.item()), float(n.item())
+    return ms, tokens, tokens / (ms / 1e3)
+
+
 # ---------------------------------------------------------------- work model
 
 def algorithmic(idx: torch.Tensor):
@@ -178,6 +193,11 @@ def make_pool(dev, rank: int, l2_bytes: int, only_T=None):
 
 
 FUSED_STEP = True  # shrink + expand_slice through the chained (PDL) entry point
+
+# DRAM bytes (read + write) of one launch of each kernel for the T=1024 batch,
+# from an ncu capture of `bench.py --profile --T 1024` (summaries under
+# profiles/); None until a capture of the current kernel exists.
+NCU_TRAFFIC = {"shrink": None, "expand_slice": None}
 
 
 def run_step(lg, batches, fused: bool = FUSED_STEP):
@@ -419,13 +439,8 @@ def main_ours(args):
     gr_ms = op_only_ms(pool, lambda b: lg.lora_group_tokens(b["idx"], L, b["plan"]))
     ex_src = (f"CUDA events around graphs of back-to-back launches, one per pool set "
               f"({nsets} sets, inputs from HBM), per batch size")
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-
     tokens_rank = K * sum(li.DECODE_T)
-    value = tokens_rank * ws / (ms / 1e3)
+    ms, _, value = aggregate(ms, tokens_rank, ws, dev)
 
     per_T = {}
     fu_bytes = 0
@@ -445,16 +460,20 @@ def main_ours(args):
                          "expand_GBps": eb / (ex_ms[i] / 1e3) / 1e9,
                          "fused_bytes": fb, "shrink_bytes": sb, "expand_bytes": eb}
     hbm, tf, src = peaks()
-    # dominant kernel of the step: expand_slice (two-launch step) or the fused launch
-    if FUSED_STEP:
-        dom, dom_bytes, dom_time = "shrink_expand_slice (PDL-chained pair)", fu_bytes, fu_time
-    else:
-        dom = "expand_slice"
-        dom_bytes = sum(v["expand_bytes"] for v in per_T.values())
-        dom_time = sum(ex_ms) / 1e3
-    achieved = dom_bytes / dom_time / 1e9        # bytes of the 5 launches / their summed time
+    # dominant kernel: the largest summed per-step time among the three
+    # kernels; its roofline is taken on its launch for the largest batch
+    # (algorithmic bytes of that launch / its measured duration), with the
+    # all-batch figure beside it
+    kern = {"shrink": (sh_ms, "shrink_bytes"), "expand_slice": (ex_ms, "expand_bytes"),
+            "grouping": (gr_ms, None)}
+    dom = max(("shrink", "expand_slice"), key=lambda k: sum(kern[k][0]))
+    dom_ms, dom_key = kern[dom]
+    Tmax = str(li.DECODE_T[-1])
+    achieved = per_T[Tmax][dom_key] / (dom_ms[-1] / 1e3) / 1e9
+    all_achieved = sum(v[dom_key] for v in per_T.values()) / (sum(dom_ms) / 1e3) / 1e9
     step_s = ms / 1e3 / K
     path_frac = (fu_bytes / (hbm * 1e9)) / step_s
+    traffic = NCU_TRAFFIC.get(dom)
 
     e2e_v, h2d, d2h, e2e_wall = e2e_run(lg, dev, max(10, min(K, 300)), 3)
 
@@ -470,10 +489,14 @@ def main_ours(args):
                              "five independent batches are concurrent branches of the graph"},
         "sequential_batches": {"value": tokens_rank * ws / (seq_ms / 1e3), "unit": "tokens/s",
                                "ms_per_step": seq_ms / K},
-        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved,
-                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_source": f"{src} hbm_gbs", "traffic": None,
-                     "timing": ex_src},
+        "roofline": {"kernel": dom, "launch": f"T={Tmax} batch", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": f"{src} hbm_gbs",
+                     "traffic": traffic["bytes"] if traffic else None,
+                     "traffic_source": traffic["source"] if traffic else None,
+                     "all_batches_achieved": all_achieved, "timing": ex_src},
+        "step_time_share": {k: sum(v[0]) / (sum(sh_ms) + sum(ex_ms) + sum(gr_ms))
+                            for k, v in kern.items()},
         "path_roofline_frac": path_frac,
         "gpu_launches": K * nb * (2 if FUSED_STEP else 3),
         "e2e": {"value": e2e_v, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
