@@ -92,6 +92,32 @@ __device__ __forceinline__ void fetch_stage(uint4 (&ld)[kMaxLd], const E *__rest
     }
 }
 
+// Stage loads straight to shared memory (aligned rows): cp.async 16-byte
+// chunks, zero-filled past h_end; rows past the tile are not read (their
+// results are never stored).
+template <typename E>
+__device__ __forceinline__ void async_stage(unsigned char *stage, const E *__restrict__ x,
+                                            int64_t ldx, const E *__restrict__ Al, int H,
+                                            const int *s_rows, const int *s_arow, int n,
+                                            int nrows, int h0, int h_end) {
+    E *sX = reinterpret_cast<E *>(stage);
+    E *sA = reinterpret_cast<E *>(stage + kTile * kK * 2);
+    for (int it = threadIdx.x; it < (kTile + nrows) * kCh; it += kThreads) {
+        const int r = it / kCh, c = it % kCh;
+        const int h = h0 + 8 * c;
+        if (r < kTile) {
+            const int row = s_rows[r];
+            if (r < n && row >= 0)
+                cp_async16(smem_u32(sX + swz(r, c)), x + (int64_t)row * ldx + (h < h_end ? h : 0),
+                           h < h_end ? 16 : 0);
+        } else {
+            const int ar = r - kTile;
+            const E *src = Al + (int64_t)s_arow[ar] * H;
+            cp_async16(smem_u32(sA + swz(ar, c)), src + (h < h_end ? h : 0), h < h_end ? 16 : 0);
+        }
+    }
+}
+
 __device__ __forceinline__ void store_stage(const uint4 (&ld)[kMaxLd], unsigned char *stage,
                                             int rows_cap, int n, int nrows) {
     uint4 *sX = reinterpret_cast<uint4 *>(stage);
@@ -197,17 +223,34 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
 
-        uint4 ld[kMaxLd];
-        if (nstages > 0) {
-            fetch_stage<E, VEC>(ld, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, h_begin, h_end);
-            store_stage(ld, smem, rows_cap, n, nrows);
+        // Aligned rows: both buffers are filled by cp.async at once (a CTA's
+        // whole H range is in flight for the decode split-K shapes), then
+        // each stage refills its buffer two stages ahead.  Otherwise loads go
+        // through registers one stage ahead.
+        uint4 ld[VEC ? 1 : kMaxLd];
+        if (VEC) {
+            if (nstages > 0)
+                async_stage<E>(smem, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, h_begin, h_end);
+            cp_async_commit();
+            if (nstages > 1)
+                async_stage<E>(smem + stage_bytes, x, a.ldx, Al, H, s_rows, s_arow, n, nrows,
+                               h_begin + kK, h_end);
+            cp_async_commit();
+        } else if (nstages > 0) {
+            fetch_stage<E, VEC>(reinterpret_cast<uint4 (&)[kMaxLd]>(ld), x, a.ldx, Al, H, s_rows,
+                                s_arow, n, nrows, h_begin, h_end);
+            store_stage(reinterpret_cast<uint4 (&)[kMaxLd]>(ld), smem, rows_cap, n, nrows);
         }
-        __syncthreads();
+        if (!VEC) __syncthreads();
         for (int st = 0; st < nstages; ++st) {
             unsigned char *cur = smem + (st & 1) * stage_bytes;
-            if (st + 1 < nstages)  // next stage in flight while this one is multiplied
-                fetch_stage<E, VEC>(ld, x, a.ldx, Al, H, s_rows, s_arow, n, nrows,
-                                    h_begin + (st + 1) * kK, h_end);
+            if (VEC) {
+                cp_async_wait<1>();
+                __syncthreads();
+            } else if (st + 1 < nstages) {  // next stage in flight while this one is multiplied
+                fetch_stage<E, VEC>(reinterpret_cast<uint4 (&)[kMaxLd]>(ld), x, a.ldx, Al, H,
+                                    s_rows, s_arow, n, nrows, h_begin + (st + 1) * kK, h_end);
+            }
             if (wact) {
                 const E *bx = reinterpret_cast<const E *>(cur);
                 const E *ba = reinterpret_cast<const E *>(cur + kTile * kK * 2);
@@ -227,9 +270,20 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
                     }
                 }
             }
-            if (st + 1 < nstages) store_stage(ld, smem + ((st + 1) & 1) * stage_bytes, rows_cap, n, nrows);
-            __syncthreads();
+            if (VEC) {
+                __syncthreads();  // everyone is done with this buffer
+                if (st + 2 < nstages)
+                    async_stage<E>(cur, x, a.ldx, Al, H, s_rows, s_arow, n, nrows,
+                                   h_begin + (st + 2) * kK, h_end);
+                cp_async_commit();
+            } else {
+                if (st + 1 < nstages)
+                    store_stage(reinterpret_cast<uint4 (&)[kMaxLd]>(ld),
+                                smem + ((st + 1) & 1) * stage_bytes, rows_cap, n, nrows);
+                __syncthreads();
+            }
         }
+        if (VEC) cp_async_wait<0>();
 
         // warp partials -> P[warp], then the CTA partial summed in warp order
         if (wact) {
