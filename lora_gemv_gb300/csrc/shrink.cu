@@ -11,15 +11,19 @@
 // (mma.sync m16n8k16, fp32 accumulate), where rows are the adapter's
 // S * r_l live rows only (rank-aware: padded rows are never read).
 //  - H is split across a thread-block CLUSTER of up to 16 CTAs (split-K);
-//    each CTA walks its H range in 128-wide stages, double-buffered: the
-//    next stage is read with 16-byte global loads into registers while the
-//    current one feeds ldmatrix + mma from 256-byte-swizzled shared memory
-//    (plain loads keep far more bytes in flight per SM than cp.async);
-//  - the 8 warps split the tile's 16-row blocks and, for small tiles, each
-//    stage's k steps, so decode tiles of a few tokens still use every warp;
-//  - partials are summed over warps in shared memory and over the cluster
-//    through distributed shared memory, in a fixed order (deterministic, no
-//    global scratch, no atomics), each CTA finishing a share of the tile;
+//    each CTA walks its H range in 128-wide stages through two
+//    256-byte-swizzled shared-memory buffers feeding ldmatrix + mma: aligned
+//    rows are copied with cp.async, both buffers at once (for the decode
+//    split-K shapes a CTA's whole H range is then in flight), other rows
+//    through registers one stage ahead;
+//  - the 8 warps split the tile's 16-row blocks and, within a block,
+//    either its 8-column n-tiles (every output has one owner warp and the
+//    CTA partial is written straight from the accumulators) or, for batches
+//    of a few tokens per adapter, each stage's k steps (short mma chains;
+//    the warp partials are then summed in shared memory);
+//  - partials are summed over the cluster through distributed shared
+//    memory, in a fixed order (deterministic, no global scratch, no
+//    atomics), each CTA finishing a share of the tile;
 //  - tiles of adapter -1 load nothing (block skipping); their y rows are
 //    zeroed unless add_inputs.
 #include <cooperative_groups.h>
@@ -41,11 +45,12 @@ constexpr int kK = 128;        // H elements per stage (256-byte rows)
 constexpr int kCh = kK / 8;    // 16-byte chunks per row and stage
 
 // Shared-memory bytes: two stages of (64 x rows + rows_cap A rows) x 256 B,
-// reused after the k loop for the warp partials and the CTA partial.
+// reused after the k loop for the CTA partial [64][rows] and, for k-split
+// warps, their partials [8 warps][16][rows].
 __host__ __device__ constexpr int part_pitch(int ntmax) { return ntmax * 8 + 4; }
 __host__ __device__ constexpr int smem_bytes(int rows_cap, int ntmax) {
     const int stages = 2 * (kTile + rows_cap) * kK * 2;
-    const int parts = (kWarps * 16 + kTile) * part_pitch(ntmax) * 4;
+    const int parts = (kTile + kWarps * 16) * part_pitch(ntmax) * 4;
     return stages > parts ? stages : parts;
 }
 
@@ -136,7 +141,10 @@ __device__ __forceinline__ void store_stage(const uint4 (&ld)[kMaxLd], unsigned 
     }
 }
 
-template <typename E, bool VEC, int NTMAX>
+// KS: warps of one row block split its k steps (else its n-tiles).  No
+// minimum-occupancy bound: capping registers for more resident CTAs measured
+// slower (the CTAs per SM are limited by shared memory anyway).
+template <typename E, bool VEC, int NTMAX, bool KS>
 __global__ void __launch_bounds__(kThreads)
 shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -174,8 +182,8 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
     const int h_end = min(H, h_begin + kchunk);
     const int nstages = h_end > h_begin ? (h_end - h_begin + kK - 1) / kK : 0;
     const int stage_bytes = (kTile + rows_cap) * kK * 2;
-    float *P = reinterpret_cast<float *>(smem);             // [kWarps][16][PP]
-    float *Ct = P + kWarps * 16 * PP;                        // [64][PP]
+    float *Ct = reinterpret_cast<float *>(smem);  // CTA partial [64][PP]
+    float *P = Ct + kTile * PP;                    // warp partials [8][16][PP]
 
     const int n_tiles = min(h1.z, a.max_tiles);
     for (int tile = blockIdx.y; tile < n_tiles; tile += gridDim.y) {
@@ -211,15 +219,20 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
         const E *Al = static_cast<const E *>(a.A) + (int64_t)l * S * R * H;
         const int NT = (nrows + 7) / 8;
         const int nmb = (n + 15) / 16;
+        // warp -> (16-row block mb, n-tile share ns, k share kp)
         const int nmbp = nmb <= 1 ? 1 : (nmb <= 2 ? 2 : 4);
-        const int kparts = kWarps / nmbp;               // warps sharing one 16-row block
-        const int mb = warp % nmbp, kp = warp / nmbp;
+        const int nsplit = KS ? 1 : kWarps / nmbp;
+        const int kparts = KS ? kWarps / nmbp : 1;
+        const int mb = warp % nmbp, ns = (warp / nmbp) % nsplit, kp = warp / (nmbp * nsplit);
+        const int ntw = (NT + nsplit - 1) / nsplit;
+        const int nt0 = ns * ntw, nt1 = min(NT, nt0 + ntw);
         const int kk0 = kp * (kK / 16) / kparts, kk1 = (kp + 1) * (kK / 16) / kparts;
-        const bool wact = mb < nmb;
+        const bool wact = mb < nmb && nt0 < nt1;
 
-        float acc[NTMAX][4];
+        constexpr int NTW = KS ? NTMAX : NTMAX / 2;  // n-tiles per warp at most
+        float acc[NTW][4];
 #pragma unroll
-        for (int i = 0; i < NTMAX; ++i)
+        for (int i = 0; i < NTW; ++i)
 #pragma unroll
             for (int k = 0; k < 4; ++k) acc[i][k] = 0.f;
 
@@ -259,13 +272,19 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
                     const int ar = mb * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
                     ldmatrix_x4(af, smem_u32(bx + swz(ar, 2 * kk + (lane >> 4))));
 #pragma unroll
-                    for (int np = 0; np < NTMAX / 2; ++np) {
-                        if (2 * np < NT) {
+                    for (int j = 0; j < NTW; j += 2) {
+                        const int nt = nt0 + j;
+                        if (j + 1 < NTW && nt + 1 < nt1) {
                             uint32_t bf[4];
-                            const int br = 8 * (2 * np + (lane >> 4)) + (lane & 7);
+                            const int br = 8 * (nt + (lane >> 4)) + (lane & 7);
                             ldmatrix_x4(bf, smem_u32(ba + swz(br, 2 * kk + ((lane >> 3) & 1))));
-                            mma16816<E>(acc[2 * np], af, bf[0], bf[1]);
-                            if (2 * np + 1 < NT) mma16816<E>(acc[2 * np + 1], af, bf[2], bf[3]);
+                            mma16816<E>(acc[j], af, bf[0], bf[1]);
+                            mma16816<E>(acc[j + 1], af, bf[2], bf[3]);
+                        } else if (nt < nt1) {
+                            uint32_t bf[2];
+                            const int br = 8 * nt + (lane & 7);
+                            ldmatrix_x2(bf, smem_u32(ba + swz(br, 2 * kk + ((lane >> 3) & 1))));
+                            mma16816<E>(acc[j], af, bf[0], bf[1]);
                         }
                     }
                 }
@@ -285,27 +304,28 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
         }
         if (VEC) cp_async_wait<0>();
 
-        // warp partials -> P[warp], then the CTA partial summed in warp order
+        // the CTA partial: straight from each owner warp's accumulators, or
+        // the k-split warps' partials summed in warp order
         if (wact) {
-            float *pw = P + warp * 16 * PP;
+            float *c0 = (kparts == 1 ? Ct + mb * 16 * PP : P + warp * 16 * PP) + g * PP + 2 * q;
 #pragma unroll
-            for (int nt = 0; nt < NTMAX; ++nt) {
-                if (nt < NT) {
-                    const int cc = nt * 8 + 2 * q;
-                    pw[g * PP + cc] = acc[nt][0];
-                    pw[g * PP + cc + 1] = acc[nt][1];
-                    pw[(g + 8) * PP + cc] = acc[nt][2];
-                    pw[(g + 8) * PP + cc + 1] = acc[nt][3];
+            for (int j = 0; j < NTW; ++j) {
+                if (nt0 + j < nt1) {
+                    const int cc = (nt0 + j) * 8;
+                    *reinterpret_cast<float2 *>(c0 + cc) = make_float2(acc[j][0], acc[j][1]);
+                    *reinterpret_cast<float2 *>(c0 + 8 * PP + cc) = make_float2(acc[j][2], acc[j][3]);
                 }
             }
         }
-        __syncthreads();
-        for (int it = threadIdx.x; it < n * nrows; it += kThreads) {
-            const int i = it / nrows, j = it - i * nrows;
-            const int m = i >> 4, r = i & 15;
-            float sum = 0.f;
-            for (int k = 0; k < kparts; ++k) sum += P[((k * nmbp + m) * 16 + r) * PP + j];
-            Ct[i * PP + j] = sum;
+        if (kparts > 1) {
+            __syncthreads();
+            for (int it = threadIdx.x; it < n * nrows; it += kThreads) {
+                const int i = it / nrows, j = it - i * nrows;
+                const float *src = P + ((i >> 4) * 16 + (i & 15)) * PP + j;
+                float sum = 0.f;
+                for (int k = 0; k < kparts; ++k) sum += src[k * nmbp * 16 * PP];
+                Ct[i * PP + j] = sum;
+            }
         }
         if (ksplit > 1) cluster.sync();
         else __syncthreads();
@@ -342,79 +362,32 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
     }
 }
 
-template <typename E, bool VEC, int NTMAX>
-cudaError_t configure_one(int max_cluster) {
-    cudaError_t e = cudaFuncSetAttribute(shrink_kernel<E, VEC, NTMAX>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes(kRows, NTMAX));
-    if (e != cudaSuccess) return e;
-    if (max_cluster > 8)
-        e = cudaFuncSetAttribute(shrink_kernel<E, VEC, NTMAX>,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    return e;
-}
+using ShrinkFn = void (*)(const ShrinkArgs, int, int);
 
-template <typename E, bool VEC>
-cudaError_t configure_vec(int max_cluster) {
-    cudaError_t e;
-    if ((e = configure_one<E, VEC, 2>(max_cluster)) != cudaSuccess) return e;
-    if ((e = configure_one<E, VEC, 4>(max_cluster)) != cudaSuccess) return e;
-    if ((e = configure_one<E, VEC, 8>(max_cluster)) != cudaSuccess) return e;
-    return configure_one<E, VEC, 16>(max_cluster);
-}
-
-// Resident CTAs per SM of each instantiation at its largest shared memory,
-// [dtype][vec][n-tile class], filled by configure_shrink_kernels.
-int g_occ[2][2][4] = {};
-
-template <typename E, bool VEC, int NTMAX>
-cudaError_t occ_one(int &occ) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, shrink_kernel<E, VEC, NTMAX>, kThreads, smem_bytes(NTMAX * 8 < kRows ? NTMAX * 8 : kRows, NTMAX));
+// Instantiation for n-tile class c (NTMAX = 2 << c).
+template <typename E, bool VEC, bool KS>
+ShrinkFn kernel_nt(int c) {
+    switch (c) {
+        case 0: return shrink_kernel<E, VEC, 2, KS>;
+        case 1: return shrink_kernel<E, VEC, 4, KS>;
+        case 2: return shrink_kernel<E, VEC, 8, KS>;
+        default: return shrink_kernel<E, VEC, 16, KS>;
+    }
 }
 
 template <typename E>
-cudaError_t occ_dtype(int (&occ)[2][4]) {
-    cudaError_t e;
-    if ((e = occ_one<E, false, 2>(occ[0][0])) != cudaSuccess) return e;
-    if ((e = occ_one<E, false, 4>(occ[0][1])) != cudaSuccess) return e;
-    if ((e = occ_one<E, false, 8>(occ[0][2])) != cudaSuccess) return e;
-    if ((e = occ_one<E, false, 16>(occ[0][3])) != cudaSuccess) return e;
-    if ((e = occ_one<E, true, 2>(occ[1][0])) != cudaSuccess) return e;
-    if ((e = occ_one<E, true, 4>(occ[1][1])) != cudaSuccess) return e;
-    if ((e = occ_one<E, true, 8>(occ[1][2])) != cudaSuccess) return e;
-    return occ_one<E, true, 16>(occ[1][3]);
+ShrinkFn kernel_e(bool vec, int c, bool ks) {
+    if (vec) return ks ? kernel_nt<E, true, true>(c) : kernel_nt<E, true, false>(c);
+    return ks ? kernel_nt<E, false, true>(c) : kernel_nt<E, false, false>(c);
 }
 
-template <typename E, bool VEC, int NTMAX>
-cudaError_t launch_nt(const ShrinkArgs &a, int ksplit, int kchunk, int rows_cap, dim3 grid,
-                      cudaStream_t stream, bool pdl) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes(rows_cap, NTMAX);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = ksplit;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, shrink_kernel<E, VEC, NTMAX>, a, kchunk, rows_cap);
+ShrinkFn kernel_for(int dt, bool vec, int c, bool ks) {
+    return dt == LORA_F16 ? kernel_e<__half>(vec, c, ks) : kernel_e<__nv_bfloat16>(vec, c, ks);
 }
 
-template <typename E, bool VEC>
-cudaError_t launch_vec(const ShrinkArgs &a, int ksplit, int kchunk, int rows_cap, dim3 grid,
-                       cudaStream_t stream, bool pdl) {
-    const int nt = rows_cap / 8;
-    if (nt <= 2) return launch_nt<E, VEC, 2>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
-    if (nt <= 4) return launch_nt<E, VEC, 4>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
-    if (nt <= 8) return launch_nt<E, VEC, 8>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
-    return launch_nt<E, VEC, 16>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
-}
+// Resident CTAs per SM of each instantiation at its largest shared memory,
+// [dtype][vec][n-tile class][ks], filled by configure_shrink_kernels.
+int g_occ[2][2][4][2] = {};
 
 }  // namespace
 
@@ -422,11 +395,11 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
     // Largest cluster the GPU can hold with this kernel's largest shared memory.
     int max_cluster = 8;
     {
-        cudaError_t e = cudaFuncSetAttribute(shrink_kernel<__half, true, 16>,
-                                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        const ShrinkFn k = kernel_for(LORA_F16, true, 3, false);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(shrink_kernel<__half, true, 16>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(kRows, 16));
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem_bytes(kRows, 16));
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(16, 1, 1);
@@ -440,19 +413,27 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, shrink_kernel<__half, true, 16>, &cfg) == cudaSuccess &&
-            n > 0)
-            max_cluster = 16;
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) == cudaSuccess && n > 0) max_cluster = 16;
         cudaGetLastError();  // a refused query is not an error: fall back to 8
     }
     info->max_cluster = max_cluster;
-    cudaError_t e;
-    if ((e = configure_vec<__half, true>(max_cluster)) != cudaSuccess) return e;
-    if ((e = configure_vec<__half, false>(max_cluster)) != cudaSuccess) return e;
-    if ((e = configure_vec<__nv_bfloat16, true>(max_cluster)) != cudaSuccess) return e;
-    if ((e = configure_vec<__nv_bfloat16, false>(max_cluster)) != cudaSuccess) return e;
-    if ((e = occ_dtype<__half>(g_occ[LORA_F16])) != cudaSuccess) return e;
-    return occ_dtype<__nv_bfloat16>(g_occ[LORA_BF16]);
+    for (int dt = 0; dt < 2; ++dt)
+        for (int vec = 0; vec < 2; ++vec)
+            for (int c = 0; c < 4; ++c)
+                for (int ks = 0; ks < 2; ++ks) {
+                    const ShrinkFn k = kernel_for(dt, vec, c, ks);
+                    const int ntmax = 2 << c;
+                    cudaError_t e = cudaFuncSetAttribute(
+                        k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(kRows, ntmax));
+                    if (e == cudaSuccess && max_cluster > 8)
+                        e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                    if (e == cudaSuccess)
+                        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                            &g_occ[dt][vec][c][ks], k, kThreads,
+                            smem_bytes(std::min(ntmax * 8, kRows), ntmax));
+                    if (e != cudaSuccess) return e;
+                }
+    return cudaSuccess;
 }
 
 cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo &dev,
@@ -470,7 +451,9 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     const int ntmax = rows_cap / 8 <= 2 ? 2 : rows_cap / 8 <= 4 ? 4 : rows_cap / 8 <= 8 ? 8 : 16;
     // CTAs resident per SM (registers and shared memory)
     const int ntc = ntmax == 2 ? 0 : ntmax == 4 ? 1 : ntmax == 8 ? 2 : 3;
-    const int per_sm = std::max(1, g_occ[dt][vec ? 1 : 0][ntc]);
+    // warps split k steps when adapters average at most one 16-token row block
+    const bool ks = a.T <= 16LL * std::min(a.L, a.T);
+    const int per_sm = std::max(1, g_occ[dt][vec ? 1 : 0][ntc][ks ? 1 : 0]);
     // Split K across a cluster so that the whole grid is resident at once
     // (one wave; a cluster needs all its CTAs placed together, so keep some
     // slack), each CTA keeping >= 2 stages of work.
@@ -482,12 +465,21 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     int kchunk = ((a.H + ksplit - 1) / ksplit + kK - 1) / kK * kK;
     while (ksplit > 1 && (long long)(ksplit - 1) * kchunk >= a.H) ksplit /= 2;  // no empty CTAs
     kchunk = ((a.H + ksplit - 1) / ksplit + kK - 1) / kK * kK;
-    dim3 grid(ksplit, gy, gz);
-    if (dt == LORA_F16)
-        return vec ? launch_vec<__half, true>(a, ksplit, kchunk, rows_cap, grid, stream, pdl)
-                   : launch_vec<__half, false>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
-    return vec ? launch_vec<__nv_bfloat16, true>(a, ksplit, kchunk, rows_cap, grid, stream, pdl)
-               : launch_vec<__nv_bfloat16, false>(a, ksplit, kchunk, rows_cap, grid, stream, pdl);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ksplit, gy, gz);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes(rows_cap, ntmax);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ksplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel_for(dt, vec, ntc, ks), a, kchunk, rows_cap);
 }
 
 }  // namespace lora

@@ -184,6 +184,34 @@ def test_edge_shapes(cuda_lib, dtype, T, H, R, L, Ns):
     full_check(cuda_lib, c)
 
 
+def skewed_idx(T, counts, seed):
+    """Token indices giving adapter a exactly counts[a] tokens (the rest -1),
+    shuffled: tiles of every size in one batch."""
+    idx = torch.full((T,), -1, dtype=torch.int32)
+    pos = torch.randperm(T, generator=torch.Generator().manual_seed(seed))
+    k = 0
+    for a, n in enumerate(counts):
+        idx[pos[k:k + n]] = a
+        k += n
+    return idx
+
+
+# The shrink's warps split a tile's k steps when the batch averages at most 16
+# tokens per adapter, else its n-tiles; both must hold for tiles of every size
+# (1..64 tokens) and every A-row count (1..16 n-tiles).
+@pytest.mark.parametrize("T,L,counts", [
+    (64, 4, [60, 1, 2, 0]),           # k-split warps, one near-full tile
+    (48, 4, [33, 9, 0, 5]),           # k-split warps, 3 row blocks
+    (200, 4, [150, 1, 20, 3]),        # n-split warps, 1- and 3-token tiles
+    (1024, 8, [900, 1, 2, 4, 17, 31, 40, 29]),
+])
+@pytest.mark.parametrize("R,S", [(16, 3), (64, 2), (8, 1), (20, 1)])
+def test_warp_splits_every_tile_size(cuda_lib, T, L, counts, R, S):
+    c = make_case(T, 512, R, L, [96] * S, torch.bfloat16, seed=T + R + S, sscale=1.0)
+    c.token_idx = skewed_idx(T, counts, seed=T + L)
+    full_check(cuda_lib, c)
+
+
 @pytest.mark.parametrize("add", [False, True])
 def test_add_flag_and_inactive_rows(cuda_lib, add):
     c = make_case(150, 256, 16, 3, [512], torch.float16, seed=3, add=add, p_neg=0.3)
