@@ -241,7 +241,7 @@ lora_status_t lora_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_
     const lora::DeviceInfo *dev;
     if ((s = device_info(&dev)) != LORA_OK) return s;
     lora::PlanPtrs p = plan_ptrs(const_cast<void *>(plan), lay);
-    lora::ShrinkArgs a;
+    lora::ShrinkArgs a{};
     a.x = x;
     a.ldx = ldx;
     a.T = T;
@@ -340,7 +340,7 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
     lora_plan_layout(T, L, &lay);
     lora::PlanPtrs p = plan_ptrs(const_cast<void *>(plan), lay);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    lora::ShrinkArgs sa;
+    lora::ShrinkArgs sa{};
     sa.x = x;
     sa.ldx = ldx;
     sa.T = T;

@@ -81,6 +81,7 @@ expand_kernel(const ExpandArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
     grid_dep_wait();  // y (and anything else) may come from the previous kernel
+    grid_dep_launch();
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, q = lane & 3;
@@ -423,8 +424,10 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     uint32_t ah[MB][KSMAX][4], al[MB][KSMAX][4];
 
     // As a programmatic dependent of the shrink, everything above (plan, out,
-    // B) overlaps the shrink's tail; y is read only after this wait.
+    // B) overlaps the shrink's tail; y is read only after this wait.  A
+    // following dependent waits for this grid in turn.
     grid_dep_wait();
+    grid_dep_launch();
 
     for (int u = u_begin; u < u_end; ++u) {
         // ---- the next unit: position, and its loads issued now

@@ -98,6 +98,10 @@ group_tokens_kernel(const int32_t *__restrict__ idx_g, int T, int L, PlanPtrs p)
     __shared__ int s_bad;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int *idx_s = hist + kPlanWarps * L;  // STAGED only
+    // A programmatic dependent (the shrink) may be scheduled now: it reads
+    // the plan only after its own wait, i.e. after this grid completes.
+    grid_dep_wait();
+    grid_dep_launch();
     int *perm_s = idx_s + T;
     // tile records start at a multiple of 4 ints (16 bytes): kPlanWarps*L is one
     int4 *tiles_s = reinterpret_cast<int4 *>(perm_s + T + ((4 - ((2 * T) & 3)) & 3));
@@ -249,6 +253,8 @@ group_segments_kernel(const int32_t *__restrict__ ss, const int32_t *__restrict_
     __shared__ int sh_lora[kPlanThreads], sh_end[kPlanThreads];
     __shared__ int s_err, s_bad;
     const int lane = threadIdx.x & 31;
+    grid_dep_wait();
+    grid_dep_launch();  // dependents read the plan only after their own wait
 
     for (int l = threadIdx.x; l < L; l += blockDim.x) p.count[l] = 0;
     if (threadIdx.x == 0) {
