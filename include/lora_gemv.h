@@ -7,8 +7,9 @@
  *    an expand variant, with block skipping and fast mask creation;
  *  - vLLM PR #11579 "[misc] Add LoRA kernel micro benchmarks": the operators
  *    bgmv_shrink, bgmv_expand, bgmv_expand_slice, sgmv_shrink, sgmv_expand,
- *    sgmv_expand_slice; the add_inputs flag of expand ("group-gemm + outputs");
- *    the fp32 intermediate between shrink and expand ("f32xf16=>f16"); the
+ *    sgmv_expand_slice; the add_inputs flag of expand (the product is added
+ *    to out); the fp32 intermediate between shrink and expand (fp32 times
+ *    fp16 weights giving fp16); the
  *    num_slices of a fused output; split-K shrink that adds partials;
  *  - Punica issue #17 "The smallest rank supported is 16?": BGMV (one adapter
  *    per input) versus SGMV (segments of inputs sharing one adapter, the
@@ -135,8 +136,8 @@ lora_status_t lora_plan_layout(int32_t T, int32_t L, lora_plan_layout_t *layout)
 size_t lora_workspace_size(int32_t T, int32_t L);
 
 /*
- * BGMV grouping (Punica issue #17, "each input is for a different model";
- * vLLM PR #15655 "faster mask creation"): builds the plan from a per-token
+ * BGMV grouping (Punica issue #17: every input may use its own adapter;
+ * vLLM PR #15655 summary: cheap mask construction): builds the plan from a per-token
  * adapter index token_idx[T] (device, int32; -1 = no LoRA; other values
  * outside [0, L) are counted in LORA_HDR_BAD_IDS and treated as -1).
  * One single-block kernel on `stream`; the grouping is a stable counting sort.

@@ -1,8 +1,9 @@
 // Expand / expand_slice: out[t, off_s + n] (+)= scale * sum_i y[t, s*ys + i] * B_s[l, n, i].
 //
 // Pages: vLLM PR #11579 "[misc] Add LoRA kernel micro benchmarks"
-// (bgmv_expand, sgmv_expand, the _slice forms with num_slices, add_inputs as
-// "group-gemm + outputs", the f32 x f16 => f16 typing); Punica issue #17
+// (bgmv_expand, sgmv_expand, the _slice forms with num_slices, add_inputs
+// adding the product to the existing outputs, the f32 x f16 => f16 typing);
+// Punica issue #17
 // (SGMV: tokens sharing an adapter reuse its weights).
 //
 // Design (GB300): the operator is an HBM-bound read-modify-write of out; the

@@ -4,8 +4,8 @@
 //
 // Pages: Punica issue #17 "The smallest rank supported is 16?" (BGMV = one
 // adapter per input, SGMV = segments of inputs sharing an adapter, the
-// "AAABCC" batch); vLLM PR #15655 summary ("faster mask creation", "allowing
-// for some blocks to be skipped"): here the mask becomes a stable counting
+// "AAABCC" batch); vLLM PR #15655 summary (cheap mask construction, blocks
+// without work skipped): here the mask becomes a stable counting
 // sort done once per batch on the device, and skipped blocks are simply the
 // tiles that do not exist (empty adapters) or carry adapter -1.
 //

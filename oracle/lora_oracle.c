@@ -16,9 +16,10 @@
  *  - vLLM PR #15655 "Multi-LoRA Optimisations for the V1 TPU backend",
  *    summary list: the kernel is split into a shrink and an expand variant.
  *  - vLLM PR #11579 "Add LoRA kernel micro benchmarks": the six operators
- *    bgmv/sgmv x shrink/expand/expand_slice; add_inputs means "group-gemm +
- *    outputs" rather than the group-gemm alone; the expand reads an fp32
- *    intermediate and fp16 weights ("f32xf16=>f16"); m = batch x seq-len
+ *    bgmv/sgmv x shrink/expand/expand_slice; add_inputs adds the group-GEMM
+ *    product to the existing outputs instead of overwriting them; the expand
+ *    reads an fp32 intermediate and fp16 weights (fp32 x fp16 -> fp16);
+ *    m = batch x seq-len
  *    tokens, k = rank, n = hidden for expand; expand_slice writes a column
  *    slice of a fused output (num_slices).
  *  - Punica issue #17 "The smallest rank supported is 16?": BGMV gives every
@@ -54,7 +55,7 @@ void oracle_set_threads(int n)
 }
 
 /*
- * BGMV token map (Punica issue #17: "each input is for a different model").
+ * BGMV token map (Punica issue #17: every input may use a different adapter).
  * lora_of[t] = idx[t] when 0 <= idx[t] < L; -1 means "no LoRA".  Any other
  * value is counted as a bad id and treated as -1.  Returns the bad-id count.
  */
@@ -109,7 +110,7 @@ int oracle_map_segments(const int32_t *start, const int32_t *len, const int32_t 
 }
 
 /*
- * Token grouping ("sort by lora id" in vLLM PR #11579's benchmark options;
+ * Token grouping (vLLM PR #11579's benchmark option that sorts tokens by adapter id;
  * the "AAABCC" sharing of Punica issue #17).
  *
  * by_adapter = 1 (BGMV): active tokens (lora_of >= 0) in ascending adapter
