@@ -385,9 +385,11 @@ ShrinkFn kernel_for(int dt, bool vec, int c, bool ks) {
     return dt == LORA_F16 ? kernel_e<__half>(vec, c, ks) : kernel_e<__nv_bfloat16>(vec, c, ks);
 }
 
-// Resident CTAs per SM of each instantiation at its largest shared memory,
-// [dtype][vec][n-tile class][ks], filled by configure_shrink_kernels.
-int g_occ[2][2][4][2] = {};
+// Split-K clusters of 1, 2, 4, 8, 16 CTAs the GPU holds at once, per
+// instantiation at its largest shared memory, [dtype][vec][n-tile class][ks]
+// [log2 cluster], filled by configure_shrink_kernels.  Clusters are placed
+// within one GPC, so this is below CTAs-per-SM x SMs / cluster.
+int g_clusters[2][2][4][2][5] = {};
 
 }  // namespace
 
@@ -425,12 +427,27 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
                     const int ntmax = 2 << c;
                     cudaError_t e = cudaFuncSetAttribute(
                         k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(kRows, ntmax));
+                    // all of the SM's unified L1 / shared memory as shared memory:
+                    // the default split fits fewer CTAs than registers allow
+                    if (e == cudaSuccess)
+                        e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                 cudaSharedmemCarveoutMaxShared);
                     if (e == cudaSuccess && max_cluster > 8)
                         e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-                    if (e == cudaSuccess)
-                        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                            &g_occ[dt][vec][c][ks], k, kThreads,
-                            smem_bytes(std::min(ntmax * 8, kRows), ntmax));
+                    for (int lc = 0; e == cudaSuccess && (1 << lc) <= max_cluster; ++lc) {
+                        cudaLaunchConfig_t cfg = {};
+                        cfg.gridDim = dim3(1 << lc, 1, 1);
+                        cfg.blockDim = dim3(kThreads);
+                        cfg.dynamicSmemBytes = smem_bytes(std::min(ntmax * 8, kRows), ntmax);
+                        cudaLaunchAttribute attr[1];
+                        attr[0].id = cudaLaunchAttributeClusterDimension;
+                        attr[0].val.clusterDim.x = 1 << lc;
+                        attr[0].val.clusterDim.y = 1;
+                        attr[0].val.clusterDim.z = 1;
+                        cfg.attrs = attr;
+                        cfg.numAttrs = 1;
+                        e = cudaOccupancyMaxActiveClusters(&g_clusters[dt][vec][c][ks][lc], k, &cfg);
+                    }
                     if (e != cudaSuccess) return e;
                 }
     return cudaSuccess;
@@ -453,15 +470,15 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     const int ntc = ntmax == 2 ? 0 : ntmax == 4 ? 1 : ntmax == 8 ? 2 : 3;
     // warps split k steps when adapters average at most one 16-token row block
     const bool ks = a.T <= 16LL * std::min(a.L, a.T);
-    const int per_sm = std::max(1, g_occ[dt][vec ? 1 : 0][ntc][ks ? 1 : 0]);
-    // Split K across a cluster so that the whole grid is resident at once
-    // (one wave; a cluster needs all its CTAs placed together, so keep some
-    // slack), each CTA keeping >= 2 stages of work.
-    const long long slots = (long long)per_sm * dev.sm_count * 3 / 4;
-    int ksplit = 1;
-    while (ksplit < dev.max_cluster && (long long)gy * gz * ksplit * 2 <= slots &&
-           a.H / (ksplit * 2) >= 2 * kK)
+    // Split K across the largest cluster for which the whole grid is resident
+    // at once (one wave of clusters), each CTA keeping >= 2 stages of work.
+    const int *cap = g_clusters[dt][vec ? 1 : 0][ntc][ks ? 1 : 0];
+    int ksplit = 1, lc = 0;
+    while (ksplit < dev.max_cluster && (long long)gy * gz <= cap[lc + 1] &&
+           a.H / (ksplit * 2) >= 2 * kK) {
         ksplit *= 2;
+        ++lc;
+    }
     int kchunk = ((a.H + ksplit - 1) / ksplit + kK - 1) / kK * kK;
     while (ksplit > 1 && (long long)(ksplit - 1) * kchunk >= a.H) ksplit /= 2;  // no empty CTAs
     kchunk = ((a.H + ksplit - 1) / ksplit + kK - 1) / kK * kK;
