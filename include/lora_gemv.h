@@ -98,6 +98,8 @@ enum {
 #define LORA_PLANERR_SEG_RANGE 1    /* a segment had start < 0, len < 0 or start+len > T: ignored */
 #define LORA_PLANERR_SEG_ORDER 2    /* a segment began before the end of an earlier one: ignored */
 #define LORA_PLANERR_MISMATCH 4     /* an operator got a plan built for another T or L: it wrote nothing */
+#define LORA_PLANERR_TIMEOUT 8      /* a kernel's bounded wait for its cluster peers expired: its
+                                       outputs for that call are not valid (never expected) */
 
 /*
  * Plan layout: byte offsets of each array inside the caller's plan buffer.

@@ -33,7 +33,7 @@ MAX_RANK = 128
 MAX_SLICES = 8
 HDR_WORDS = 16
 HDR = dict(MAGIC=0, T=1, L=2, KIND=3, NACTIVE=4, NGROUPS=5, NTILES=6, BAD_IDS=7, ERR=8)
-PLANERR_SEG_RANGE, PLANERR_SEG_ORDER, PLANERR_MISMATCH = 1, 2, 4
+PLANERR_SEG_RANGE, PLANERR_SEG_ORDER, PLANERR_MISMATCH, PLANERR_TIMEOUT = 1, 2, 4, 8
 PLAN_MAGIC = 0x4C6F5241
 
 EXPORTS = ("lora_plan_layout", "lora_workspace_size", "lora_group_tokens",

@@ -101,6 +101,69 @@ __device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
                  : "memory");
 }
 
+// ------------------------------------------------------------------ clusters
+// Split cluster barrier (every thread of every CTA of the cluster arrives,
+// then waits): release / acquire order each CTA's shared-memory accesses.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+// Arrival without ordering this CTA's memory accesses (mbarrier
+// initialisation is published by mbar_init's own fence).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// The shared::cluster address of `addr` (a shared::cta address) in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Asynchronous 16-byte store into a cluster CTA's shared memory (`addr`)
+// that counts its bytes on that CTA's mbarrier (`bar`), both shared::cluster
+// addresses of the same CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(
+            addr),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+        : "memory");
+}
+
+// mbarrier in this CTA's shared memory, arrived at from the cluster.
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+// This CTA's arrival on its own mbarrier, announcing `bytes` of
+// asynchronous stores for the current phase (they may land before or after).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+// Bounded wait for phase `parity` of this CTA's mbarrier (acquire at cluster
+// scope): false once kWaitPolls polls have failed.
+constexpr int kWaitPolls = 1 << 20;
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    for (int i = 0; i < kWaitPolls; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred p;\n"
+            "  mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            "  selp.u32 %0, 1, 0, p; }\n"
+            : "=r"(ok)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
 // Programmatic dependent launch: wait for the previous grid's results; let
 // the next grid start launching.  Both are no-ops for an ordinary launch.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }

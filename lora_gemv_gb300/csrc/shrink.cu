@@ -23,7 +23,11 @@
 //    the warp partials are then summed in shared memory);
 //  - partials are summed over the cluster through distributed shared
 //    memory, in a fixed order (deterministic, no global scratch, no
-//    atomics), each CTA finishing a share of the tile;
+//    atomics), each CTA finishing a share of the tile's rows: every CTA
+//    sends its partial rows to their owner's receive buffer with
+//    asynchronous stores that count their bytes on the owner's mbarrier
+//    (or, where the receive buffer would cost residency, the owners read
+//    the partials after a cluster barrier);
 //  - tiles of adapter -1 load nothing (block skipping); their y rows are
 //    zeroed unless add_inputs.
 #include <cooperative_groups.h>
@@ -53,6 +57,10 @@ __host__ __device__ constexpr int smem_bytes(int rows_cap, int ntmax) {
     const int parts = (kTile + kWarps * 16) * part_pitch(ntmax) * 4;
     return stages > parts ? stages : parts;
 }
+
+// Receive buffer of the push reduction, after the above: [ksplit][64 /
+// ksplit rows][rows_cap] floats from the cluster's CTAs.
+__host__ __device__ constexpr int recv_bytes(int rows_cap) { return kTile * rows_cap * 4; }
 
 // 256-byte rows, 16-byte chunks XOR-swizzled (within each 128-byte half) by the row.
 __device__ __forceinline__ int swz(int row, int chunk) {
@@ -144,12 +152,14 @@ __device__ __forceinline__ void store_stage(const uint4 (&ld)[kMaxLd], unsigned 
 // KS: warps of one row block split its k steps (else its n-tiles).  No
 // minimum-occupancy bound: capping registers for more resident CTAs measured
 // slower (the CTAs per SM are limited by shared memory anyway).
+// push: reduce over the cluster through the receive buffers (ksplit > 1).
 template <typename E, bool VEC, int NTMAX, bool KS>
 __global__ void __launch_bounds__(kThreads)
-shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
+shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
     __shared__ int s_arow[kRows];
+    __shared__ uint64_t s_bar;  // push: the cluster's partials of this CTA's rows have arrived
     constexpr int PP = part_pitch(NTMAX);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -184,6 +194,13 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
     const int stage_bytes = (kTile + rows_cap) * kK * 2;
     float *Ct = reinterpret_cast<float *>(smem);  // CTA partial [64][PP]
     float *P = Ct + kTile * PP;                    // warp partials [8][16][PP]
+    float *Rb = reinterpret_cast<float *>(smem + smem_bytes(rows_cap, NTMAX));  // push only
+    const int rpo = kTile / ksplit;                // rows owned per CTA (push)
+    uint32_t phase = 0;
+    if (push) {  // every peer's barrier is initialised before anyone stores to it
+        if (threadIdx.x == 0) mbar_init(&s_bar, 1);
+        cluster_arrive_relaxed();
+    }
 
     const int n_tiles = min(h1.z, a.max_tiles);
     for (int tile = blockIdx.y; tile < n_tiles; tile += gridDim.y) {
@@ -327,6 +344,43 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
                 Ct[i * PP + j] = sum;
             }
         }
+        if (push) {
+            __syncthreads();
+            cluster_wait();  // peers' barriers initialised / receive buffers read
+            const int nc4 = (nrows + 3) >> 2;
+            const int r0 = kc * rpo, nr = max(0, min(n - r0, rpo));
+            // the bytes every CTA of the cluster sends to my rows
+            if (threadIdx.x == 0) mbar_arrive_expect_tx(&s_bar, (uint32_t)(ksplit * nr * nc4 * 16));
+            // my partial rows -> slot kc of their owner's receive buffer
+            const uint32_t rb = smem_u32(Rb), bar = smem_u32(&s_bar);
+            for (int it = threadIdx.x; it < n * nc4; it += kThreads) {
+                const int i = it / nc4, c4 = it - i * nc4;
+                const int o = i / rpo;
+                const float4 v = *reinterpret_cast<const float4 *>(Ct + i * PP + 4 * c4);
+                st_async_v4(cluster_map(rb + 4u * ((kc * rpo + i - o * rpo) * rows_cap + 4 * c4), o), v,
+                            cluster_map(bar, o));
+            }
+            // my rows: the partials of every CTA, summed in rank order
+            if (!mbar_wait_cluster(&s_bar, phase) && threadIdx.x == 0)
+                atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+            phase ^= 1;
+            for (int it = threadIdx.x; it < nr * nrows; it += kThreads) {
+                const int ii = it / nrows, c = it - ii * nrows;
+                float sum = 0.f;
+                for (int r = 0; r < ksplit; ++r) sum += Rb[(r * rpo + ii) * rows_cap + c];
+                const int row = s_rows[r0 + ii];
+                if (row >= 0) {
+                    float *yp = a.y + (int64_t)row * a.ldy + s_arow[c];
+                    const float v = a.scale * sum;
+                    *yp = a.add ? *yp + v : v;
+                }
+            }
+            // my receive buffer is read (released before a next tile's stores)
+            if (tile + (int)gridDim.y < n_tiles) cluster_arrive();
+            else cluster_arrive_relaxed();
+            __syncthreads();  // s_rows / s_arow are rewritten by the next tile
+            continue;
+        }
         if (ksplit > 1) cluster.sync();
         else __syncthreads();
 
@@ -360,9 +414,10 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap) {
         if (ksplit > 1) cluster.sync();
         else __syncthreads();
     }
+    if (push) cluster_wait();  // no CTA leaves while a peer may still store into it
 }
 
-using ShrinkFn = void (*)(const ShrinkArgs, int, int);
+using ShrinkFn = void (*)(const ShrinkArgs, int, int, int);
 
 // Instantiation for n-tile class c (NTMAX = 2 << c).
 template <typename E, bool VEC, bool KS>
@@ -385,11 +440,20 @@ ShrinkFn kernel_for(int dt, bool vec, int c, bool ks) {
     return dt == LORA_F16 ? kernel_e<__half>(vec, c, ks) : kernel_e<__nv_bfloat16>(vec, c, ks);
 }
 
-// Split-K clusters of 1, 2, 4, 8, 16 CTAs the GPU holds at once, per
-// instantiation at its largest shared memory, [dtype][vec][n-tile class][ks]
-// [log2 cluster], filled by configure_shrink_kernels.  Clusters are placed
-// within one GPC, so this is below CTAs-per-SM x SMs / cluster.
-int g_clusters[2][2][4][2][5] = {};
+// Residency tables, filled by configure_shrink_kernels:
+//  - CTAs per SM of each instantiation without dynamic shared memory
+//    (registers, threads), [dtype][vec][n-tile class][ks], and its static
+//    shared memory;
+//  - clusters of 1, 2, 4, 8, 16 CTAs the GPU holds at once when k CTAs fit
+//    per SM, [k][log2 cluster] (clusters are placed within one GPC, so this
+//    is below k x SMs / cluster).
+int g_reg_occ[2][2][4][2] = {};
+int g_static_smem[2][2][4][2] = {};
+int g_cap[9][5] = {};
+int g_smem_sm = 0, g_smem_reserved = 0;
+
+// Stand-in for the capacity queries: residency set by shared memory alone.
+__global__ void __launch_bounds__(kThreads) capacity_probe_kernel() {}
 
 }  // namespace
 
@@ -419,35 +483,58 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
         cudaGetLastError();  // a refused query is not an error: fall back to 8
     }
     info->max_cluster = max_cluster;
+    cudaError_t e = cudaSuccess;
+    {
+        int dev = 0, optin = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+        cudaDeviceGetAttribute(&g_smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        e = cudaFuncSetAttribute(capacity_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin);
+        if (e == cudaSuccess && max_cluster > 8)
+            e = cudaFuncSetAttribute(capacity_probe_kernel,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        for (int k = 1; e == cudaSuccess && k <= 8; ++k) {
+            const int dyn = std::min(optin, (g_smem_sm / k - g_smem_reserved - 64) & ~15);
+            for (int lc = 0; e == cudaSuccess && (1 << lc) <= max_cluster; ++lc) {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = dim3(1 << lc, 1, 1);
+                cfg.blockDim = dim3(kThreads);
+                cfg.dynamicSmemBytes = dyn;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeClusterDimension;
+                attr[0].val.clusterDim.x = 1 << lc;
+                attr[0].val.clusterDim.y = 1;
+                attr[0].val.clusterDim.z = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                e = cudaOccupancyMaxActiveClusters(&g_cap[k][lc], capacity_probe_kernel, &cfg);
+            }
+        }
+        if (e != cudaSuccess) return e;
+    }
     for (int dt = 0; dt < 2; ++dt)
         for (int vec = 0; vec < 2; ++vec)
             for (int c = 0; c < 4; ++c)
                 for (int ks = 0; ks < 2; ++ks) {
                     const ShrinkFn k = kernel_for(dt, vec, c, ks);
                     const int ntmax = 2 << c;
-                    cudaError_t e = cudaFuncSetAttribute(
-                        k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(kRows, ntmax));
-                    // all of the SM's unified L1 / shared memory as shared memory:
-                    // the default split fits fewer CTAs than registers allow
+                    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             smem_bytes(kRows, ntmax) + recv_bytes(kRows));
+                    // all of the SM's unified L1 / shared memory may serve as shared
+                    // memory (the residency tables assume it)
                     if (e == cudaSuccess)
                         e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                                  cudaSharedmemCarveoutMaxShared);
                     if (e == cudaSuccess && max_cluster > 8)
                         e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-                    for (int lc = 0; e == cudaSuccess && (1 << lc) <= max_cluster; ++lc) {
-                        cudaLaunchConfig_t cfg = {};
-                        cfg.gridDim = dim3(1 << lc, 1, 1);
-                        cfg.blockDim = dim3(kThreads);
-                        cfg.dynamicSmemBytes = smem_bytes(std::min(ntmax * 8, kRows), ntmax);
-                        cudaLaunchAttribute attr[1];
-                        attr[0].id = cudaLaunchAttributeClusterDimension;
-                        attr[0].val.clusterDim.x = 1 << lc;
-                        attr[0].val.clusterDim.y = 1;
-                        attr[0].val.clusterDim.z = 1;
-                        cfg.attrs = attr;
-                        cfg.numAttrs = 1;
-                        e = cudaOccupancyMaxActiveClusters(&g_clusters[dt][vec][c][ks][lc], k, &cfg);
-                    }
+                    if (e == cudaSuccess)
+                        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_reg_occ[dt][vec][c][ks], k,
+                                                                          kThreads, 0);
+                    cudaFuncAttributes fa;
+                    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k);
+                    if (e == cudaSuccess) g_static_smem[dt][vec][c][ks] = (int)fa.sharedSizeBytes;
                     if (e != cudaSuccess) return e;
                 }
     return cudaSuccess;
@@ -470,11 +557,21 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     const int ntc = ntmax == 2 ? 0 : ntmax == 4 ? 1 : ntmax == 8 ? 2 : 3;
     // warps split k steps when adapters average at most one 16-token row block
     const bool ks = a.T <= 16LL * std::min(a.L, a.T);
+    // CTAs resident per SM with `dyn` bytes of dynamic shared memory
+    const int vi = vec ? 1 : 0, ki = ks ? 1 : 0;
+    auto resident = [&](size_t dyn) {
+        const long long by_smem =
+            g_smem_sm / ((long long)dyn + g_static_smem[dt][vi][ntc][ki] + g_smem_reserved);
+        return (int)std::max(1LL, std::min<long long>({by_smem, g_reg_occ[dt][vi][ntc][ki], 8}));
+    };
+    size_t smem = smem_bytes(rows_cap, ntmax);
+    const int occ = resident(smem);
+    // the push reduction's receive buffer, where it costs no residency
+    const bool push_fits = resident(smem + recv_bytes(rows_cap)) == occ;
     // Split K across the largest cluster for which the whole grid is resident
     // at once (one wave of clusters), each CTA keeping >= 2 stages of work.
-    const int *cap = g_clusters[dt][vec ? 1 : 0][ntc][ks ? 1 : 0];
     int ksplit = 1, lc = 0;
-    while (ksplit < dev.max_cluster && (long long)gy * gz <= cap[lc + 1] &&
+    while (ksplit < dev.max_cluster && (long long)gy * gz <= g_cap[occ][lc + 1] &&
            a.H / (ksplit * 2) >= 2 * kK) {
         ksplit *= 2;
         ++lc;
@@ -485,7 +582,9 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ksplit, gy, gz);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem_bytes(rows_cap, ntmax);
+    const int push = push_fits && ksplit > 1 ? 1 : 0;
+    if (push) smem += recv_bytes(rows_cap);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -496,7 +595,7 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kernel_for(dt, vec, ntc, ks), a, kchunk, rows_cap);
+    return cudaLaunchKernelEx(&cfg, kernel_for(dt, vec, ntc, ks), a, kchunk, rows_cap, push);
 }
 
 }  // namespace lora
