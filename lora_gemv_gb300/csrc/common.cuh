@@ -164,6 +164,103 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     return false;
 }
 
+// ------------------------------------------------------------------ tcgen05
+// Fifth-generation tensor core: MMAs issued by one thread read both operands
+// from shared memory (64-bit descriptors) and accumulate in tensor memory
+// (TMEM), allocated per CTA in columns of 32-bit lanes x 128.
+
+// Shared-memory descriptor of a K-major operand in the canonical 128-byte
+// swizzled layout: rows of 128 bytes (64 fp16/bf16 of K), 8-row atoms of
+// 1024 bytes (16-byte chunk c of row r at chunk c ^ (r & 7)), atoms stacked
+// along M/N every 1024 bytes.  `addr`: shared address of the first row (an
+// atom base, or an atom base + 32 * k for the k-th 16-wide K step).
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFF) >> 4)  // start address
+           | (uint64_t)1 << 16                // leading byte offset (unused for this layout)
+           | (uint64_t)(1024 >> 4) << 32      // stride byte offset: next 8-row atom
+           | (uint64_t)1 << 46                // descriptor version
+           | (uint64_t)2 << 61;               // 128-byte swizzle
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, A and B both fp16 or
+// both bf16, both K-major, M x N.
+__host__ __device__ constexpr uint32_t tc_idesc_f16(bool bf16, int M, int N) {
+    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// One warp: allocate `ncols` (power of two >= 32) TMEM columns; the base
+// address is written to shared memory at `slot`.
+__device__ __forceinline__ void tc_alloc(uint32_t *slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     smem_u32(slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+// D[taddr] (+)= A . B^T for one M x N x 16 step (accumulate: keep D).
+__device__ __forceinline__ void tc_mma_f16(uint32_t taddr, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{ .reg .pred p;\n"
+        "  setp.ne.b32 p, %4, 0;\n"
+        "  tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }\n" ::"r"(taddr),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate ? 1 : 0)
+        : "memory");
+}
+// Arrive once on the mbarrier when this thread's earlier tcgen05 ops are done.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+// Warp-collective: this thread's TMEM lane (warp's lane quadrant + lane id),
+// 16 consecutive 32-bit columns from `taddr`.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// Makes this thread's shared-memory writes (st.shared, cp.async) visible to
+// the async proxy (tensor-core operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+// Bounded wait for phase `parity` of a CTA-local mbarrier: false once
+// kWaitPolls polls have failed.
+__device__ __forceinline__ bool mbar_wait_cta(uint64_t *bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    for (int i = 0; i < kWaitPolls; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred p;\n"
+            "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "  selp.u32 %0, 1, 0, p; }\n"
+            : "=r"(ok)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
 // Programmatic dependent launch: wait for the previous grid's results; let
 // the next grid start launching.  Both are no-ops for an ordinary launch.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }

@@ -7,20 +7,27 @@
 // bins of 16/32/64).
 //
 // Design (GB300): per plan tile (<= 64 tokens of one adapter) the cluster
-// computes Y[64, rows] = X[64, H] . A_l[rows, H]^T on the tensor cores
-// (mma.sync m16n8k16, fp32 accumulate), where rows are the adapter's
-// S * r_l live rows only (rank-aware: padded rows are never read).
+// computes Y[64, rows] = X[64, H] . A_l[rows, H]^T on the tensor cores with
+// fp32 accumulation, where rows are the adapter's S * r_l live rows only
+// (rank-aware: padded rows are never read).
 //  - H is split across a thread-block CLUSTER of up to 16 CTAs (split-K);
-//    each CTA walks its H range in 128-wide stages through two
-//    256-byte-swizzled shared-memory buffers feeding ldmatrix + mma: aligned
-//    rows are copied with cp.async, both buffers at once (for the decode
-//    split-K shapes a CTA's whole H range is then in flight), other rows
-//    through registers one stage ahead;
-//  - the 8 warps split the tile's 16-row blocks and, within a block,
-//    either its 8-column n-tiles (every output has one owner warp and the
-//    CTA partial is written straight from the accumulators) or, for batches
-//    of a few tokens per adapter, each stage's k steps (short mma chains;
-//    the warp partials are then summed in shared memory);
+//    each CTA walks its H range in 128-wide stages through two shared-memory
+//    buffers: aligned rows are copied with cp.async, both buffers at once
+//    (for the decode split-K shapes a CTA's whole H range is then in
+//    flight), other rows through registers one stage ahead;
+//  - aligned rows (batches of more than 16 tokens per adapter on average):
+//    the stages are laid out as 128-byte-swizzled K-major tcgen05 operands,
+//    one thread issues each stage's eight M = 128 x N = rows x K = 16
+//    tcgen05.mma (the x tile as A, its 64 token rows plus rows of whatever
+//    follows, whose results are never read; the adapter rows as B) into a
+//    TMEM accumulator, commits to a per-buffer mbarrier, and two warps read
+//    the 64 token lanes back with tcgen05.ld;
+//  - otherwise ldmatrix + mma.sync m16n8k16: the 8 warps split the tile's
+//    16-row blocks and, within a block, either its 8-column n-tiles (every
+//    output has one owner warp and the CTA partial is written straight from
+//    the accumulators) or, for batches of a few tokens per adapter, each
+//    stage's k steps (short mma chains; the warp partials are then summed
+//    in shared memory);
 //  - partials are summed over the cluster through distributed shared
 //    memory, in a fixed order (deterministic, no global scratch, no
 //    atomics), each CTA finishing a share of the tile's rows: every CTA
@@ -33,6 +40,7 @@
 #include <cooperative_groups.h>
 
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -61,6 +69,14 @@ __host__ __device__ constexpr int smem_bytes(int rows_cap, int ntmax) {
 // Receive buffer of the push reduction, after the above: [ksplit][64 /
 // ksplit rows][rows_cap] floats from the cluster's CTAs.
 __host__ __device__ constexpr int recv_bytes(int rows_cap) { return kTile * rows_cap * 4; }
+
+// Tensor-core path: 1024 bytes of alignment slack, the two stages in the
+// tcgen05 layout (see async_stage_tc), then the rows the M = 128 operand
+// window of the last x region reads past it (the MMA's rows 64..127 are not
+// tokens; their results are never read).
+__host__ __device__ constexpr int tc_stage_area(int rows_cap) {
+    return 1024 + 2 * 2 * (kTile + rows_cap) * 128 + (rows_cap < 64 ? (64 - rows_cap) * 128 : 0);
+}
 
 // 256-byte rows, 16-byte chunks XOR-swizzled (within each 128-byte half) by the row.
 __device__ __forceinline__ int swz(int row, int chunk) {
@@ -131,6 +147,35 @@ __device__ __forceinline__ void async_stage(unsigned char *stage, const E *__res
     }
 }
 
+// The same stage for the tensor-core (tcgen05) path: per 64-wide K half h,
+// the x tile X_h [64 rows] then the A rows A_h [rows_cap rows], 128-byte
+// rows in the canonical 128-byte swizzled K-major layout (chunk c of row r at
+// c ^ (r & 7)): [X_0][A_0][X_1][A_1], every region 1024-byte aligned.
+__host__ __device__ constexpr int tc_half_bytes(int rows_cap) { return (kTile + rows_cap) * 128; }
+template <typename E>
+__device__ __forceinline__ void async_stage_tc(unsigned char *stage, const E *__restrict__ x,
+                                               int64_t ldx, const E *__restrict__ Al, int H,
+                                               const int *s_rows, const int *s_arow, int n,
+                                               int nrows, int rows_cap, int h0, int h_end) {
+    const int half = tc_half_bytes(rows_cap);
+    for (int it = threadIdx.x; it < (kTile + nrows) * kCh; it += kThreads) {
+        const int r = it / kCh, c = it % kCh;
+        const int h = h0 + 8 * c;
+        unsigned char *region = stage + (c >> 3) * half;
+        if (r < kTile) {
+            const int row = s_rows[r];
+            if (r < n && row >= 0)
+                cp_async16(smem_u32(region + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
+                           x + (int64_t)row * ldx + (h < h_end ? h : 0), h < h_end ? 16 : 0);
+        } else {
+            const int ar = r - kTile;
+            const E *src = Al + (int64_t)s_arow[ar] * H;
+            cp_async16(smem_u32(region + kTile * 128 + ar * 128 + (((c & 7) ^ (ar & 7)) << 4)),
+                       src + (h < h_end ? h : 0), h < h_end ? 16 : 0);
+        }
+    }
+}
+
 __device__ __forceinline__ void store_stage(const uint4 (&ld)[kMaxLd], unsigned char *stage,
                                             int rows_cap, int n, int nrows) {
     uint4 *sX = reinterpret_cast<uint4 *>(stage);
@@ -153,13 +198,18 @@ __device__ __forceinline__ void store_stage(const uint4 (&ld)[kMaxLd], unsigned 
 // minimum-occupancy bound: capping registers for more resident CTAs measured
 // slower (the CTAs per SM are limited by shared memory anyway).
 // push: reduce over the cluster through the receive buffers (ksplit > 1).
-template <typename E, bool VEC, int NTMAX, bool KS>
+// TC: the contraction on the tcgen05 tensor cores (aligned rows; D = X . A^T
+// with M = 128 token lanes, N = rows_cap, accumulated in TMEM), else mma.sync.
+template <typename E, bool VEC, int NTMAX, bool KS, bool TC>
 __global__ void __launch_bounds__(kThreads)
 shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
+    static_assert(!TC || (VEC && !KS), "the tensor-core path takes aligned rows, no warp split");
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
     __shared__ int s_arow[kRows];
-    __shared__ uint64_t s_bar;  // push: the cluster's partials of this CTA's rows have arrived
+    __shared__ uint64_t s_bar;     // push: the cluster's partials of this CTA's rows have arrived
+    __shared__ uint64_t s_mma[2];  // TC: the MMAs reading stage buffer b are done
+    __shared__ uint32_t s_tmem;    // TC: TMEM base address
     constexpr int PP = part_pitch(NTMAX);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -192,14 +242,32 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
     const int h_end = min(H, h_begin + kchunk);
     const int nstages = h_end > h_begin ? (h_end - h_begin + kK - 1) / kK : 0;
     const int stage_bytes = (kTile + rows_cap) * kK * 2;
-    float *Ct = reinterpret_cast<float *>(smem);  // CTA partial [64][PP]
-    float *P = Ct + kTile * PP;                    // warp partials [8][16][PP]
-    float *Rb = reinterpret_cast<float *>(smem + smem_bytes(rows_cap, NTMAX));  // push only
+    // TC: operand regions need 1024-byte alignment
+    unsigned char *sm = smem;
+    if constexpr (TC) sm = smem + ((1024 - (smem_u32(smem) & 1023)) & 1023);
+    float *Ct = reinterpret_cast<float *>(sm);  // CTA partial [64][PP]
+    float *P = Ct + kTile * PP;                  // warp partials [8][16][PP]
+    float *Rb = reinterpret_cast<float *>(TC ? smem + tc_stage_area(rows_cap)
+                                             : smem + smem_bytes(rows_cap, NTMAX));  // push only
     const int rpo = kTile / ksplit;                // rows owned per CTA (push)
     uint32_t phase = 0;
     if (push) {  // every peer's barrier is initialised before anyone stores to it
         if (threadIdx.x == 0) mbar_init(&s_bar, 1);
         cluster_arrive_relaxed();
+    }
+    // TC: TMEM for D (>= rows_cap fp32 columns), stage-buffer barriers
+    const uint32_t tcols = rows_cap <= 32 ? 32 : (rows_cap <= 64 ? 64 : 128);
+    uint32_t tmem = 0, ncommit0 = 0, ncommit1 = 0;
+    if constexpr (TC) {
+        if (warp == 0) tc_alloc(&s_tmem, tcols);
+        if (threadIdx.x == 0) {
+            mbar_init(&s_mma[0], 1);
+            mbar_init(&s_mma[1], 1);
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        tmem = s_tmem;
     }
 
     const int n_tiles = min(h1.z, a.max_tiles);
@@ -258,7 +326,16 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
         // each stage refills its buffer two stages ahead.  Otherwise loads go
         // through registers one stage ahead.
         uint4 ld[VEC ? 1 : kMaxLd];
-        if (VEC) {
+        if constexpr (TC) {
+            if (nstages > 0)
+                async_stage_tc<E>(sm, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, rows_cap, h_begin,
+                                  h_end);
+            cp_async_commit();
+            if (nstages > 1)
+                async_stage_tc<E>(sm + stage_bytes, x, a.ldx, Al, H, s_rows, s_arow, n, nrows,
+                                  rows_cap, h_begin + kK, h_end);
+            cp_async_commit();
+        } else if (VEC) {
             if (nstages > 0)
                 async_stage<E>(smem, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, h_begin, h_end);
             cp_async_commit();
@@ -272,7 +349,38 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
             store_stage(reinterpret_cast<uint4 (&)[kMaxLd]>(ld), smem, rows_cap, n, nrows);
         }
         if (!VEC) __syncthreads();
-        for (int st = 0; st < nstages; ++st) {
+        for (int st = 0; st < nstages && TC; ++st) {
+            // tcgen05: one thread issues the stage's 8 K steps once every
+            // thread's copies have landed and been handed to the async proxy
+            unsigned char *cur = sm + (st & 1) * stage_bytes;
+            cp_async_wait<1>();
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                tc_fence_after();
+                const uint32_t idesc =
+                    tc_idesc_f16(std::is_same<E, __nv_bfloat16>::value, 128, rows_cap);
+                const uint32_t base = smem_u32(cur), half = tc_half_bytes(rows_cap);
+#pragma unroll
+                for (int k = 0; k < kK / 16; ++k) {
+                    const uint32_t xh = base + (k >> 2) * half + 32 * (k & 3);
+                    tc_mma_f16(tmem, tc_desc_sw128(xh), tc_desc_sw128(xh + kTile * 128), idesc,
+                               st > 0 || k > 0);
+                }
+                tc_commit(&s_mma[st & 1]);
+            }
+            if (st & 1) ++ncommit1;
+            else ++ncommit0;
+            if (st + 2 < nstages) {  // refill this buffer once its MMAs have read it
+                const uint32_t nc = (st & 1) ? ncommit1 : ncommit0;
+                if (!mbar_wait_cta(&s_mma[st & 1], (nc - 1) & 1) && threadIdx.x == 0)
+                    atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+                async_stage_tc<E>(cur, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, rows_cap,
+                                  h_begin + (st + 2) * kK, h_end);
+            }
+            cp_async_commit();
+        }
+        for (int st = 0; st < nstages && !TC; ++st) {
             unsigned char *cur = smem + (st & 1) * stage_bytes;
             if (VEC) {
                 cp_async_wait<1>();
@@ -321,9 +429,34 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
         }
         if (VEC) cp_async_wait<0>();
 
+        if constexpr (TC) {
+            // D (all MMAs of the tile done) -> the CTA partial: warps 0 and 1
+            // hold TMEM lanes 0..63, the tile's token slots
+            if (nstages > 0) {
+                const int lst = nstages - 1;
+                const uint32_t nc = (lst & 1) ? ncommit1 : ncommit0;
+                if (!mbar_wait_cta(&s_mma[lst & 1], (nc - 1) & 1) && threadIdx.x == 0)
+                    atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+            }
+            tc_fence_after();
+            if (warp < 2) {
+                float *crow = Ct + (32 * warp + lane) * PP;
+                const uint32_t tl = tmem + ((uint32_t)(32 * warp) << 16);
+                for (int c0 = 0; c0 < nrows; c0 += 16) {
+                    float v[16];
+                    tc_ld16(tl + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4 *>(crow + c0 + j) =
+                            nstages > 0 ? make_float4(v[j], v[j + 1], v[j + 2], v[j + 3])
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            tc_fence_before();
+        }
         // the CTA partial: straight from each owner warp's accumulators, or
         // the k-split warps' partials summed in warp order
-        if (wact) {
+        if (!TC && wact) {
             float *c0 = (kparts == 1 ? Ct + mb * 16 * PP : P + warp * 16 * PP) + g * PP + 2 * q;
 #pragma unroll
             for (int j = 0; j < NTW; ++j) {
@@ -415,40 +548,52 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
         else __syncthreads();
     }
     if (push) cluster_wait();  // no CTA leaves while a peer may still store into it
+    if constexpr (TC) {
+        __syncthreads();
+        tc_fence_after();
+        if (warp == 0) tc_dealloc(tmem, tcols);
+    }
 }
 
 using ShrinkFn = void (*)(const ShrinkArgs, int, int, int);
 
+// Kernel variants: mma.sync with n-split warps, mma.sync with k-split warps,
+// tcgen05 (aligned rows only).
+enum Variant { kNSplit = 0, kKSplit = 1, kTensor = 2, kVariants = 3 };
+
 // Instantiation for n-tile class c (NTMAX = 2 << c).
-template <typename E, bool VEC, bool KS>
+template <typename E, bool VEC, bool KS, bool TC>
 ShrinkFn kernel_nt(int c) {
     switch (c) {
-        case 0: return shrink_kernel<E, VEC, 2, KS>;
-        case 1: return shrink_kernel<E, VEC, 4, KS>;
-        case 2: return shrink_kernel<E, VEC, 8, KS>;
-        default: return shrink_kernel<E, VEC, 16, KS>;
+        case 0: return shrink_kernel<E, VEC, 2, KS, TC>;
+        case 1: return shrink_kernel<E, VEC, 4, KS, TC>;
+        case 2: return shrink_kernel<E, VEC, 8, KS, TC>;
+        default: return shrink_kernel<E, VEC, 16, KS, TC>;
     }
 }
 
+// nullptr for the combination that does not exist (tcgen05 with unaligned rows)
 template <typename E>
-ShrinkFn kernel_e(bool vec, int c, bool ks) {
-    if (vec) return ks ? kernel_nt<E, true, true>(c) : kernel_nt<E, true, false>(c);
-    return ks ? kernel_nt<E, false, true>(c) : kernel_nt<E, false, false>(c);
+ShrinkFn kernel_e(bool vec, int c, int var) {
+    if (var == kTensor) return vec ? kernel_nt<E, true, false, true>(c) : nullptr;
+    const bool ks = var == kKSplit;
+    if (vec) return ks ? kernel_nt<E, true, true, false>(c) : kernel_nt<E, true, false, false>(c);
+    return ks ? kernel_nt<E, false, true, false>(c) : kernel_nt<E, false, false, false>(c);
 }
 
-ShrinkFn kernel_for(int dt, bool vec, int c, bool ks) {
-    return dt == LORA_F16 ? kernel_e<__half>(vec, c, ks) : kernel_e<__nv_bfloat16>(vec, c, ks);
+ShrinkFn kernel_for(int dt, bool vec, int c, int var) {
+    return dt == LORA_F16 ? kernel_e<__half>(vec, c, var) : kernel_e<__nv_bfloat16>(vec, c, var);
 }
 
 // Residency tables, filled by configure_shrink_kernels:
 //  - CTAs per SM of each instantiation without dynamic shared memory
-//    (registers, threads), [dtype][vec][n-tile class][ks], and its static
-//    shared memory;
+//    (registers, threads), [dtype][vec][n-tile class][variant], and its
+//    static shared memory;
 //  - clusters of 1, 2, 4, 8, 16 CTAs the GPU holds at once when k CTAs fit
 //    per SM, [k][log2 cluster] (clusters are placed within one GPC, so this
 //    is below k x SMs / cluster).
-int g_reg_occ[2][2][4][2] = {};
-int g_static_smem[2][2][4][2] = {};
+int g_reg_occ[2][2][4][kVariants] = {};
+int g_static_smem[2][2][4][kVariants] = {};
 int g_cap[9][5] = {};
 int g_smem_sm = 0, g_smem_reserved = 0;
 
@@ -461,7 +606,7 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
     // Largest cluster the GPU can hold with this kernel's largest shared memory.
     int max_cluster = 8;
     {
-        const ShrinkFn k = kernel_for(LORA_F16, true, 3, false);
+        const ShrinkFn k = kernel_for(LORA_F16, true, 3, kNSplit);
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -517,11 +662,14 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
     for (int dt = 0; dt < 2; ++dt)
         for (int vec = 0; vec < 2; ++vec)
             for (int c = 0; c < 4; ++c)
-                for (int ks = 0; ks < 2; ++ks) {
-                    const ShrinkFn k = kernel_for(dt, vec, c, ks);
+                for (int var = 0; var < kVariants; ++var) {
+                    const ShrinkFn k = kernel_for(dt, vec, c, var);
+                    if (!k) continue;
                     const int ntmax = 2 << c;
+                    const int stage_max = var == kTensor ? tc_stage_area(std::min(ntmax * 8, kRows))
+                                                         : smem_bytes(kRows, ntmax);
                     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             smem_bytes(kRows, ntmax) + recv_bytes(kRows));
+                                             stage_max + recv_bytes(kRows));
                     // all of the SM's unified L1 / shared memory may serve as shared
                     // memory (the residency tables assume it)
                     if (e == cudaSuccess)
@@ -529,12 +677,19 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
                                                  cudaSharedmemCarveoutMaxShared);
                     if (e == cudaSuccess && max_cluster > 8)
                         e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-                    if (e == cudaSuccess)
-                        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&g_reg_occ[dt][vec][c][ks], k,
-                                                                          kThreads, 0);
+                    // CTAs per SM by registers (allocated per warp in units of 8 per
+                    // thread) and threads.  The occupancy API answers 1 for kernels
+                    // that allocate tensor memory; their TMEM use (<= 128 columns
+                    // per CTA) never limits residency here: <= 4 CTAs fit by shared
+                    // memory, 4 x 128 <= 512 columns.
                     cudaFuncAttributes fa;
                     if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k);
-                    if (e == cudaSuccess) g_static_smem[dt][vec][c][ks] = (int)fa.sharedSizeBytes;
+                    if (e == cudaSuccess) {
+                        g_static_smem[dt][vec][c][var] = (int)fa.sharedSizeBytes;
+                        const int regs_cta = (fa.numRegs + 7) / 8 * 8 * kThreads;
+                        g_reg_occ[dt][vec][c][var] =
+                            std::max(1, std::min(65536 / std::max(regs_cta, 1), 2048 / kThreads));
+                    }
                     if (e != cudaSuccess) return e;
                 }
     return cudaSuccess;
@@ -555,16 +710,20 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     const int ntmax = rows_cap / 8 <= 2 ? 2 : rows_cap / 8 <= 4 ? 4 : rows_cap / 8 <= 8 ? 8 : 16;
     // CTAs resident per SM (registers and shared memory)
     const int ntc = ntmax == 2 ? 0 : ntmax == 4 ? 1 : ntmax == 8 ? 2 : 3;
-    // warps split k steps when adapters average at most one 16-token row block
+    // Batches averaging at most one 16-token row block per adapter: mma.sync
+    // with warps splitting k steps (a tile's work is too small to pay for the
+    // tensor-memory setup); otherwise tcgen05 for aligned rows, else mma.sync
+    // with warps splitting n-tiles.
     const bool ks = a.T <= 16LL * std::min(a.L, a.T);
+    const int var = ks ? kKSplit : (vec ? kTensor : kNSplit);
     // CTAs resident per SM with `dyn` bytes of dynamic shared memory
-    const int vi = vec ? 1 : 0, ki = ks ? 1 : 0;
+    const int vi = vec ? 1 : 0;
     auto resident = [&](size_t dyn) {
         const long long by_smem =
-            g_smem_sm / ((long long)dyn + g_static_smem[dt][vi][ntc][ki] + g_smem_reserved);
-        return (int)std::max(1LL, std::min<long long>({by_smem, g_reg_occ[dt][vi][ntc][ki], 8}));
+            g_smem_sm / ((long long)dyn + g_static_smem[dt][vi][ntc][var] + g_smem_reserved);
+        return (int)std::max(1LL, std::min<long long>({by_smem, g_reg_occ[dt][vi][ntc][var], 8}));
     };
-    size_t smem = smem_bytes(rows_cap, ntmax);
+    size_t smem = var == kTensor ? tc_stage_area(rows_cap) : smem_bytes(rows_cap, ntmax);
     const int occ = resident(smem);
     // the push reduction's receive buffer, where it costs no residency
     const bool push_fits = resident(smem + recv_bytes(rows_cap)) == occ;
@@ -595,7 +754,7 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kernel_for(dt, vec, ntc, ks), a, kchunk, rows_cap, push);
+    return cudaLaunchKernelEx(&cfg, kernel_for(dt, vec, ntc, var), a, kchunk, rows_cap, push);
 }
 
 }  // namespace lora
