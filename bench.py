@@ -95,6 +95,62 @@ def algorithmic(idx: torch.Tensor):
     return sh_bytes, sh_flops, ex_bytes, ex_flops
 
 
+def prefill_sgmv(lg, dev, hbm_gbs: float, tc_tflops: float, reps: int = 20):
+    """The prefill SGMV gate/up workload (8 segments, log-uniform lengths in
+    [8, 2048], adapters A A A B C C D D, H = 4096, gate/up slices of 14336,
+    fp16), per rank r: shrink and expand_slice each timed with CUDA events
+    around a graph of `reps` back-to-back launches (x rotated over copies
+    larger than L2, out > L2), against the roofline max(algorithmic bytes /
+    HBM, flops / tensor peak)."""
+    res = {}
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    for r in (16, 32, 64):
+        c = li.prefill_gateup(r=r)
+        T, S, N = c.T, c.num_slices, c.B[0].shape[1]
+        U = int(torch.unique(c.seg_lora[c.seg_len > 0]).numel())
+        ncopy = max(2, -(-2 * l2 // (T * H * 2)))
+        xs = [c.x.to(dev) for _ in range(ncopy)]
+        ys = [torch.empty(T, S * r, dtype=torch.float32, device=dev) for _ in range(ncopy)]
+        A = c.A.to(dev)
+        Bs = [b.to(dev) for b in c.B]
+        out = c.out.to(dev)
+        plan = lg.new_plan(T, c.L, dev)
+        lg.lora_group_segments(c.seg_start.to(dev), c.seg_len.to(dev), c.seg_lora.to(dev), T, c.L,
+                               plan)
+        torch.cuda.synchronize()
+
+        def timed(launch):
+            stream = torch.cuda.Stream()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(reps):
+                    launch(i % ncopy)
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) / reps / 1e3
+
+        t_sh = timed(lambda i: lg.lora_shrink(xs[i], A, ys[i], plan, num_slices=S))
+        t_ex = timed(lambda i: lg.lora_expand_slice(ys[i], Bs, out, plan, c.slice_offsets,
+                                                    y_slice_stride=r, add_inputs=True))
+        sh_b = T * H * 2 + U * S * r * H * 2 + T * S * r * 4
+        sh_f = 2 * T * H * S * r
+        ex_b = T * S * r * 4 + U * S * N * r * 2 + 2 * T * S * N * 2
+        ex_f = 2 * T * S * N * r
+        out_r = {"T": T}
+        for name, t, b, f in (("shrink", t_sh, sh_b, sh_f), ("expand_slice", t_ex, ex_b, ex_f)):
+            t_mem, t_tc = b / (hbm_gbs * 1e9), f / (tc_tflops * 1e12)
+            out_r[name] = {"us": t * 1e6, "GBps": b / t / 1e9, "TFLOPs": f / t / 1e12,
+                           "bound": "hbm" if t_mem >= t_tc else "tensor",
+                           "roofline_frac": max(t_mem, t_tc) / t}
+        res[f"r{r}"] = out_r
+        del xs, ys, out
+    return res
+
+
 def algorithmic_fused(idx: torch.Tensor):
     """Fused shrink + expand_slice: x, live A rows, y written once, live B
     rows, out read and written (y is not re-read from HBM)."""
@@ -198,8 +254,8 @@ FUSED_STEP = True  # shrink + expand_slice through the chained (PDL) entry point
 # from an ncu capture of `bench.py --profile --T 1024` (summaries under
 # profiles/); None until a capture of the current kernel exists.
 NCU_TRAFFIC = {
-    "shrink": {"bytes": 9168640, "source": "ncu --set full, dram__bytes_read.sum 9.169 MB + "
-               "dram__bytes_write.sum 0 (y stays in L2), T=1024 launch"},
+    "shrink": {"bytes": 9176576, "source": "ncu --set full, dram__bytes_read.sum 9.177 MB + "
+               "dram__bytes_write.sum 0 (y stays in L2), T=1024 launch (tcgen05 variant)"},
     "expand_slice": {"bytes": 12329984, "source": "ncu --set full, dram__bytes_read.sum 12.33 MB + "
                      "dram__bytes_write.sum 0 (out written back after the launch), T=1024 launch"},
 }
@@ -509,6 +565,7 @@ def main_ours(args):
                 "how": "public Python API per call (no graph), pinned host buffers"},
         "clocks": clk,
         "per_T": per_T,
+        "prefill_sgmv": prefill_sgmv(lg, dev, hbm, tf),
         "wall_s_timed": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:
