@@ -328,9 +328,9 @@ expand_kernel(const ExpandArgs a) {
 // measured far lower).
 constexpr int kWThreads = 128;  // 4 independent warps per CTA
 constexpr int kWCols = 32;      // output columns per warp unit
-// Token rows per warp unit: MB m16 blocks, MB = 2 for ranks <= 64 and 1 above
+// Token rows per warp unit: MB m16 blocks, MB = 2 for ranks <= 32 and 1 above
 // (the y fragments of a unit live in registers).
-__host__ __device__ constexpr int warp_mb(int ksmax) { return ksmax >= 8 ? 1 : 2; }
+__host__ __device__ constexpr int warp_mb(int ksmax) { return ksmax >= 4 ? 1 : 2; }
 
 // Loads of one warp unit that are issued a unit ahead.
 template <int MB, int KSMAX>
@@ -357,7 +357,7 @@ __device__ __forceinline__ void issue_unit(const ExpandArgs &a, UnitLoads<MB, KS
 }
 
 template <typename E, bool ADD, int KSMAX>
-__global__ void __launch_bounds__(kWThreads)
+__global__ void __launch_bounds__(kWThreads, KSMAX >= 8 ? 0 : (KSMAX >= 2 ? 3 : 4))
 expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     constexpr int MB = warp_mb(KSMAX);
     constexpr int kWRows = 16 * MB;
@@ -377,23 +377,10 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     const int4 h1 = __ldg(reinterpret_cast<const int4 *>(a.hdr) + 1);
     int t = u_begin / per_tile;
     int4 tl = t < a.max_tiles ? __ldg(a.tiles + t) : make_int4(-1, 0, 0, 0);
-    if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
-        return;
-    }
-    const int n_tiles = min(h1.z, a.max_tiles);
-    const int u_end = min(n_tiles * per_tile, u_begin + per);
-    if (u_begin >= u_end) return;
-    E *__restrict__ out = static_cast<E *>(a.out);
-
-    // position of the current unit
+    // position of the current unit, and its token rows (the plan's per-tile
+    // row lists, -1 padded), read in the same round trip as the header
     int part = (u_begin - t * per_tile) / ncb;
     int cbi = u_begin - t * per_tile - part * ncb;
-
-    // per (tile, part) state
-    int rows[MB][2];
-    int rl = 0, KS = 0, nrow = 0;
-    // a tile's token rows come from the plan's per-tile row lists (-1 padded)
     auto load_rows = [&](int tt, int pt, int (&r)[MB][2]) {
 #pragma unroll
         for (int mm = 0; mm < MB; ++mm)
@@ -403,12 +390,24 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
                 r[mm][h] = row >= a.T ? -1 : row;
             }
     };
+    int rows[MB][2];
+    load_rows(t < a.max_tiles ? t : 0, part, rows);
+    if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
+        return;
+    }
+    const int n_tiles = min(h1.z, a.max_tiles);
+    const int u_end = min(n_tiles * per_tile, u_begin + per);
+    if (u_begin >= u_end) return;
+    E *__restrict__ out = static_cast<E *>(a.out);
+
+    // per (tile, part) state
+    int rl = 0, KS = 0, nrow = 0;
     auto slice_of = [&](int c, int &s, int &c0) {
         s = 0;
         while (s + 1 < a.num_slices && c >= a.chunk_begin[s + 1]) ++s;
         c0 = (c - a.chunk_begin[s]) * kWCols;
     };
-    load_rows(t < a.max_tiles ? t : 0, part, rows);
     rl = tl.x >= 0 && tl.x < a.L ? clamp_rank(a.ranks, tl.x, a.R) : 0;
     KS = (rl + 15) / 16;
     nrow = min(kWRows, tl.z - part * kWRows);
@@ -626,7 +625,8 @@ cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceI
         for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s];
         const int ncb = a.chunk_begin[a.num_slices];
         if (ncb == 0) return cudaSuccess;
-        const long long units = (long long)tiles_grid * (kTile / (16 * warp_mb((a.R + 15) / 16 > 4 ? 8 : 1))) * ncb;
+        const int kss = (a.R + 15) / 16, ksmax = kss <= 1 ? 1 : kss <= 2 ? 2 : kss <= 4 ? 4 : 8;
+        const long long units = (long long)tiles_grid * (kTile / (16 * warp_mb(ksmax))) * ncb;
         const int occ = std::max(1, g_warp_occ[dt][a.add ? 1 : 0][ks_class((a.R + 15) / 16)]);
         const long long warps_max = (long long)dev.sm_count * occ * (kWThreads / 32);
         const long long warps = std::min(units, warps_max);

@@ -230,6 +230,10 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
     const int4 h1 = __ldcg(reinterpret_cast<const int4 *>(a.hdr) + 1);  // nactive, ngroups, ntiles
     int4 tl_next = (int)blockIdx.y < a.max_tiles ? __ldcg(a.tiles + blockIdx.y)
                                                  : make_int4(-1, 0, 0, -1);
+    // ... and its token rows (-1 past its count)
+    int row_next = threadIdx.x < kTile && (int)blockIdx.y < a.max_tiles
+                       ? __ldcg(a.tile_rows + (int64_t)blockIdx.y * kTile + threadIdx.x)
+                       : -1;
     if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
             atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
@@ -273,12 +277,14 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
     const int n_tiles = min(h1.z, a.max_tiles);
     for (int tile = blockIdx.y; tile < n_tiles; tile += gridDim.y) {
         const int4 tl = tl_next;
-        if (tile + (int)gridDim.y < n_tiles) tl_next = __ldcg(a.tiles + tile + gridDim.y);
+        const int my_row = row_next < a.T ? row_next : -1;
+        if (tile + (int)gridDim.y < n_tiles) {  // the next tile's record and rows, a tile ahead
+            tl_next = __ldcg(a.tiles + tile + gridDim.y);
+            if (threadIdx.x < kTile)
+                row_next = __ldcg(a.tile_rows + (int64_t)(tile + gridDim.y) * kTile + threadIdx.x);
+        }
         const int l = tl.x, n = tl.z;
         const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
-        // the tile's token rows (-1 past its count) load with the tile record
-        int my_row = threadIdx.x < kTile ? __ldcg(a.tile_rows + (int64_t)tile * kTile + threadIdx.x) : -1;
-        if (my_row >= a.T) my_row = -1;
 
         // y columns that get no term: every column of inactive tokens, the
         // columns i >= r_l of each slice otherwise.  Written by one CTA.
