@@ -20,6 +20,8 @@
 //    two, so the product keeps ~fp32 accuracy of y and never overflows fp16;
 //  - tiles with adapter -1 and adapters of rank 0 load nothing (block
 //    skipping) and, without add_inputs, only store zeros.
+#include <type_traits>
+
 #include "common.cuh"
 #include "frag.cuh"
 #include "kernels.h"
@@ -517,6 +519,201 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core expand (aligned shapes, ranks above 48): one CTA per (plan
+// tile, 128 output columns of one slice).  All of the unit's operands are requested at once:
+// the out block (add_inputs) and the B block before the dependency wait, the
+// y rows after it.  The y rows become scaled hi/lo fp16/bf16 pairs (per-row
+// power-of-two scale, as in the warp kernel) in the 128-byte-swizzled K-major
+// layout; one thread issues D = Y_hi . B^T + Y_lo . B^T as tcgen05.mma
+// (M = 128 token lanes, the tile's 64 tokens plus rows of whatever follows,
+// whose results are never read; N = 128 columns; K = 16 per step) into
+// TMEM; warps 0 and 1 read their token lanes back, scale, add the old out
+// values and store 16-byte groups.
+constexpr int kTcCols = 128;                    // output columns per CTA (N)
+constexpr int kTcOutPitch = kTcCols * 2 + 16;   // bytes per staged out row
+
+// Shared memory: [Yh | Yl] per 64-wide rank half, then the B halves, the out
+// block and the fp32 y rows; 1024 bytes of alignment slack in front.
+__host__ __device__ constexpr int tc_halves(int R) { return R > 64 ? 2 : 1; }
+__host__ __device__ constexpr int tc_ypitch(int R) { return (R + 15) / 16 * 16; }  // floats
+__host__ __device__ constexpr int tc_expand_smem(int R) {
+    return 1024 + tc_halves(R) * (2 * kTile * 128 + kTcCols * 128) + kTile * kTcOutPitch +
+           kTile * tc_ypitch(R) * 4;
+}
+
+template <typename E, bool ADD>
+__global__ void __launch_bounds__(kThreads)
+expand_tc_kernel(const ExpandArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int s_rows[kTile];
+    __shared__ float s_f[kTile];
+    __shared__ uint64_t s_bar;
+    __shared__ uint32_t s_tmem;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tile = blockIdx.x, chunk = blockIdx.y;
+
+    // plan header, tile record and token rows in one round trip
+    const int4 h0 = __ldg(reinterpret_cast<const int4 *>(a.hdr));
+    const int4 h1 = __ldg(reinterpret_cast<const int4 *>(a.hdr) + 1);
+    const int4 tl = tile < a.max_tiles ? __ldg(a.tiles + tile) : make_int4(-1, 0, 0, 0);
+    int my_row = threadIdx.x < kTile && tile < a.max_tiles
+                     ? __ldg(a.tile_rows + (int64_t)tile * kTile + threadIdx.x)
+                     : -1;
+    if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
+        if (tile == 0 && chunk == 0 && threadIdx.x == 0)
+            atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
+        return;
+    }
+    if (tile >= min(h1.z, a.max_tiles)) return;
+    if (threadIdx.x < kTile) s_rows[threadIdx.x] = my_row < a.T ? my_row : -1;
+
+    int s = 0;
+    while (s + 1 < a.num_slices && chunk >= a.chunk_begin[s + 1]) ++s;
+    const int n0 = (chunk - a.chunk_begin[s]) * kTcCols;
+    const int ncols = min(kTcCols, a.N[s] - n0);
+    const int64_t col0 = (int64_t)a.off[s] + n0;
+    const int l = tl.x, n = tl.z;
+    const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, a.R) : 0;
+    E *__restrict__ out = static_cast<E *>(a.out);
+    __syncthreads();
+
+    if (rl == 0) {  // adapter -1 or rank 0: untouched with add_inputs, zeros without
+        grid_dep_wait();
+        grid_dep_launch();
+        if (!ADD)
+            for (int it = threadIdx.x; it < n * (ncols / 8); it += kThreads) {
+                const int i = it / (ncols / 8), c8 = it - i * (ncols / 8);
+                const int row = s_rows[i];
+                if (row >= 0) st_global_v4(out + (int64_t)row * a.ldo + col0 + 8 * c8, make_uint4(0, 0, 0, 0));
+            }
+        return;
+    }
+
+    const int R = a.R, KS = (rl + 15) / 16, KH = tc_halves(R), YP = tc_ypitch(R);
+    unsigned char *sm = smem + ((1024 - (smem_u32(smem) & 1023)) & 1023);
+    unsigned char *sY = sm;                                   // [KH][Yh 64 rows | Yl 64 rows] x 128 B
+    unsigned char *sB = sY + KH * 2 * kTile * 128;             // [KH][128 rows] x 128 B
+    unsigned char *sO = sB + KH * kTcCols * 128;               // [64][kTcOutPitch]
+    float *sYf = reinterpret_cast<float *>(sO + kTile * kTcOutPitch);  // [64][YP]
+
+    if (warp == 0) tc_alloc(&s_tmem, kTcCols);
+    if (threadIdx.x == 0) mbar_init(&s_bar, 1);
+
+    // out block and B block (neither written by the previous kernel)
+    const E *Bl = static_cast<const E *>(a.B[s]) + ((int64_t)l * a.N[s] + n0) * R;
+    if (ADD)
+        for (int it = threadIdx.x; it < n * (ncols / 8); it += kThreads) {
+            const int i = it / (ncols / 8), c8 = it - i * (ncols / 8);
+            const int row = s_rows[i];
+            if (row >= 0)
+                cp_async16(smem_u32(sO + i * kTcOutPitch + 16 * c8),
+                           out + (int64_t)row * a.ldo + col0 + 8 * c8, 16);
+        }
+    for (int it = threadIdx.x; it < ncols * KS * 2; it += kThreads) {  // 8 ranks per chunk
+        const int j = it / (KS * 2), k8 = it - j * (KS * 2);
+        const int nv = min(8, rl - 8 * k8);  // live ranks in this chunk
+        cp_async16(smem_u32(sB + (k8 >> 3) * kTcCols * 128 + j * 128 + (((k8 & 7) ^ (j & 7)) << 4)),
+                   Bl + (int64_t)j * R + (nv > 0 ? 8 * k8 : 0), nv > 0 ? 2 * nv : 0);
+    }
+    cp_async_commit();
+
+    // y rows: produced by the previous kernel
+    grid_dep_wait();
+    grid_dep_launch();
+    const float *ys = a.y + (int64_t)s * a.y_slice_stride;
+    for (int it = threadIdx.x; it < n * KS * 4; it += kThreads) {  // 4 ranks per chunk
+        const int i = it / (KS * 4), k4 = it - i * (KS * 4);
+        const int row = s_rows[i];
+        const int nv = row >= 0 ? min(4, rl - 4 * k4) : 0;
+        cp_async16(smem_u32(sYf + i * YP + 4 * k4),
+                   ys + (int64_t)(row >= 0 ? row : 0) * a.ldy + (nv > 0 ? 4 * k4 : 0),
+                   nv > 0 ? 4 * nv : 0);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // y -> scaled hi/lo operands; the KS*2 threads of a row reduce its max
+    {
+        const int G = KS * 2;  // 2, 4, 8 or 16 chunks of 8 ranks per row
+        for (int it = threadIdx.x; it < kTile * G; it += kThreads) {
+            const int i = it / G, k8 = it - i * G;
+            float v[8];
+            float m = 0.f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                v[k] = i < n ? sYf[i * YP + 8 * k8 + k] : 0.f;
+                m = fmaxf(m, fabsf(v[k]));
+            }
+            for (int o = 1; o < G; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            const int e = row_exponent(m);
+            const float inv = exp2i(-e);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] *= inv;
+            uint4 hi, lo;
+            split_hilo8<E>(v, hi, lo);
+            unsigned char *yh = sY + (k8 >> 3) * 2 * kTile * 128;
+            const int off = i * 128 + (((k8 & 7) ^ (i & 7)) << 4);
+            *reinterpret_cast<uint4 *>(yh + off) = hi;
+            *reinterpret_cast<uint4 *>(yh + kTile * 128 + off) = lo;
+            if (k8 == 0) s_f[i] = a.scale * exp2i(e);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (threadIdx.x == 0) {
+        const uint32_t idesc = tc_idesc_f16(std::is_same<E, __nv_bfloat16>::value, 128, kTcCols);
+        for (int k = 0; k < KS; ++k) {
+            const int h = k >> 2;
+            const uint32_t yh = smem_u32(sY) + h * 2 * kTile * 128 + 32 * (k & 3);
+            const uint32_t bb = smem_u32(sB) + h * kTcCols * 128 + 32 * (k & 3);
+            tc_mma_f16(tmem, tc_desc_sw128(yh), tc_desc_sw128(bb), idesc, k > 0);
+            tc_mma_f16(tmem, tc_desc_sw128(yh + kTile * 128), tc_desc_sw128(bb), idesc, true);
+        }
+        tc_commit(&s_bar);
+    }
+    if (!mbar_wait_cta(&s_bar, 0) && threadIdx.x == 0)
+        atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+    tc_fence_after();
+
+    // epilogue: warps 0 and 1 own the tile's 64 token lanes
+    if (warp < 2) {
+        const int i = 32 * warp + lane;
+        const int row = i < n ? s_rows[i] : -1;
+        const float f = s_f[i];
+        const uint32_t tl_addr = tmem + ((uint32_t)(32 * warp) << 16);
+        for (int c0 = 0; c0 < ncols; c0 += 16) {  // warp-uniform
+            float d[16];
+            tc_ld16(tl_addr + c0, d);
+            if (row < 0) continue;
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                const int c = c0 + 8 * hlf;
+                if (c >= ncols) break;
+                float v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = f * d[8 * hlf + k];
+                if (ADD) {
+                    float o[8];
+                    unpack8<E>(*reinterpret_cast<const uint4 *>(sO + i * kTcOutPitch + 2 * c), o);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[k] += o[k];
+                }
+                st_global_v4(out + (int64_t)row * a.ldo + col0 + c, pack8<E>(v));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tc_dealloc(tmem, kTcCols);
+}
+
 template <typename E, bool ADD, bool VEC>
 cudaError_t configure_one() {
     const int ks = LORA_MAX_RANK / 16;
@@ -526,8 +723,41 @@ cudaError_t configure_one() {
 }
 
 template <typename E>
+cudaError_t configure_tc() {
+    cudaError_t e = cudaSuccess;
+    for (int add = 0; add < 2; ++add) {
+        const void *k = add ? reinterpret_cast<const void *>(expand_tc_kernel<E, true>)
+                            : reinterpret_cast<const void *>(expand_tc_kernel<E, false>);
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 tc_expand_smem(LORA_MAX_RANK));
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess) return e;
+    }
+    return e;
+}
+
+template <typename E>
+cudaError_t launch_tc(const ExpandArgs &a, dim3 grid, cudaStream_t st, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = tc_expand_smem(a.R);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (a.add) return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, true>, a);
+    return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, false>, a);
+}
+
+template <typename E>
 cudaError_t configure_dtype() {
     cudaError_t e;
+    if ((e = configure_tc<E>()) != cudaSuccess) return e;
     if ((e = configure_one<E, false, false>()) != cudaSuccess) return e;
     return configure_one<E, true, false>();
 }
@@ -617,6 +847,25 @@ cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceI
     for (int s = 0; s < a.num_slices; ++s)
         vec = vec && a.off[s] % 8 == 0 && a.N[s] % 8 == 0 &&
               (reinterpret_cast<uintptr_t>(a.B[s]) & 15) == 0;
+    const bool y_vec = (reinterpret_cast<uintptr_t>(a.y) & 15) == 0 && a.ldy % 4 == 0 &&
+                       a.y_slice_stride % 4 == 0;
+    // Ranks above 48 (4+ k steps): the tensor-core kernel (one round trip for
+    // a unit's operands; the warp kernel's per-unit B re-reads and register
+    // pressure grow with the rank).  Measured: prefill gate/up r = 64 expand
+    // 363 -> 276 us; at r <= 32 and for decode batches the warp kernel is
+    // faster (its units are lighter than a CTA's load/convert/MMA chain).
+    if (vec && y_vec && (a.R + 15) / 16 >= 4) {
+        // tensor-core path: 128-column chunks per slice
+        a.chunk_begin[0] = 0;
+        for (int s = 0; s < a.num_slices; ++s)
+            a.chunk_begin[s + 1] = a.chunk_begin[s] + (a.N[s] + kTcCols - 1) / kTcCols;
+        for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s];
+        const int chunks = a.chunk_begin[a.num_slices];
+        if (chunks == 0) return cudaSuccess;
+        const dim3 grid(tiles_grid, chunks);
+        return dt == LORA_F16 ? launch_tc<__half>(a, grid, stream, pdl)
+                              : launch_tc<__nv_bfloat16>(a, grid, stream, pdl);
+    }
     if (vec) {
         // 32-column blocks per slice (prefix sums in chunk_begin)
         a.chunk_begin[0] = 0;
