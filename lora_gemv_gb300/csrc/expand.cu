@@ -634,16 +634,19 @@ expand_tc_kernel(const ExpandArgs a) {
     cp_async_wait<0>();
     __syncthreads();
 
-    // y -> scaled hi/lo operands; the KS*2 threads of a row reduce its max
+    // y -> scaled hi/lo operands.  The G threads of a row (G = KS * 2 chunks
+    // of 8 ranks rounded up to a power of two, so a row's group is aligned
+    // inside one warp) reduce its max; padding chunks hold zeros.
     {
-        const int G = KS * 2;  // 2, 4, 8 or 16 chunks of 8 ranks per row
+        const int G = KS <= 1 ? 2 : (KS <= 2 ? 4 : (KS <= 4 ? 8 : 16));
         for (int it = threadIdx.x; it < kTile * G; it += kThreads) {
             const int i = it / G, k8 = it - i * G;
+            const bool live = i < n && k8 < KS * 2;
             float v[8];
             float m = 0.f;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                v[k] = i < n ? sYf[i * YP + 8 * k8 + k] : 0.f;
+                v[k] = live ? sYf[i * YP + 8 * k8 + k] : 0.f;
                 m = fmaxf(m, fabsf(v[k]));
             }
             for (int o = 1; o < G; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));

@@ -184,6 +184,22 @@ def test_edge_shapes(cuda_lib, dtype, T, H, R, L, Ns):
     full_check(cuda_lib, c)
 
 
+# Ranks above 48 take the tcgen05 expand: rank-aware adapters (ranks 0, 1,
+# 17, 33 and the full R, K steps padded past the rank), R not a multiple of
+# 16, both add_inputs settings, ragged tiles and slices.
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("add", [False, True])
+@pytest.mark.parametrize("T,R,ranks,Ns", [
+    (200, 64, [0, 1, 17, 33, 64], [256, 136]),
+    (77, 56, None, [200]),
+    (130, 128, [128, 65, 3], [384, 8]),
+])
+def test_large_rank_expand(cuda_lib, dtype, add, T, R, ranks, Ns):
+    L = len(ranks) if ranks else 3
+    c = make_case(T, 512, R, L, Ns, dtype, seed=T + R + add, add=add, ranks=ranks)
+    full_check(cuda_lib, c)
+
+
 def skewed_idx(T, counts, seed):
     """Token indices giving adapter a exactly counts[a] tokens (the rest -1),
     shuffled: tiles of every size in one batch."""
