@@ -28,7 +28,9 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "lora_oracle.c")
-_LIB = os.path.join(_HERE, "liblora_oracle.so")
+# A prebuilt library may be named by LORA_ORACLE_LIB (the mutation tests load
+# deliberately broken copies of the oracle this way); it is used as is.
+_LIB = os.environ.get("LORA_ORACLE_LIB") or os.path.join(_HERE, "liblora_oracle.so")
 _lib = None
 
 TILE_DEFAULT = 64
@@ -36,6 +38,8 @@ TILE_DEFAULT = 64
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (plain -O2, no fast-math: IEEE double)."""
+    if os.environ.get("LORA_ORACLE_LIB"):
+        return _LIB
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",

@@ -209,6 +209,27 @@ def test_expand_slice_equals_concatenated_expand():
     np.testing.assert_array_equal(sliced, seq)
 
 
+def test_expand_slice_reads_each_slice_y_block():
+    """vLLM PR #11579 (num_slices): slice s of a stacked shrink output lives in
+    y columns [s*R, (s+1)*R); expand_slice with y_stride = R equals one
+    single-slice expand per y column block into that slice's out columns."""
+    g = rng(11)
+    T, R, L = 17, 5, 3
+    Ns = [6, 4, 9]
+    offs = [0, 6, 10]
+    Bs = [g.standard_normal((L, n, R)) for n in Ns]
+    y = g.standard_normal((T, 3 * R + 2))  # ldy > S * R
+    out0 = g.standard_normal((T, sum(Ns) + 3))
+    idx = g.integers(-1, L, T).astype(np.int32)
+    sliced = oracle.expand_slice(y, Bs, offs, idx, out0, y_stride=R, scale=0.7)
+    for s in range(3):
+        cols = slice(offs[s], offs[s] + Ns[s])
+        part = oracle.expand(y[:, s * R:(s + 1) * R].copy(), Bs[s], idx, out0[:, cols].copy(),
+                             scale=0.7)
+        np.testing.assert_array_equal(sliced[:, cols], part)
+    np.testing.assert_array_equal(sliced[:, sum(Ns):], out0[:, sum(Ns):])
+
+
 def test_expand_slice_leaves_other_columns():
     g = rng(7)
     T, R, L = 9, 4, 2
@@ -246,6 +267,42 @@ def test_rank_aware_equals_zero_padded():
     o_g = oracle.expand(y_g, f64(garbage.B[0]), lo, f64(garbage.out), ranks=garbage.ranks.numpy())
     o_z = oracle.expand(y_z, f64(zero.B[0]), lo, f64(zero.out))
     np.testing.assert_array_equal(o_g, o_z)
+
+
+def test_rank_aware_ignores_padding_in_y_and_b():
+    """Punica issue #17 (ranks are not padded to bins): adapter l contributes
+    through its first rank(l) coefficients only, whatever y and B hold past
+    them.  Brute force with numpy on a tiny case."""
+    g = rng(12)
+    T, N, R, L = 10, 7, 6, 3
+    ranks = np.array([2, 6, 0], np.int32)
+    y = g.standard_normal((T, R))
+    B = g.standard_normal((L, N, R))
+    idx = np.array([0, 1, 2, 1, 0, 2, 2, 0, 1, 0], np.int32)
+    out0 = g.standard_normal((T, N))
+    got = oracle.expand(y, B, idx, out0, ranks=ranks, scale=1.5)
+    for t in range(T):
+        l, r = idx[t], ranks[idx[t]]
+        ref = out0[t] + 1.5 * (B[l][:, :r] @ y[t, :r])
+        np.testing.assert_allclose(got[t], ref, rtol=1e-13, atol=1e-13)
+
+
+def test_rank_table_clamps():
+    """A rank below 0 acts as 0 (no term) and one above R as R (the reading of
+    out-of-range ranks: clamped to the stored rows)."""
+    g = rng(13)
+    T, H, R, N, L = 8, 12, 4, 5, 2
+    x = g.standard_normal((T, H))
+    A = g.standard_normal((L, R, H))
+    B = g.standard_normal((L, N, R))
+    idx = np.array([0, 1] * 4, np.int32)
+    y = oracle.shrink(x, A, idx, ranks=np.array([-3, 9], np.int32))
+    assert (y[idx == 0] == 0).all()
+    np.testing.assert_array_equal(y[idx == 1], oracle.shrink(x, A, idx)[idx == 1])
+    out0 = g.standard_normal((T, N))
+    o = oracle.expand(y, B, idx, out0, ranks=np.array([-3, 9], np.int32))
+    np.testing.assert_array_equal(o[idx == 0], out0[idx == 0])
+    np.testing.assert_array_equal(o[idx == 1], oracle.expand(y, B, idx, out0)[idx == 1])
 
 
 def test_inactive_tokens():
