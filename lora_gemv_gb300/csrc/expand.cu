@@ -521,37 +521,47 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
 
 // ---------------------------------------------------------------------------
 // Tensor-core expand (aligned shapes, ranks above 48): one CTA per (plan
-// tile, 128 output columns of one slice).  All of the unit's operands are requested at once:
-// the out block (add_inputs) and the B block before the dependency wait, the
-// y rows after it.  The y rows become scaled hi/lo fp16/bf16 pairs (per-row
-// power-of-two scale, as in the warp kernel) in the 128-byte-swizzled K-major
-// layout; one thread issues D = Y_hi . B^T + Y_lo . B^T as tcgen05.mma
-// (M = 128 token lanes, the tile's 64 tokens plus rows of whatever follows,
-// whose results are never read; N = 128 columns; K = 16 per step) into
-// TMEM; warps 0 and 1 read their token lanes back, scale, add the old out
-// values and store 16-byte groups.
-constexpr int kTcCols = 128;                    // output columns per CTA (N)
+// tile, span of `cpb` consecutive 128-column chunks of one slice).  The tile's
+// y rows are read and turned into scaled hi/lo fp16/bf16 pairs (per-row
+// power-of-two scale, as in the warp kernel) once per CTA, in the
+// 128-byte-swizzled K-major layout; then, per chunk, one thread issues
+// D = Y_hi . B^T + Y_lo . B^T as tcgen05.mma (M = 128 token lanes, the tile's
+// 64 tokens plus rows of whatever follows, whose results are never read;
+// N = 128 columns; K = 16 per step) into TMEM, and warps 0 and 1 read their
+// token lanes back, scale, add the old out values and store 16-byte groups.
+// The chunks are pipelined: the next chunk's out block is requested before
+// the current chunk's MMA (two out buffers), the next B block by warps 2
+// and 3 while warps 0 and 1 run the epilogue (one B buffer, free once the
+// MMA is done).
+constexpr int kTcCols = 128;                    // output columns per chunk (N)
+constexpr int kTcWaves = 3;                     // least waves of CTAs a span size leaves
+constexpr int kTcMaxSpan = 256;                 // chunks per span at most
 constexpr int kTcOutPitch = kTcCols * 2 + 16;   // bytes per staged out row
 
-// Shared memory: [Yh | Yl] per 64-wide rank half, then the B halves, the out
-// block and the fp32 y rows; 1024 bytes of alignment slack in front.
+// Shared memory: [Yh | Yl] per 64-wide rank half, then the B halves and the
+// two out buffers (the second also holds the fp32 y rows before the
+// conversion); 1024 bytes of alignment slack in front.
 __host__ __device__ constexpr int tc_halves(int R) { return R > 64 ? 2 : 1; }
 __host__ __device__ constexpr int tc_ypitch(int R) { return (R + 15) / 16 * 16; }  // floats
+__host__ __device__ constexpr int tc_out1_bytes(int R) {
+    return kTile * kTcOutPitch > kTile * tc_ypitch(R) * 4 ? kTile * kTcOutPitch
+                                                          : kTile * tc_ypitch(R) * 4;
+}
 __host__ __device__ constexpr int tc_expand_smem(int R) {
     return 1024 + tc_halves(R) * (2 * kTile * 128 + kTcCols * 128) + kTile * kTcOutPitch +
-           kTile * tc_ypitch(R) * 4;
+           tc_out1_bytes(R);
 }
 
 template <typename E, bool ADD>
 __global__ void __launch_bounds__(kThreads)
-expand_tc_kernel(const ExpandArgs a) {
+expand_tc_kernel(const ExpandArgs a, int cpb) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
     __shared__ float s_f[kTile];
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int tile = blockIdx.x, chunk = blockIdx.y;
+    const int tile = blockIdx.x, span = blockIdx.y;
 
     // plan header, tile record and token rows in one round trip
     const int4 h0 = __ldg(reinterpret_cast<const int4 *>(a.hdr));
@@ -561,7 +571,7 @@ expand_tc_kernel(const ExpandArgs a) {
                      ? __ldg(a.tile_rows + (int64_t)tile * kTile + threadIdx.x)
                      : -1;
     if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
-        if (tile == 0 && chunk == 0 && threadIdx.x == 0)
+        if (tile == 0 && span == 0 && threadIdx.x == 0)
             atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
         return;
     }
@@ -569,10 +579,11 @@ expand_tc_kernel(const ExpandArgs a) {
     if (threadIdx.x < kTile) s_rows[threadIdx.x] = my_row < a.T ? my_row : -1;
 
     int s = 0;
-    while (s + 1 < a.num_slices && chunk >= a.chunk_begin[s + 1]) ++s;
-    const int n0 = (chunk - a.chunk_begin[s]) * kTcCols;
-    const int ncols = min(kTcCols, a.N[s] - n0);
-    const int64_t col0 = (int64_t)a.off[s] + n0;
+    while (s + 1 < a.num_slices && span >= a.chunk_begin[s + 1]) ++s;
+    const int n_span = (span - a.chunk_begin[s]) * kTcCols * cpb;  // first column in slice s
+    const int span_cols = min(kTcCols * cpb, a.N[s] - n_span);      // > 0, a multiple of 8
+    const int nsub = (span_cols + kTcCols - 1) / kTcCols;
+    const int64_t colbase = (int64_t)a.off[s] + n_span;
     const int l = tl.x, n = tl.z;
     const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, a.R) : 0;
     E *__restrict__ out = static_cast<E *>(a.out);
@@ -582,10 +593,10 @@ expand_tc_kernel(const ExpandArgs a) {
         grid_dep_wait();
         grid_dep_launch();
         if (!ADD)
-            for (int it = threadIdx.x; it < n * (ncols / 8); it += kThreads) {
-                const int i = it / (ncols / 8), c8 = it - i * (ncols / 8);
+            for (int it = threadIdx.x; it < n * (span_cols / 8); it += kThreads) {
+                const int i = it / (span_cols / 8), c8 = it - i * (span_cols / 8);
                 const int row = s_rows[i];
-                if (row >= 0) st_global_v4(out + (int64_t)row * a.ldo + col0 + 8 * c8, make_uint4(0, 0, 0, 0));
+                if (row >= 0) st_global_v4(out + (int64_t)row * a.ldo + colbase + 8 * c8, make_uint4(0, 0, 0, 0));
             }
         return;
     }
@@ -594,28 +605,40 @@ expand_tc_kernel(const ExpandArgs a) {
     unsigned char *sm = smem + ((1024 - (smem_u32(smem) & 1023)) & 1023);
     unsigned char *sY = sm;                                   // [KH][Yh 64 rows | Yl 64 rows] x 128 B
     unsigned char *sB = sY + KH * 2 * kTile * 128;             // [KH][128 rows] x 128 B
-    unsigned char *sO = sB + KH * kTcCols * 128;               // [64][kTcOutPitch]
-    float *sYf = reinterpret_cast<float *>(sO + kTile * kTcOutPitch);  // [64][YP]
+    unsigned char *sO0 = sB + KH * kTcCols * 128;              // [64][kTcOutPitch]
+    unsigned char *sO1 = sO0 + kTile * kTcOutPitch;            // [64][kTcOutPitch], first y
+    float *sYf = reinterpret_cast<float *>(sO1);               // [64][YP] before the conversion
+    const E *Bl = static_cast<const E *>(a.B[s]) + ((int64_t)l * a.N[s] + n_span) * R;
+
+    // chunk j's out block into dst (threads t0, t0 + nt, ...)
+    auto load_out = [&](unsigned char *dst, int j, int t0, int nt) {
+        const int c0 = j * kTcCols, c8n = min(kTcCols, span_cols - c0) / 8;
+        for (int it = t0; it < n * c8n; it += nt) {
+            const int i = it / c8n, c8 = it - i * c8n;
+            const int row = s_rows[i];
+            if (row >= 0)
+                cp_async16(smem_u32(dst + i * kTcOutPitch + 16 * c8),
+                           out + (int64_t)row * a.ldo + colbase + c0 + 8 * c8, 16);
+        }
+    };
+    // chunk j's B block (8 ranks per 16-byte piece, ranks >= rl zero-filled)
+    auto load_b = [&](int j, int t0, int nt) {
+        const int c0 = j * kTcCols, nc = min(kTcCols, span_cols - c0);
+        const E *Bj = Bl + (int64_t)c0 * R;
+        for (int it = t0; it < nc * KS * 2; it += nt) {
+            const int jj = it / (KS * 2), k8 = it - jj * (KS * 2);
+            const int nv = min(8, rl - 8 * k8);
+            cp_async16(smem_u32(sB + (k8 >> 3) * kTcCols * 128 + jj * 128 + (((k8 & 7) ^ (jj & 7)) << 4)),
+                       Bj + (int64_t)jj * R + (nv > 0 ? 8 * k8 : 0), nv > 0 ? 2 * nv : 0);
+        }
+    };
 
     if (warp == 0) tc_alloc(&s_tmem, kTcCols);
     if (threadIdx.x == 0) mbar_init(&s_bar, 1);
 
-    // out block and B block (neither written by the previous kernel)
-    const E *Bl = static_cast<const E *>(a.B[s]) + ((int64_t)l * a.N[s] + n0) * R;
-    if (ADD)
-        for (int it = threadIdx.x; it < n * (ncols / 8); it += kThreads) {
-            const int i = it / (ncols / 8), c8 = it - i * (ncols / 8);
-            const int row = s_rows[i];
-            if (row >= 0)
-                cp_async16(smem_u32(sO + i * kTcOutPitch + 16 * c8),
-                           out + (int64_t)row * a.ldo + col0 + 8 * c8, 16);
-        }
-    for (int it = threadIdx.x; it < ncols * KS * 2; it += kThreads) {  // 8 ranks per chunk
-        const int j = it / (KS * 2), k8 = it - j * (KS * 2);
-        const int nv = min(8, rl - 8 * k8);  // live ranks in this chunk
-        cp_async16(smem_u32(sB + (k8 >> 3) * kTcCols * 128 + j * 128 + (((k8 & 7) ^ (j & 7)) << 4)),
-                   Bl + (int64_t)j * R + (nv > 0 ? 8 * k8 : 0), nv > 0 ? 2 * nv : 0);
-    }
+    // first chunk's out and B blocks (neither written by the previous kernel)
+    if (ADD) load_out(sO0, 0, threadIdx.x, kThreads);
+    load_b(0, threadIdx.x, kThreads);
     cp_async_commit();
 
     // y rows: produced by the previous kernel
@@ -663,56 +686,72 @@ expand_tc_kernel(const ExpandArgs a) {
             if (k8 == 0) s_f[i] = a.scale * exp2i(e);
         }
     }
-    fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // the y rows in sO1 are consumed; sO1 may take chunk 1's out block
     tc_fence_after();
     const uint32_t tmem = s_tmem;
+    const uint32_t idesc = tc_idesc_f16(std::is_same<E, __nv_bfloat16>::value, 128, kTcCols);
 
-    if (threadIdx.x == 0) {
-        const uint32_t idesc = tc_idesc_f16(std::is_same<E, __nv_bfloat16>::value, 128, kTcCols);
-        for (int k = 0; k < KS; ++k) {
-            const int h = k >> 2;
-            const uint32_t yh = smem_u32(sY) + h * 2 * kTile * 128 + 32 * (k & 3);
-            const uint32_t bb = smem_u32(sB) + h * kTcCols * 128 + 32 * (k & 3);
-            tc_mma_f16(tmem, tc_desc_sw128(yh), tc_desc_sw128(bb), idesc, k > 0);
-            tc_mma_f16(tmem, tc_desc_sw128(yh + kTile * 128), tc_desc_sw128(bb), idesc, true);
+    for (int j = 0; j < nsub; ++j) {
+        unsigned char *sOc = (j & 1) ? sO1 : sO0;
+        // next chunk's out block into the other buffer (its epilogue is over)
+        if (ADD && j + 1 < nsub) load_out((j & 1) ? sO0 : sO1, j + 1, threadIdx.x, kThreads);
+        cp_async_commit();
+        cp_async_wait<1>();          // this chunk's out and B blocks are in
+        fence_proxy_async_smem();    // ... and visible to the tensor cores
+        __syncthreads();
+        tc_fence_after();
+        if (threadIdx.x == 0) {
+            for (int k = 0; k < KS; ++k) {
+                const int h = k >> 2;
+                const uint32_t yh = smem_u32(sY) + h * 2 * kTile * 128 + 32 * (k & 3);
+                const uint32_t bb = smem_u32(sB) + h * kTcCols * 128 + 32 * (k & 3);
+                tc_mma_f16(tmem, tc_desc_sw128(yh), tc_desc_sw128(bb), idesc, k > 0);
+                tc_mma_f16(tmem, tc_desc_sw128(yh + kTile * 128), tc_desc_sw128(bb), idesc, true);
+            }
+            tc_commit(&s_bar);
         }
-        tc_commit(&s_bar);
-    }
-    if (!mbar_wait_cta(&s_bar, 0) && threadIdx.x == 0)
-        atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
-    tc_fence_after();
+        const bool timed_out = !mbar_wait_cta(&s_bar, j & 1);
+        if (timed_out && threadIdx.x == 0) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+        tc_fence_after();
 
-    // epilogue: warps 0 and 1 own the tile's 64 token lanes
-    if (warp < 2) {
-        const int i = 32 * warp + lane;
-        const int row = i < n ? s_rows[i] : -1;
-        const float f = s_f[i];
-        const uint32_t tl_addr = tmem + ((uint32_t)(32 * warp) << 16);
-        for (int c0 = 0; c0 < ncols; c0 += 16) {  // warp-uniform
-            float d[16];
-            tc_ld16(tl_addr + c0, d);
-            if (row < 0) continue;
+        if (warp >= 2) {
+            // the MMA has read B: next chunk's B block
+            if (j + 1 < nsub) load_b(j + 1, threadIdx.x - 64, kThreads - 64);
+            cp_async_commit();
+        } else {
+            // epilogue: warps 0 and 1 own the tile's 64 token lanes
+            const int i = 32 * warp + lane;
+            const int row = i < n ? s_rows[i] : -1;
+            const float f = s_f[i];
+            const uint32_t tl_addr = tmem + ((uint32_t)(32 * warp) << 16);
+            const int cj = j * kTcCols, nc = min(kTcCols, span_cols - cj);
+            for (int c0 = 0; c0 < nc; c0 += 32) {  // warp-uniform
+                float d[32];
+                tc_ld32(tl_addr + c0, d);
+                if (row < 0) continue;
 #pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                const int c = c0 + 8 * hlf;
-                if (c >= ncols) break;
-                float v[8];
+                for (int g = 0; g < 4; ++g) {
+                    const int c = c0 + 8 * g;
+                    if (c >= nc) break;
+                    float v[8];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = f * d[8 * hlf + k];
-                if (ADD) {
-                    float o[8];
-                    unpack8<E>(*reinterpret_cast<const uint4 *>(sO + i * kTcOutPitch + 2 * c), o);
+                    for (int k = 0; k < 8; ++k) v[k] = f * d[8 * g + k];
+                    if (ADD) {
+                        float o[8];
+                        unpack8<E>(*reinterpret_cast<const uint4 *>(sOc + i * kTcOutPitch + 2 * c), o);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) v[k] += o[k];
+                        for (int k = 0; k < 8; ++k) v[k] += o[k];
+                    }
+                    st_global_v4(out + (int64_t)row * a.ldo + colbase + cj + c, pack8<E>(v));
                 }
-                st_global_v4(out + (int64_t)row * a.ldo + col0 + c, pack8<E>(v));
             }
         }
+        tc_fence_before();
+        // TMEM and this out buffer are free again; a timed-out wait ends the CTA
+        if (__syncthreads_or(timed_out)) break;
     }
-    tc_fence_before();
-    __syncthreads();
+    cp_async_wait<0>();
     tc_fence_after();
     if (warp == 0) tc_dealloc(tmem, kTcCols);
 }
@@ -725,8 +764,13 @@ cudaError_t configure_one() {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
 }
 
+// Static shared memory of the tensor-core kernels [dtype][add], and the SM's
+// shared memory and per-block reservation, for their residency.
+int g_tc_static[2][2] = {};
+int g_smem_sm = 0, g_smem_reserved = 0;
+
 template <typename E>
-cudaError_t configure_tc() {
+cudaError_t configure_tc(int (&stat)[2]) {
     cudaError_t e = cudaSuccess;
     for (int add = 0; add < 2; ++add) {
         const void *k = add ? reinterpret_cast<const void *>(expand_tc_kernel<E, true>)
@@ -736,13 +780,16 @@ cudaError_t configure_tc() {
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
+        cudaFuncAttributes fa;
+        if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, k);
         if (e != cudaSuccess) return e;
+        stat[add] = (int)fa.sharedSizeBytes;
     }
     return e;
 }
 
 template <typename E>
-cudaError_t launch_tc(const ExpandArgs &a, dim3 grid, cudaStream_t st, bool pdl) {
+cudaError_t launch_tc(const ExpandArgs &a, dim3 grid, int cpb, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
@@ -753,14 +800,14 @@ cudaError_t launch_tc(const ExpandArgs &a, dim3 grid, cudaStream_t st, bool pdl)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (a.add) return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, true>, a);
-    return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, false>, a);
+    if (a.add) return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, true>, a, cpb);
+    return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, false>, a, cpb);
 }
 
 template <typename E>
-cudaError_t configure_dtype() {
+cudaError_t configure_dtype(int (&tc_static)[2]) {
     cudaError_t e;
-    if ((e = configure_tc<E>()) != cudaSuccess) return e;
+    if ((e = configure_tc<E>(tc_static)) != cudaSuccess) return e;
     if ((e = configure_one<E, false, false>()) != cudaSuccess) return e;
     return configure_one<E, true, false>();
 }
@@ -829,9 +876,15 @@ cudaError_t launch_dtype(const ExpandArgs &a, dim3 grid, size_t smem, cudaStream
 }  // namespace
 
 cudaError_t configure_expand_kernels() {
-    cudaError_t e = configure_dtype<__half>();
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&g_smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&g_smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e == cudaSuccess) e = configure_dtype<__half>(g_tc_static[LORA_F16]);
     if (e != cudaSuccess) return e;
-    if ((e = configure_dtype<__nv_bfloat16>()) != cudaSuccess) return e;
+    if ((e = configure_dtype<__nv_bfloat16>(g_tc_static[LORA_BF16])) != cudaSuccess) return e;
     if ((e = query_occ_dtype<__half>(g_warp_occ[LORA_F16])) != cudaSuccess) return e;
     return query_occ_dtype<__nv_bfloat16>(g_warp_occ[LORA_BF16]);
 }
@@ -852,22 +905,43 @@ cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceI
               (reinterpret_cast<uintptr_t>(a.B[s]) & 15) == 0;
     const bool y_vec = (reinterpret_cast<uintptr_t>(a.y) & 15) == 0 && a.ldy % 4 == 0 &&
                        a.y_slice_stride % 4 == 0;
-    // Ranks above 48 (4+ k steps): the tensor-core kernel (one round trip for
-    // a unit's operands; the warp kernel's per-unit B re-reads and register
-    // pressure grow with the rank).  Measured: prefill gate/up r = 64 expand
-    // 363 -> 276 us; at r <= 32 and for decode batches the warp kernel is
-    // faster (its units are lighter than a CTA's load/convert/MMA chain).
-    if (vec && y_vec && (a.R + 15) / 16 >= 4) {
-        // tensor-core path: 128-column chunks per slice
-        a.chunk_begin[0] = 0;
-        for (int s = 0; s < a.num_slices; ++s)
-            a.chunk_begin[s + 1] = a.chunk_begin[s] + (a.N[s] + kTcCols - 1) / kTcCols;
-        for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s];
-        const int chunks = a.chunk_begin[a.num_slices];
-        if (chunks == 0) return cudaSuccess;
-        const dim3 grid(tiles_grid, chunks);
-        return dt == LORA_F16 ? launch_tc<__half>(a, grid, stream, pdl)
-                              : launch_tc<__nv_bfloat16>(a, grid, stream, pdl);
+    // The tensor-core kernel for ranks above 48 (4+ k steps: the warp
+    // kernel's per-unit B re-reads and register pressure grow with the rank),
+    // and for ranks 17-48 when the batch is large enough for spans of two or
+    // more chunks per CTA (the y conversion then pays for itself).  Measured,
+    // prefill gate/up: r = 64 363 -> 155 us, r = 32 150 -> 135 us; at r = 16
+    // and for decode batches the warp kernel is faster (its units are lighter
+    // than a CTA's load/convert/MMA chain).
+    const int ksr = (a.R + 15) / 16;
+    if (vec && y_vec && ksr >= 2) {
+        // spans of cpb 128-column chunks per slice: cpb is the largest power of
+        // two that still leaves at least kTcWaves waves of CTAs
+        const int dyn = tc_expand_smem(a.R);
+        const long long by_smem =
+            g_smem_sm / ((long long)dyn + g_tc_static[dt][a.add ? 1 : 0] + g_smem_reserved);
+        // TMEM: 128 columns per CTA, 512 per SM
+        const long long slots = (long long)dev.sm_count * std::max(1LL, std::min(by_smem, 4LL));
+        auto spans = [&](long long c) {
+            long long n = 0;
+            for (int s = 0; s < a.num_slices; ++s) n += (a.N[s] + kTcCols * c - 1) / (kTcCols * c);
+            return n;
+        };
+        int cpb = 1;
+        while (cpb < kTcMaxSpan && (long long)tiles_grid * spans(2LL * cpb) >= kTcWaves * slots)
+            cpb *= 2;
+        if (ksr >= 4 || cpb >= 2) {
+            a.chunk_begin[0] = 0;
+            for (int s = 0; s < a.num_slices; ++s)
+                a.chunk_begin[s + 1] =
+                    a.chunk_begin[s] + (a.N[s] + kTcCols * cpb - 1) / (kTcCols * cpb);
+            for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s)
+                a.chunk_begin[s + 1] = a.chunk_begin[s];
+            const int nspans = a.chunk_begin[a.num_slices];
+            if (nspans == 0) return cudaSuccess;
+            const dim3 grid(tiles_grid, nspans);
+            return dt == LORA_F16 ? launch_tc<__half>(a, grid, cpb, stream, pdl)
+                                  : launch_tc<__nv_bfloat16>(a, grid, cpb, stream, pdl);
+        }
     }
     if (vec) {
         // 32-column blocks per slice (prefix sums in chunk_begin)

@@ -200,6 +200,31 @@ def test_large_rank_expand(cuda_lib, dtype, add, T, R, ranks, Ns):
     full_check(cuda_lib, c)
 
 
+# Large batches give each tensor-core expand CTA a span of several 128-column
+# chunks (pipelined out / B blocks, y converted once); ranks 17-48 take that
+# kernel too once spans hold two or more chunks.  Ragged last chunks (slices
+# of 2600 and 2504 columns), rank-0 adapters and -1 tokens, both dtypes and
+# add_inputs settings; sampled rows, and every inactive row checked in full.
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("add", [False, True])
+@pytest.mark.parametrize("R,ranks", [(32, [32, 9, 0, 20]), (64, [64, 0, 17, 33, 40]),
+                                     (100, [100, 65, 0, 3])])
+def test_tensor_expand_spans(cuda_lib, dtype, add, R, ranks):
+    c = make_case(4096, 256, R, len(ranks), [2600, 2504], dtype, seed=R + 3 * add, add=add,
+                  ranks=ranks)
+    rows = np.sort(np.random.default_rng(R).choice(c.T, 256, replace=False))
+    y, out_full, _ = gpu_run(cuda_lib, c)
+    y_ref, o_ref = oracle_run(c, rows)
+    assert_close(y[rows], y_ref, c.dtype, f"{c.name} y")
+    assert_close(out_full[rows], o_ref, c.dtype, f"{c.name} out")
+    idx = c.token_idx.numpy()
+    inactive = (idx == -1) | (c.ranks.numpy()[np.maximum(idx, 0)] == 0)
+    if add:
+        assert torch.equal(out_full[inactive].view(torch.int16), c.out[inactive].view(torch.int16))
+    else:
+        assert (out_full[inactive].float() == 0).all()
+
+
 def skewed_idx(T, counts, seed):
     """Token indices giving adapter a exactly counts[a] tokens (the rest -1),
     shuffled: tiles of every size in one batch."""
