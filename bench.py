@@ -629,11 +629,31 @@ def _ref_step(oracle, prepared, rows):
 
 def main_profile(args):
     """A few eager launches of the path on one decode batch, for profilers
-    (e.g. ncu -k regex:expand -s 2 -c 1 python bench.py --profile --T 1024)."""
+    (e.g. ncu -k regex:expand -s 2 -c 1 python bench.py --profile --T 1024),
+    or with --prefill-r R on the prefill gate/up workload at rank R (grouping,
+    shrink, expand_slice per repetition)."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     import lora_gemv_gb300 as lg
     lg.load()
+    if args.prefill_r:
+        r = args.prefill_r
+        c = li.prefill_gateup(r=r)
+        x, A = c.x.to(dev), c.A.to(dev)
+        Bs = [b.to(dev) for b in c.B]
+        out = c.out.to(dev)
+        y = torch.empty(c.T, c.num_slices * r, dtype=torch.float32, device=dev)
+        plan = lg.new_plan(c.T, c.L, dev)
+        ss, sl, slo = c.seg_start.to(dev), c.seg_len.to(dev), c.seg_lora.to(dev)
+        for _ in range(args.profile_reps):
+            lg.lora_group_segments(ss, sl, slo, c.T, c.L, plan)
+            lg.lora_shrink(x, A, y, plan, num_slices=c.num_slices)
+            lg.lora_expand_slice(y, Bs, out, plan, c.slice_offsets, y_slice_stride=r,
+                                 add_inputs=True)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": True, "workload": "prefill_gateup", "r": r, "T": c.T,
+                          "reps": args.profile_reps}))
+        return
     pool, _ = make_pool(dev, 0, 0, only_T=args.T)
     for _ in range(args.profile_reps):
         for batches in pool:
@@ -655,6 +675,8 @@ def main():
                     help="run a few eager steps of one decode batch (for ncu), no timing")
     ap.add_argument("--T", type=int, default=1024, help="batch size for --profile")
     ap.add_argument("--profile-reps", type=int, default=3)
+    ap.add_argument("--prefill-r", type=int, default=0,
+                    help="with --profile: the prefill gate/up workload at this rank instead")
     args = ap.parse_args()
     if args.profile:
         return main_profile(args)
