@@ -151,6 +151,127 @@ def prefill_sgmv(lg, dev, hbm_gbs: float, tc_tflops: float, reps: int = 20):
     return res
 
 
+def pool_op_us(make_set, launch, set_bytes: int, l2_bytes: int, reps: int = 5,
+               max_sets: int = 512):
+    """Average duration of one operator launch: `make_set(i)` builds argument
+    set i on the device; enough sets that together they are >= 4x L2 (so each
+    launch reads from HBM), one launch per set captured in a CUDA graph,
+    replayed `reps` times between two events on the launching stream."""
+    nsets = int(min(max_sets, max(2, -(-4 * l2_bytes // max(set_bytes, 1)))))
+    sets = [make_set(i) for i in range(nsets)]
+    launch(sets[0])  # first use outside the capture (library handles, lazy setup)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for a in sets:
+            launch(a)
+    g.replay()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) * 1e3 / (reps * nsets), nsets
+
+
+def next_rows(lg, dev, hbm_gbs: float):
+    """The widening rows after the decode and prefill paths:
+    - the microbenchmark PR's printed point (SGMV expand, m = 256 as 16
+      requests x 16 tokens, r = 16, n = 2048, 4 adapters sorted by id,
+      add_inputs=False) beside torch.mm of the same shape (f16 [256,16] x
+      [16,2048]), the pages' own two figures given for context;
+    - the single-adapter dense case of that shape (one segment, one adapter)
+      against the same torch.mm;
+    - Llama-3 o_proj / down_proj shapes at decode batches T = 16 and 1024
+      (BGMV, r = 16, 4 adapters, 10 % idx = -1, bf16), shrink and expand.
+    Each figure is the average launch over a rotating pool of argument sets
+    >= 4x L2, against the HBM roofline (algorithmic bytes / measured copy
+    bandwidth)."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    res = {}
+
+    def point(c, tag):
+        T, N, r = c.T, c.B[0].shape[1], c.R
+        U = int(torch.unique(c.seg_lora[c.seg_len > 0]).numel())
+        plan = lg.new_plan(T, c.L, dev)
+        lg.lora_group_segments(c.seg_start.to(dev), c.seg_len.to(dev), c.seg_lora.to(dev), T,
+                               c.L, plan)
+        B0, out0 = c.B[0].to(dev), c.out.to(dev)
+        g = torch.Generator(device="cpu").manual_seed(3)
+        y0 = torch.randn(T, r, generator=g).to(dev)
+        ex_bytes = T * r * 4 + U * N * r * 2 + T * N * 2
+        sb = ex_bytes
+
+        def mk(i):
+            return {"y": y0.clone(), "B": B0.clone(), "out": out0.clone()}
+
+        t_ex, n = pool_op_us(mk, lambda a: lg.lora_expand(a["y"], a["B"], a["out"], plan,
+                                                          add_inputs=False), sb, l2)
+        a16 = y0.to(torch.float16)
+        b16 = B0[0].t().contiguous()
+
+        def mk_mm(i):
+            return {"a": a16.clone(), "b": b16.clone(), "c": torch.empty(T, N, dtype=torch.float16,
+                                                                         device=dev)}
+
+        mm_bytes = T * r * 2 + r * N * 2 + T * N * 2
+        t_mm, _ = pool_op_us(mk_mm, lambda a: torch.mm(a["a"], a["b"], out=a["c"]), mm_bytes, l2)
+        return {"workload": tag, "expand_us": t_ex, "expand_GBps": ex_bytes / t_ex / 1e3,
+                "expand_roofline_frac": ex_bytes / (hbm_gbs * 1e3) / t_ex,
+                "torch_mm_us": t_mm, "torch_mm_roofline_frac": mm_bytes / (hbm_gbs * 1e3) / t_mm,
+                "pool_sets": n}
+
+    c = li.pages_point()
+    r0 = point(c, "SGMV expand m=256 (16x16), r=16, n=2048, 4 adapters sorted, add=0, fp16")
+    r0["pages_figures_us"] = {"sgmv_expand": 5.45, "torch_mm": 4.14,
+                              "note": "the pages' GPU is not named; context only"}
+    res["pages_point"] = r0
+    c1 = li.pages_point()
+    c1.seg_start = torch.zeros(1, dtype=torch.int32)
+    c1.seg_len = torch.full((1,), c1.T, dtype=torch.int32)
+    c1.seg_lora = torch.zeros(1, dtype=torch.int32)
+    res["single_adapter"] = point(c1, "one adapter, one 256-token segment, r=16, n=2048, "
+                                      "add=0, fp16 (the dense special case)")
+
+    shapes = {}
+    for name in li.MODEL_SHAPES:
+        per_T = {}
+        for T in (16, 1024):
+            c = li.model_shape(name, T)
+            Hm, N, r = c.A.shape[2], c.B[0].shape[1], c.R
+            idx = c.token_idx
+            act = idx >= 0
+            Ta = int(act.sum())
+            U = int(torch.unique(idx[act]).numel())
+            sh_bytes = Ta * Hm * 2 + U * r * Hm * 2 + T * r * 4
+            ex_bytes = Ta * r * 4 + U * N * r * 2 + 2 * Ta * N * 2
+            A0, B0 = c.A.to(dev), c.B[0].to(dev)
+            idx_d = idx.to(dev)
+
+            def mk(i, c=c, A0=A0, B0=B0, idx_d=idx_d, T=T):
+                plan = lg.new_plan(T, c.L, dev)
+                lg.lora_group_tokens(idx_d, c.L, plan)
+                return {"x": c.x.to(dev), "A": A0, "B": B0, "out": c.out.to(dev),
+                        "y": torch.zeros(T, r, dtype=torch.float32, device=dev), "plan": plan}
+
+            set_bytes = T * Hm * 2 + T * N * 2 + T * r * 4
+            t_sh, n = pool_op_us(mk, lambda a: lg.lora_shrink(a["x"], a["A"], a["y"], a["plan"]),
+                                 set_bytes, l2)
+            t_ex, _ = pool_op_us(mk, lambda a: lg.lora_expand(a["y"], a["B"], a["out"], a["plan"],
+                                                              add_inputs=True), set_bytes, l2)
+            per_T[str(T)] = {"H": Hm, "N": N, "shrink_us": t_sh,
+                             "shrink_roofline_frac": sh_bytes / (hbm_gbs * 1e3) / t_sh,
+                             "expand_us": t_ex,
+                             "expand_roofline_frac": ex_bytes / (hbm_gbs * 1e3) / t_ex,
+                             "pool_sets": n}
+            torch.cuda.synchronize()
+        shapes[name] = per_T
+    res["model_shapes"] = shapes
+    return res
+
+
 def algorithmic_fused(idx: torch.Tensor):
     """Fused shrink + expand_slice: x, live A rows, y written once, live B
     rows, out read and written (y is not re-read from HBM)."""
@@ -566,6 +687,7 @@ def main_ours(args):
         "clocks": clk,
         "per_T": per_T,
         "prefill_sgmv": prefill_sgmv(lg, dev, hbm, tf),
+        "next_rows": next_rows(lg, dev, hbm),
         "wall_s_timed": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -21,6 +21,13 @@ vLLM LoRA microbenchmark PR (#11579) sweeps and the Llama-3 layer shapes its
 * ``sweep``          H in {1024,2048,2049,4096,8192,16384}, batch in
                      {16..8192}, seq-len 1 (BGMV, sorted ids) or 8 (SGMV,
                      one 8-token segment per request, sorted), r=16, L=4, fp16
+* ``pages_point``    the single kernel timing the microbenchmark PR prints:
+                     SGMV expand, m = 256 tokens (16 requests x 16 tokens),
+                     r = 16, n = 2048, 4 adapters, requests sorted by adapter
+                     id, add_inputs=False, fp16
+* ``model_shape``    Llama-3 projections besides q/k/v and gate/up (o_proj and
+                     down_proj, H and N as the layer's input and output
+                     widths), decode batches as ``decode_qkv``, one slice
 
 Weights are N(0, 0.02^2) (std 0.02), activations and the base output N(0, 1).
 """
@@ -41,6 +48,13 @@ GATEUP_N = 14336
 SWEEP_H = (1024, 2048, 2049, 4096, 8192, 16384)
 SWEEP_BATCH = (16, 128, 256, 512, 1024, 2048, 8192)
 MIXED_RANKS = (2, 8, 16, 20, 64, 128)
+# (H, N) of the Llama-3 o_proj / down_proj layers (input width, output width)
+MODEL_SHAPES = {
+    "llama3_8b_o_proj": (4096, 4096),
+    "llama3_8b_down_proj": (14336, 4096),
+    "llama3_70b_o_proj": (8192, 8192),
+    "llama3_70b_down_proj": (28672, 8192),
+}
 
 
 @dataclass
@@ -243,4 +257,29 @@ def sweep(H: int, batch: int, seq_len: int, seed: Optional[int] = None, r: int =
         case.seg_start = torch.arange(batch, dtype=i32) * seq_len
         case.seg_len = torch.full((batch,), seq_len, dtype=i32)
         case.seg_lora = req_ids.clone()
+    return case
+
+
+def pages_point(seed: Optional[int] = None, dtype=torch.float16) -> Case:
+    """The printed microbenchmark point: 16 requests x 16 tokens (m = 256),
+    r = 16, n = 2048, 4 adapters, sorted request ids, add_inputs=False.  The
+    shrink side (not part of the printed point) uses H = n."""
+    case = sweep(H=2048, batch=16, seq_len=16, seed=SEED_BASE + 6 if seed is None else seed,
+                 dtype=dtype)
+    case.name = "pages_point_m256_r16_n2048"
+    case.add = False
+    case.meta = {"m": 256, "batch": 16, "seq_len": 16, "n": 2048}
+    return case
+
+
+def model_shape(name: str, T: int, seed: Optional[int] = None, r: int = 16, L: int = 4,
+                dtype=torch.bfloat16) -> Case:
+    """A decode batch (as ``decode_qkv``: 10 % of tokens idx=-1, the rest
+    uniform over L adapters) for one Llama-3 o_proj / down_proj shape."""
+    H, N = MODEL_SHAPES[name]
+    if seed is None:
+        seed = SEED_BASE + 7 + 100 * list(MODEL_SHAPES).index(name) + T
+    case = decode_qkv(T, seed=seed, H=H, r=r, L=L, slices=(N,), dtype=dtype)
+    case.name = f"{name}_T{T}"
+    case.meta = {"T": T, "H": H, "N": N}
     return case

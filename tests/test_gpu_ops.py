@@ -66,6 +66,27 @@ def test_sweep_points(cuda_lib, H, batch, sl):
     full_check(cuda_lib, c, rows)
 
 
+def test_pages_point(cuda_lib):
+    """The microbenchmark PR's printed SGMV expand point (m = 256 as 16 x 16,
+    r = 16, n = 2048, 4 sorted adapters, add_inputs=False), and the same
+    shape with one adapter over one segment (the dense special case)."""
+    c = li.pages_point()
+    full_check(cuda_lib, c)
+    c.seg_start = torch.zeros(1, dtype=torch.int32)
+    c.seg_len = torch.full((1,), c.T, dtype=torch.int32)
+    c.seg_lora = torch.zeros(1, dtype=torch.int32)
+    full_check(cuda_lib, c)
+
+
+@pytest.mark.parametrize("name", list(li.MODEL_SHAPES))
+@pytest.mark.parametrize("T", [200, 1024])
+def test_model_shapes(cuda_lib, name, T):
+    """Llama-3 o_proj / down_proj shapes (H up to 28672) at decode batches."""
+    c = li.model_shape(name, T)
+    rows = None if T <= 200 else np.sort(np.random.default_rng(T).choice(c.T, 192, replace=False))
+    full_check(cuda_lib, c, rows)
+
+
 def test_sweep_largest_point_sampled(cuda_lib):
     """batch 8192 x seq-len 8 = 65536 tokens at H = N = 16384: sampled rows."""
     c = li.sweep(H=16384, batch=8192, seq_len=8)

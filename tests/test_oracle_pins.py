@@ -376,3 +376,10 @@ def test_workload_recipes():
     s = li.sweep(H=2049, batch=16, seq_len=8)
     assert s.T == 128 and s.seg_len.tolist() == [8] * 16
     assert (s.seg_lora.diff() >= 0).all()
+    pp = li.pages_point()
+    assert pp.T == 256 and pp.seg_len.tolist() == [16] * 16 and not pp.add
+    assert pp.B[0].shape == (4, 2048, 16) and (pp.seg_lora.diff() >= 0).all()
+    for name, (Hm, N) in li.MODEL_SHAPES.items():
+        c = li.model_shape(name, 100)
+        assert c.x.shape == (100, Hm) and c.B[0].shape == (4, N, 16) and c.out.shape == (100, N)
+        assert (c.token_idx == -1).sum().item() == 10
