@@ -520,7 +520,8 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core expand (aligned shapes, ranks above 48): one CTA per (plan
+// Tensor-core expand (aligned shapes; ranks above 48, or 17-48 on batches
+// large enough for spans of two or more chunks): one CTA per (plan
 // tile, span of `cpb` consecutive 128-column chunks of one slice).  The tile's
 // y rows are read and turned into scaled hi/lo fp16/bf16 pairs (per-row
 // power-of-two scale, as in the warp kernel) once per CTA, in the
