@@ -680,7 +680,8 @@ def main_ours(args):
         "step_time_share": {k: sum(v[0]) / (sum(sh_ms) + sum(ex_ms) + sum(gr_ms))
                             for k, v in kern.items()},
         "path_roofline_frac": path_frac,
-        "gpu_launches": K * nb * (2 if FUSED_STEP else 3),
+        # per batch: grouping, then shrink and expand_slice (chained or not)
+        "gpu_launches": K * nb * 3,
         "e2e": {"value": e2e_v, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "wall_tokens_per_s": e2e_wall,
                 "how": "public Python API per call (no graph), pinned host buffers"},
