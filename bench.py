@@ -375,7 +375,7 @@ FUSED_STEP = True  # shrink + expand_slice through the chained (PDL) entry point
 # from an ncu capture of `bench.py --profile --T 1024` (summaries under
 # profiles/); None until a capture of the current kernel exists.
 NCU_TRAFFIC = {
-    "shrink": {"bytes": 9176576, "source": "ncu --set full, dram__bytes_read.sum 9.177 MB + "
+    "shrink": {"bytes": 9177344, "source": "ncu --set full, dram__bytes_read.sum 9.177 MB + "
                "dram__bytes_write.sum 0 (y stays in L2), T=1024 launch (tcgen05 variant)"},
     "expand_slice": {"bytes": 12329984, "source": "ncu --set full, dram__bytes_read.sum 12.33 MB + "
                      "dram__bytes_write.sum 0 (out written back after the launch), T=1024 launch"},
