@@ -1,0 +1,35 @@
+"""The benchmark's algorithmic work formulas (the numerators of every
+roofline fraction), checked on a hand-worked batch."""
+import torch
+
+
+def test_decode_algorithmic_work_hand_example():
+    import bench
+    # 4 tokens: adapters 0, -1, 1, 0 -> 3 active tokens, 2 adapters used.
+    # q/k/v workload: H = 4096, S = 3 slices of rank 16, N_tot = 6144, 2-byte elements.
+    idx = torch.tensor([0, -1, 1, 0], dtype=torch.int32)
+    sh_bytes, sh_flops, ex_bytes, ex_flops = bench.algorithmic(idx)
+    # shrink: x rows of active tokens + live A rows of used adapters + y written (fp32)
+    assert sh_bytes == 3 * 4096 * 2 + 2 * 48 * 4096 * 2 + 4 * 48 * 4
+    assert sh_flops == 2 * 4096 * 48 * 3
+    # expand_slice: y rows read + live B rows of used adapters + out read and written
+    assert ex_bytes == 3 * 48 * 4 + 2 * 6144 * 16 * 2 + 2 * 3 * 6144 * 2
+    assert ex_flops == 2 * 6144 * 16 * 3
+
+
+def test_decode_algorithmic_work_all_inactive():
+    import bench
+    idx = torch.full((8,), -1, dtype=torch.int32)
+    sh_bytes, sh_flops, ex_bytes, ex_flops = bench.algorithmic(idx)
+    assert sh_flops == 0 and ex_flops == 0 and ex_bytes == 0
+    assert sh_bytes == 8 * 48 * 4  # y rows are still written (zeros)
+
+
+def test_chained_work_counts_y_once():
+    import bench
+    idx = torch.tensor([0, -1, 1, 0], dtype=torch.int32)
+    sh_bytes, sh_flops, ex_bytes, ex_flops = bench.algorithmic(idx)
+    fu_bytes, fu_flops = bench.algorithmic_fused(idx)
+    # the expand's y re-read (3 active tokens x 48 fp32) is not counted again
+    assert fu_bytes == sh_bytes + ex_bytes - 3 * 48 * 4
+    assert fu_flops == sh_flops + ex_flops
