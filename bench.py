@@ -95,6 +95,28 @@ def algorithmic(idx: torch.Tensor):
     return sh_bytes, sh_flops, ex_bytes, ex_flops
 
 
+def segment_work(T: int, Hm: int, N: int, r: int, S: int, U: int):
+    """Algorithmic bytes / flops of an SGMV batch in which every token is
+    active (fp16/bf16 operands, fp32 y, add_inputs=True): shrink = x + live
+    A rows + y written; expand_slice = y read + live B rows + out read and
+    written, over S slices of N columns each."""
+    sh_b = T * Hm * E + U * S * r * Hm * E + T * S * r * 4
+    sh_f = 2 * T * Hm * S * r
+    ex_b = T * S * r * 4 + U * S * N * r * E + 2 * T * S * N * E
+    ex_f = 2 * T * S * N * r
+    return sh_b, sh_f, ex_b, ex_f
+
+
+def single_slice_work(Ta: int, T: int, U: int, Hm: int, N: int, r: int, add: bool):
+    """Algorithmic bytes of one shrink and one single-slice expand: shrink =
+    x rows of the Ta active tokens + live A rows of the U used adapters + y
+    written for all T tokens; expand = y rows read + live B rows + out read
+    and written (add_inputs) or written for every token (without)."""
+    sh_b = Ta * Hm * E + U * r * Hm * E + T * r * 4
+    ex_b = Ta * r * 4 + U * N * r * E + (2 * Ta * N * E if add else T * N * E)
+    return sh_b, ex_b
+
+
 def prefill_sgmv(lg, dev, hbm_gbs: float, tc_tflops: float, reps: int = 20):
     """The prefill SGMV gate/up workload (8 segments, log-uniform lengths in
     [8, 2048], adapters A A A B C C D D, H = 4096, gate/up slices of 14336,
@@ -136,10 +158,7 @@ def prefill_sgmv(lg, dev, hbm_gbs: float, tc_tflops: float, reps: int = 20):
         t_sh = timed(lambda i: lg.lora_shrink(xs[i], A, ys[i], plan, num_slices=S))
         t_ex = timed(lambda i: lg.lora_expand_slice(ys[i], Bs, out, plan, c.slice_offsets,
                                                     y_slice_stride=r, add_inputs=True))
-        sh_b = T * H * 2 + U * S * r * H * 2 + T * S * r * 4
-        sh_f = 2 * T * H * S * r
-        ex_b = T * S * r * 4 + U * S * N * r * 2 + 2 * T * S * N * 2
-        ex_f = 2 * T * S * N * r
+        sh_b, sh_f, ex_b, ex_f = segment_work(T, H, N, r, S, U)
         out_r = {"T": T}
         for name, t, b, f in (("shrink", t_sh, sh_b, sh_f), ("expand_slice", t_ex, ex_b, ex_f)):
             t_mem, t_tc = b / (hbm_gbs * 1e9), f / (tc_tflops * 1e12)
@@ -201,7 +220,7 @@ def next_rows(lg, dev, hbm_gbs: float):
         B0, out0 = c.B[0].to(dev), c.out.to(dev)
         g = torch.Generator(device="cpu").manual_seed(3)
         y0 = torch.randn(T, r, generator=g).to(dev)
-        ex_bytes = T * r * 4 + U * N * r * 2 + T * N * 2
+        _, ex_bytes = single_slice_work(T, T, U, c.A.shape[2], N, r, add=False)
         sb = ex_bytes
 
         def mk(i):
@@ -245,8 +264,7 @@ def next_rows(lg, dev, hbm_gbs: float):
             act = idx >= 0
             Ta = int(act.sum())
             U = int(torch.unique(idx[act]).numel())
-            sh_bytes = Ta * Hm * 2 + U * r * Hm * 2 + T * r * 4
-            ex_bytes = Ta * r * 4 + U * N * r * 2 + 2 * Ta * N * 2
+            sh_bytes, ex_bytes = single_slice_work(Ta, T, U, Hm, N, r, add=True)
             A0, B0 = c.A.to(dev), c.B[0].to(dev)
             idx_d = idx.to(dev)
 
