@@ -255,6 +255,58 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
                                        lora_stream_t stream);
 
 /*
+ * lora_shrink_expand_slice for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point: it is a convenience of
+ * this library, not a step of the method.
+ *
+ * Who needs it: a caller that receives its input and output buffers from a
+ * host that owns all device memory (a plugin's enqueue step in an inference
+ * engine, for example) has no way to obtain the plan buffer the other
+ * entry points require, and a latency-critical serving loop may not accept
+ * cudaMalloc, which can synchronise the device.  This call needs only the
+ * inputs and outputs: it groups token_idx (as lora_group_tokens) into a plan
+ * kept in a fixed device array owned by the library, then runs
+ * lora_shrink_expand_slice on that plan.  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *
+ * Arguments: those of lora_shrink_expand_slice, with token_idx [T] (device,
+ * int32, the BGMV adapter index of each token; -1 = no LoRA; values outside
+ * [-1, L) count as bad ids and act as -1) in place of the plan.  Results are
+ * those of lora_group_tokens followed by lora_shrink_expand_slice.
+ *
+ * Limits: T <= LORA_NOALLOC_MAX_TOKENS (4096); larger T returns
+ * LORA_ERR_UNSUPPORTED before anything is enqueued.  The array is
+ * LORA_NOALLOC_PLAN_BYTES (1.25 MiB) of device memory on every GPU that
+ * loads the library, held until the process exits.
+ *
+ * Set-up: the first call made with a given device current looks up the
+ * array's device address on that device (cudaGetSymbolAddress); make that
+ * first call before any stream capture.
+ *
+ * Shared state: every call on a device uses the same array and leaves its
+ * plan there (nothing in it has to start at zero: each call's grouping
+ * rewrites every word its operators read).  Calls whose work overlaps on the
+ * GPU (other streams, other threads, unordered graph branches) race on the
+ * array and may produce wrong results; order them, e.g. on one stream.  The
+ * plan's error words are not readable through this entry point.
+ * Errors: those of lora_group_tokens and lora_shrink_expand_slice, plus
+ * LORA_ERR_UNSUPPORTED for T > LORA_NOALLOC_MAX_TOKENS and LORA_ERR_CUDA if
+ * the array's address cannot be obtained.
+ */
+#define LORA_NOALLOC_MAX_TOKENS 4096
+#define LORA_NOALLOC_PLAN_BYTES (1280 * 1024)
+lora_status_t lora_shrink_expand_slice_noalloc(lora_dtype_t dtype, const int32_t *token_idx,
+                                               const void *x, int64_t ldx, int32_t T, int32_t H,
+                                               const void *A, int32_t L, int32_t R,
+                                               const int32_t *ranks, float *y, int64_t ldy,
+                                               int32_t num_slices, const void *const *B_slices,
+                                               const int32_t *slice_N,
+                                               const int32_t *slice_offset, void *out,
+                                               int64_t ldo, float scale_shrink,
+                                               float scale_expand, int add_inputs,
+                                               lora_stream_t stream);
+
+/*
  * Reads the plan's device-side error words.  SYNCHRONISES `stream` (a
  * device-to-host copy); for tests and debugging, not for the hot path.
  * *bad_ids <- LORA_HDR_BAD_IDS, *err_flags <- LORA_HDR_ERR (either may be NULL).

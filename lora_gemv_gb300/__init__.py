@@ -14,6 +14,8 @@ Functions carry the C names:
 * ``lora_expand(y, B, out, plan, ...)``
 * ``lora_expand_slice(y, B_slices, out, plan, slice_offsets, ...)``
 * ``lora_shrink_expand_slice(x, A, y, B_slices, out, plan, slice_offsets, ...)``
+* ``lora_shrink_expand_slice_noalloc(token_idx, x, A, y, B_slices, out, slice_offsets, ...)``
+  (the decode pair with the library's own plan array: no plan argument)
 * ``lora_get_error(plan)``
 """
 from __future__ import annotations
@@ -38,8 +40,9 @@ PLAN_MAGIC = 0x4C6F5241
 
 EXPORTS = ("lora_plan_layout", "lora_workspace_size", "lora_group_tokens",
            "lora_group_segments", "lora_shrink", "lora_expand", "lora_expand_slice",
-           "lora_shrink_expand_slice", "lora_get_error", "lora_status_string",
-           "lora_last_error_detail", "lora_version")
+           "lora_shrink_expand_slice", "lora_shrink_expand_slice_noalloc", "lora_get_error",
+           "lora_status_string", "lora_last_error_detail", "lora_version")
+NOALLOC_MAX_TOKENS = 4096
 
 _lib = None
 
@@ -90,6 +93,11 @@ def load():
                                              ctypes.POINTER(i32), vp, i64, vp, f32, f32,
                                              ctypes.c_int, vp]
     lib.lora_shrink_expand_slice.restype = st
+    lib.lora_shrink_expand_slice_noalloc.argtypes = [st, vp, vp, i64, i32, i32, vp, i32, i32, vp,
+                                                     vp, i64, i32, ctypes.POINTER(vp),
+                                                     ctypes.POINTER(i32), ctypes.POINTER(i32), vp,
+                                                     i64, f32, f32, ctypes.c_int, vp]
+    lib.lora_shrink_expand_slice_noalloc.restype = st
     lib.lora_get_error.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), vp]
     lib.lora_get_error.restype = st
     lib.lora_status_string.argtypes = [st]
@@ -308,3 +316,41 @@ def lora_shrink_expand_slice(x: torch.Tensor, A: torch.Tensor, y: torch.Tensor,
         _dev(y, "y"), _rows(y, "y"), S, ptrs, Ns, offs, _dev(out, "out"), _rows(out, "out"),
         _dev(plan, "plan"), float(scale_shrink), float(scale_expand), int(bool(add_inputs)),
         _stream(x)))
+
+
+def lora_shrink_expand_slice_noalloc(token_idx: torch.Tensor, x: torch.Tensor, A: torch.Tensor,
+                                     y: torch.Tensor, B_slices: Sequence[torch.Tensor],
+                                     out: torch.Tensor, slice_offsets: Sequence[int], *,
+                                     ranks: Optional[torch.Tensor] = None,
+                                     scale_shrink: float = 1.0, scale_expand: float = 1.0,
+                                     add_inputs: bool = True) -> None:
+    """As lora_group_tokens followed by lora_shrink_expand_slice, with the plan
+    kept in the library's own device array (no plan buffer; T <= 4096; calls
+    on one device must not overlap on the GPU)."""
+    T, H = x.shape
+    S = len(B_slices)
+    if A.dim() != 3 or not A.is_contiguous() or A.shape[2] != H or A.dtype != x.dtype:
+        raise ValueError("A must be a contiguous [L, S*R, H] tensor of x's dtype")
+    L, SR, _ = A.shape
+    if SR % S or S != len(slice_offsets):
+        raise ValueError("A rows must be S*R with one offset per slice")
+    if token_idx.numel() != T:
+        raise ValueError("token_idx must hold one index per row of x")
+    R = SR // S
+    for b in B_slices:
+        if b.dim() != 3 or not b.is_contiguous() or b.shape[0] != L or b.shape[2] != R \
+                or b.dtype != out.dtype or out.dtype != x.dtype:
+            raise ValueError("every B_s must be a contiguous [L, N_s, R] tensor of x's dtype")
+    if y.dtype != torch.float32 or y.shape[0] != T or y.shape[1] < SR:
+        raise ValueError("y must be fp32 [T, >= S*R]")
+    if out.shape[0] != T or any(int(o) + b.shape[1] > out.shape[1]
+                                for o, b in zip(slice_offsets, B_slices)):
+        raise ValueError("a slice ends past out's columns")
+    ptrs = (ctypes.c_void_p * S)(*[_dev(b, "B_s") for b in B_slices])
+    Ns = (ctypes.c_int32 * S)(*[b.shape[1] for b in B_slices])
+    offs = (ctypes.c_int32 * S)(*[int(o) for o in slice_offsets])
+    _check(load().lora_shrink_expand_slice_noalloc(
+        _dtype(x), _i32(token_idx, "token_idx"), _dev(x, "x"), _rows(x, "x"), T, H, _dev(A, "A"),
+        L, R, _i32(ranks, "ranks"), _dev(y, "y"), _rows(y, "y"), S, ptrs, Ns, offs,
+        _dev(out, "out"), _rows(out, "out"), float(scale_shrink), float(scale_expand),
+        int(bool(add_inputs)), _stream(x)))

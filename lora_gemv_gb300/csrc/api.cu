@@ -160,7 +160,10 @@ lora_status_t lora_group_segments(const int32_t *seg_start, const int32_t *seg_l
 
 }  // extern "C"
 
-namespace {
+namespace lora {
+
+// Reports a failure status with a message (the thread's lora_last_error_detail).
+lora_status_t report(lora_status_t s, const char *msg) { return fail(s, "%s", msg); }
 
 lora_status_t check_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_t T, int32_t H,
                            const void *A, int32_t L, int32_t R, int32_t num_slices,
@@ -222,7 +225,10 @@ lora_status_t check_expand(lora_dtype_t dtype, const float *y, int64_t ldy, int3
     return lora_plan_layout(T, L, &lay);
 }
 
-}  // namespace
+}  // namespace lora
+
+using lora::check_expand;
+using lora::check_shrink;
 
 extern "C" {
 

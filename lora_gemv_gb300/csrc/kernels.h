@@ -77,4 +77,17 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
 cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a, const DeviceInfo &dev,
                           cudaStream_t stream, bool pdl = false);
 
+// Host-side argument checks of the C ABI (api.cu): LORA_OK or the status the
+// operator would return, with lora_last_error_detail() set.
+lora_status_t check_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_t T, int32_t H,
+                           const void *A, int32_t L, int32_t R, int32_t num_slices,
+                           const int32_t *ranks, const float *y, int64_t ldy, const void *plan);
+lora_status_t check_expand(lora_dtype_t dtype, const float *y, int64_t ldy, int32_t T,
+                           int32_t num_slices, const void *const *B_slices,
+                           const int32_t *slice_N, const int32_t *slice_offset,
+                           int32_t y_slice_stride, int32_t L, int32_t R, const int32_t *ranks,
+                           const void *out, int64_t ldo, const void *plan);
+// Returns `s` and records `msg` as this thread's lora_last_error_detail().
+lora_status_t report(lora_status_t s, const char *msg);
+
 }  // namespace lora
