@@ -372,17 +372,17 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     // units (tile, row part, column block), tile-major; ranges use the host's
     // tile bound so the first tile record loads together with the header
     const int per_tile = kParts * ncb;
-    const int U_grid = tiles_grid * per_tile;
-    const int per = (U_grid + nwarps - 1) / nwarps;
-    const int u_begin = gwarp * per;
+    const long long U_grid = (long long)tiles_grid * per_tile;
+    long long per = (U_grid + nwarps - 1) / nwarps;
+    long long u_begin = gwarp * per;
     const int4 h0 = __ldg(reinterpret_cast<const int4 *>(a.hdr));
     const int4 h1 = __ldg(reinterpret_cast<const int4 *>(a.hdr) + 1);
-    int t = u_begin / per_tile;
+    int t = (int)(u_begin / per_tile);
     int4 tl = t < a.max_tiles ? __ldg(a.tiles + t) : make_int4(-1, 0, 0, 0);
     // position of the current unit, and its token rows (the plan's per-tile
     // row lists, -1 padded), read in the same round trip as the header
-    int part = (u_begin - t * per_tile) / ncb;
-    int cbi = u_begin - t * per_tile - part * ncb;
+    int part = (int)(u_begin - (long long)t * per_tile) / ncb;
+    int cbi = (int)(u_begin - (long long)t * per_tile) - part * ncb;
     auto load_rows = [&](int tt, int pt, int (&r)[MB][2]) {
 #pragma unroll
         for (int mm = 0; mm < MB; ++mm)
@@ -399,7 +399,20 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
         return;
     }
     const int n_tiles = min(h1.z, a.max_tiles);
-    const int u_end = min(n_tiles * per_tile, u_begin + per);
+    if (n_tiles > tiles_grid) {
+        // More tiles than the host's bound (a segment table not sorted by
+        // adapter): spread all of them over the warps instead.
+        per = ((long long)n_tiles * per_tile + nwarps - 1) / nwarps;
+        u_begin = gwarp * per;
+        t = (int)(u_begin / per_tile);
+        part = (int)(u_begin - (long long)t * per_tile) / ncb;
+        cbi = (int)(u_begin - (long long)t * per_tile) - part * ncb;
+        if (t < n_tiles) {
+            tl = __ldg(a.tiles + t);
+            load_rows(t, part, rows);
+        }
+    }
+    const long long u_end = min((long long)n_tiles * per_tile, u_begin + per);
     if (u_begin >= u_end) return;
     E *__restrict__ out = static_cast<E *>(a.out);
 
@@ -431,7 +444,7 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     grid_dep_wait();
     grid_dep_launch();
 
-    for (int u = u_begin; u < u_end; ++u) {
+    for (long long u = u_begin; u < u_end; ++u) {
         // ---- the next unit: position, and its loads issued now
         int nt = t, npart = part, ncbi = cbi + 1;
         if (ncbi == ncb) {
@@ -562,12 +575,13 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
     __shared__ uint64_t s_bar;
     __shared__ uint32_t s_tmem;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int tile = blockIdx.x, span = blockIdx.y;
+    const int span = blockIdx.y;
 
-    // plan header, tile record and token rows in one round trip
+    // plan header, first tile record and its token rows in one round trip
     const int4 h0 = __ldg(reinterpret_cast<const int4 *>(a.hdr));
     const int4 h1 = __ldg(reinterpret_cast<const int4 *>(a.hdr) + 1);
-    const int4 tl = tile < a.max_tiles ? __ldg(a.tiles + tile) : make_int4(-1, 0, 0, 0);
+    int tile = blockIdx.x;
+    int4 tl = tile < a.max_tiles ? __ldg(a.tiles + tile) : make_int4(-1, 0, 0, 0);
     int my_row = threadIdx.x < kTile && tile < a.max_tiles
                      ? __ldg(a.tile_rows + (int64_t)tile * kTile + threadIdx.x)
                      : -1;
@@ -576,8 +590,9 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
             atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
         return;
     }
-    if (tile >= min(h1.z, a.max_tiles)) return;
-    if (threadIdx.x < kTile) s_rows[threadIdx.x] = my_row < a.T ? my_row : -1;
+    // The grid covers the host's tile bound; a plan with more tiles (segment
+    // tables not sorted by adapter) is covered by CTAs taking tile + gridDim.x.
+    const int n_tiles = min(h1.z, a.max_tiles);
 
     int s = 0;
     while (s + 1 < a.num_slices && span >= a.chunk_begin[s + 1]) ++s;
@@ -585,176 +600,210 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
     const int span_cols = min(kTcCols * cpb, a.N[s] - n_span);      // > 0, a multiple of 8
     const int nsub = (span_cols + kTcCols - 1) / kTcCols;
     const int64_t colbase = (int64_t)a.off[s] + n_span;
-    const int l = tl.x, n = tl.z;
-    const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, a.R) : 0;
     E *__restrict__ out = static_cast<E *>(a.out);
-    __syncthreads();
-
-    if (rl == 0) {  // adapter -1 or rank 0: untouched with add_inputs, zeros without
-        grid_dep_wait();
-        grid_dep_launch();
-        if (!ADD)
-            for (int it = threadIdx.x; it < n * (span_cols / 8); it += kThreads) {
-                const int i = it / (span_cols / 8), c8 = it - i * (span_cols / 8);
-                const int row = s_rows[i];
-                if (row >= 0) st_global_v4(out + (int64_t)row * a.ldo + colbase + 8 * c8, make_uint4(0, 0, 0, 0));
-            }
-        return;
-    }
-
-    const int R = a.R, KS = (rl + 15) / 16, KH = tc_halves(R), YP = tc_ypitch(R);
+    const int R = a.R, KH = tc_halves(R), YP = tc_ypitch(R);
     unsigned char *sm = smem + ((1024 - (smem_u32(smem) & 1023)) & 1023);
     unsigned char *sY = sm;                                   // [KH][Yh 64 rows | Yl 64 rows] x 128 B
     unsigned char *sB = sY + KH * 2 * kTile * 128;             // [KH][128 rows] x 128 B
     unsigned char *sO0 = sB + KH * kTcCols * 128;              // [64][kTcOutPitch]
     unsigned char *sO1 = sO0 + kTile * kTcOutPitch;            // [64][kTcOutPitch], first y
     float *sYf = reinterpret_cast<float *>(sO1);               // [64][YP] before the conversion
-    const E *Bl = static_cast<const E *>(a.B[s]) + ((int64_t)l * a.N[s] + n_span) * R;
-
-    // chunk j's out block into dst (threads t0, t0 + nt, ...)
-    auto load_out = [&](unsigned char *dst, int j, int t0, int nt) {
-        const int c0 = j * kTcCols, c8n = min(kTcCols, span_cols - c0) / 8;
-        for (int it = t0; it < n * c8n; it += nt) {
-            const int i = it / c8n, c8 = it - i * c8n;
-            const int row = s_rows[i];
-            if (row >= 0)
-                cp_async16(smem_u32(dst + i * kTcOutPitch + 16 * c8),
-                           out + (int64_t)row * a.ldo + colbase + c0 + 8 * c8, 16);
-        }
-    };
-    // chunk j's B block (8 ranks per 16-byte piece, ranks >= rl zero-filled)
-    auto load_b = [&](int j, int t0, int nt) {
-        const int c0 = j * kTcCols, nc = min(kTcCols, span_cols - c0);
-        const E *Bj = Bl + (int64_t)c0 * R;
-        for (int it = t0; it < nc * KS * 2; it += nt) {
-            const int jj = it / (KS * 2), k8 = it - jj * (KS * 2);
-            const int nv = min(8, rl - 8 * k8);
-            cp_async16(smem_u32(sB + (k8 >> 3) * kTcCols * 128 + jj * 128 + (((k8 & 7) ^ (jj & 7)) << 4)),
-                       Bj + (int64_t)jj * R + (nv > 0 ? 8 * k8 : 0), nv > 0 ? 2 * nv : 0);
-        }
-    };
-
-    if (warp == 0) tc_alloc(&s_tmem, kTcCols);
-    if (threadIdx.x == 0) mbar_init(&s_bar, 1);
-
-    // first chunk's out and B blocks (neither written by the previous kernel)
-    if (ADD) load_out(sO0, 0, threadIdx.x, kThreads);
-    load_b(0, threadIdx.x, kThreads);
-    cp_async_commit();
-
-    // y rows: produced by the previous kernel
-    grid_dep_wait();
-    grid_dep_launch();
-    const float *ys = a.y + (int64_t)s * a.y_slice_stride;
-    for (int it = threadIdx.x; it < n * KS * 4; it += kThreads) {  // 4 ranks per chunk
-        const int i = it / (KS * 4), k4 = it - i * (KS * 4);
-        const int row = s_rows[i];
-        const int nv = row >= 0 ? min(4, rl - 4 * k4) : 0;
-        cp_async16(smem_u32(sYf + i * YP + 4 * k4),
-                   ys + (int64_t)(row >= 0 ? row : 0) * a.ldy + (nv > 0 ? 4 * k4 : 0),
-                   nv > 0 ? 4 * nv : 0);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-
-    // y -> scaled hi/lo operands.  The G threads of a row (G = KS * 2 chunks
-    // of 8 ranks rounded up to a power of two, so a row's group is aligned
-    // inside one warp) reduce its max; padding chunks hold zeros.
-    {
-        const int G = KS <= 1 ? 2 : (KS <= 2 ? 4 : (KS <= 4 ? 8 : 16));
-        for (int it = threadIdx.x; it < kTile * G; it += kThreads) {
-            const int i = it / G, k8 = it - i * G;
-            const bool live = i < n && k8 < KS * 2;
-            float v[8];
-            float m = 0.f;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                v[k] = live ? sYf[i * YP + 8 * k8 + k] : 0.f;
-                m = fmaxf(m, fabsf(v[k]));
-            }
-            for (int o = 1; o < G; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            const int e = row_exponent(m);
-            const float inv = exp2i(-e);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) v[k] *= inv;
-            uint4 hi, lo;
-            split_hilo8<E>(v, hi, lo);
-            unsigned char *yh = sY + (k8 >> 3) * 2 * kTile * 128;
-            const int off = i * 128 + (((k8 & 7) ^ (i & 7)) << 4);
-            *reinterpret_cast<uint4 *>(yh + off) = hi;
-            *reinterpret_cast<uint4 *>(yh + kTile * 128 + off) = lo;
-            if (k8 == 0) s_f[i] = a.scale * exp2i(e);
-        }
-    }
-    tc_fence_before();
-    __syncthreads();  // the y rows in sO1 are consumed; sO1 may take chunk 1's out block
-    tc_fence_after();
-    const uint32_t tmem = s_tmem;
     const uint32_t idesc = tc_idesc_f16(std::is_same<E, __nv_bfloat16>::value, 128, kTcCols);
 
-    for (int j = 0; j < nsub; ++j) {
-        unsigned char *sOc = (j & 1) ? sO1 : sO0;
-        // next chunk's out block into the other buffer (its epilogue is over)
-        if (ADD && j + 1 < nsub) load_out((j & 1) ? sO0 : sO1, j + 1, threadIdx.x, kThreads);
-        cp_async_commit();
-        cp_async_wait<1>();          // this chunk's out and B blocks are in
-        fence_proxy_async_smem();    // ... and visible to the tensor cores
-        __syncthreads();
-        tc_fence_after();
-        if (threadIdx.x == 0) {
-            for (int k = 0; k < KS; ++k) {
-                const int h = k >> 2;
-                const uint32_t yh = smem_u32(sY) + h * 2 * kTile * 128 + 32 * (k & 3);
-                const uint32_t bb = smem_u32(sB) + h * kTcCols * 128 + 32 * (k & 3);
-                tc_mma_f16(tmem, tc_desc_sw128(yh), tc_desc_sw128(bb), idesc, k > 0);
-                tc_mma_f16(tmem, tc_desc_sw128(yh + kTile * 128), tc_desc_sw128(bb), idesc, true);
-            }
-            tc_commit(&s_bar);
+    bool have_tmem = false;   // TMEM and the barrier are set up on the first tile needing them
+    uint32_t tmem = 0, ncommit = 0;
+    bool timed_out = false;
+    for (; tile < n_tiles; tile += gridDim.x) {
+        if (tile != (int)blockIdx.x) {
+            tl = __ldg(a.tiles + tile);
+            my_row = threadIdx.x < kTile ? __ldg(a.tile_rows + (int64_t)tile * kTile + threadIdx.x)
+                                         : -1;
+            __syncthreads();  // the previous tile is done with s_rows / s_f
         }
-        const bool timed_out = !mbar_wait_cta(&s_bar, j & 1);
-        if (timed_out && threadIdx.x == 0) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
-        tc_fence_after();
+        if (threadIdx.x < kTile) s_rows[threadIdx.x] = my_row < a.T ? my_row : -1;
+        const int l = tl.x, n = tl.z;
+        const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, a.R) : 0;
+        __syncthreads();
 
-        if (warp >= 2) {
-            // the MMA has read B: next chunk's B block
-            if (j + 1 < nsub) load_b(j + 1, threadIdx.x - 64, kThreads - 64);
-            cp_async_commit();
-        } else {
-            // epilogue: warps 0 and 1 own the tile's 64 token lanes
-            const int i = 32 * warp + lane;
-            const int row = i < n ? s_rows[i] : -1;
-            const float f = s_f[i];
-            const uint32_t tl_addr = tmem + ((uint32_t)(32 * warp) << 16);
-            const int cj = j * kTcCols, nc = min(kTcCols, span_cols - cj);
-            for (int c0 = 0; c0 < nc; c0 += 32) {  // warp-uniform
-                float d[32];
-                tc_ld32(tl_addr + c0, d);
-                if (row < 0) continue;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const int c = c0 + 8 * g;
-                    if (c >= nc) break;
-                    float v[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) v[k] = f * d[8 * g + k];
-                    if (ADD) {
-                        float o[8];
-                        unpack8<E>(*reinterpret_cast<const uint4 *>(sOc + i * kTcOutPitch + 2 * c), o);
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) v[k] += o[k];
-                    }
-                    st_global_v4(out + (int64_t)row * a.ldo + colbase + cj + c, pack8<E>(v));
+        if (rl == 0) {  // adapter -1 or rank 0: untouched with add_inputs, zeros without
+            grid_dep_wait();
+            grid_dep_launch();
+            if (!ADD)
+                for (int it = threadIdx.x; it < n * (span_cols / 8); it += kThreads) {
+                    const int i = it / (span_cols / 8), c8 = it - i * (span_cols / 8);
+                    const int row = s_rows[i];
+                    if (row >= 0)
+                        st_global_v4(out + (int64_t)row * a.ldo + colbase + 8 * c8, make_uint4(0, 0, 0, 0));
                 }
+            continue;
+        }
+
+        const int KS = (rl + 15) / 16;
+        const E *Bl = static_cast<const E *>(a.B[s]) + ((int64_t)l * a.N[s] + n_span) * R;
+
+        // chunk j's out block into dst (threads t0, t0 + nt, ...)
+        auto load_out = [&](unsigned char *dst, int j, int t0, int nt) {
+            const int c0 = j * kTcCols, c8n = min(kTcCols, span_cols - c0) / 8;
+            for (int it = t0; it < n * c8n; it += nt) {
+                const int i = it / c8n, c8 = it - i * c8n;
+                const int row = s_rows[i];
+                if (row >= 0)
+                    cp_async16(smem_u32(dst + i * kTcOutPitch + 16 * c8),
+                               out + (int64_t)row * a.ldo + colbase + c0 + 8 * c8, 16);
+            }
+        };
+        // chunk j's B block (8 ranks per 16-byte piece, ranks >= rl zero-filled)
+        auto load_b = [&](int j, int t0, int nt) {
+            const int c0 = j * kTcCols, nc = min(kTcCols, span_cols - c0);
+            const E *Bj = Bl + (int64_t)c0 * R;
+            for (int it = t0; it < nc * KS * 2; it += nt) {
+                const int jj = it / (KS * 2), k8 = it - jj * (KS * 2);
+                const int nv = min(8, rl - 8 * k8);
+                cp_async16(smem_u32(sB + (k8 >> 3) * kTcCols * 128 + jj * 128 + (((k8 & 7) ^ (jj & 7)) << 4)),
+                           Bj + (int64_t)jj * R + (nv > 0 ? 8 * k8 : 0), nv > 0 ? 2 * nv : 0);
+            }
+        };
+
+        if (!have_tmem) {
+            if (warp == 0) tc_alloc(&s_tmem, kTcCols);
+            if (threadIdx.x == 0) mbar_init(&s_bar, 1);
+        }
+
+        // first chunk's out and B blocks (neither written by the previous kernel)
+        if (ADD) load_out(sO0, 0, threadIdx.x, kThreads);
+        load_b(0, threadIdx.x, kThreads);
+        cp_async_commit();
+
+        // y rows: produced by the previous kernel
+        grid_dep_wait();
+        grid_dep_launch();
+        const float *ys = a.y + (int64_t)s * a.y_slice_stride;
+        for (int it = threadIdx.x; it < n * KS * 4; it += kThreads) {  // 4 ranks per chunk
+            const int i = it / (KS * 4), k4 = it - i * (KS * 4);
+            const int row = s_rows[i];
+            const int nv = row >= 0 ? min(4, rl - 4 * k4) : 0;
+            cp_async16(smem_u32(sYf + i * YP + 4 * k4),
+                       ys + (int64_t)(row >= 0 ? row : 0) * a.ldy + (nv > 0 ? 4 * k4 : 0),
+                       nv > 0 ? 4 * nv : 0);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+
+        // y -> scaled hi/lo operands.  The G threads of a row (G = KS * 2 chunks
+        // of 8 ranks rounded up to a power of two, so a row's group is aligned
+        // inside one warp) reduce its max; padding chunks hold zeros.
+        {
+            const int G = KS <= 1 ? 2 : (KS <= 2 ? 4 : (KS <= 4 ? 8 : 16));
+            for (int it = threadIdx.x; it < kTile * G; it += kThreads) {
+                const int i = it / G, k8 = it - i * G;
+                const bool live = i < n && k8 < KS * 2;
+                float v[8];
+                float m = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    v[k] = live ? sYf[i * YP + 8 * k8 + k] : 0.f;
+                    m = fmaxf(m, fabsf(v[k]));
+                }
+                for (int o = 1; o < G; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                const int e = row_exponent(m);
+                const float inv = exp2i(-e);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] *= inv;
+                uint4 hi, lo;
+                split_hilo8<E>(v, hi, lo);
+                unsigned char *yh = sY + (k8 >> 3) * 2 * kTile * 128;
+                const int off = i * 128 + (((k8 & 7) ^ (i & 7)) << 4);
+                *reinterpret_cast<uint4 *>(yh + off) = hi;
+                *reinterpret_cast<uint4 *>(yh + kTile * 128 + off) = lo;
+                if (k8 == 0) s_f[i] = a.scale * exp2i(e);
             }
         }
         tc_fence_before();
-        // TMEM and this out buffer are free again; a timed-out wait ends the CTA
-        if (__syncthreads_or(timed_out)) break;
+        __syncthreads();  // the y rows in sO1 are consumed; sO1 may take chunk 1's out block
+        tc_fence_after();
+        if (!have_tmem) {
+            tmem = s_tmem;
+            have_tmem = true;
+        }
+
+        for (int j = 0; j < nsub; ++j) {
+            unsigned char *sOc = (j & 1) ? sO1 : sO0;
+            // next chunk's out block into the other buffer (its epilogue is over)
+            if (ADD && j + 1 < nsub) load_out((j & 1) ? sO0 : sO1, j + 1, threadIdx.x, kThreads);
+            cp_async_commit();
+            cp_async_wait<1>();          // this chunk's out and B blocks are in
+            fence_proxy_async_smem();    // ... and visible to the tensor cores
+            __syncthreads();
+            tc_fence_after();
+            if (threadIdx.x == 0) {
+                for (int k = 0; k < KS; ++k) {
+                    const int h = k >> 2;
+                    const uint32_t yh = smem_u32(sY) + h * 2 * kTile * 128 + 32 * (k & 3);
+                    const uint32_t bb = smem_u32(sB) + h * kTcCols * 128 + 32 * (k & 3);
+                    tc_mma_f16(tmem, tc_desc_sw128(yh), tc_desc_sw128(bb), idesc, k > 0);
+                    tc_mma_f16(tmem, tc_desc_sw128(yh + kTile * 128), tc_desc_sw128(bb), idesc, true);
+                }
+                tc_commit(&s_bar);
+            }
+            // A wait that runs out (never expected) flags the plan and ends the
+            // CTA without touching out: no epilogue, no further loads.
+            const bool to = !mbar_wait_cta(&s_bar, ncommit & 1);
+            ++ncommit;
+            if (__syncthreads_or(to)) {
+                if (threadIdx.x == 0) atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+
+            if (warp >= 2) {
+                // the MMA has read B: next chunk's B block
+                if (j + 1 < nsub) load_b(j + 1, threadIdx.x - 64, kThreads - 64);
+                cp_async_commit();
+            } else {
+                // epilogue: warps 0 and 1 own the tile's 64 token lanes
+                const int i = 32 * warp + lane;
+                const int row = i < n ? s_rows[i] : -1;
+                const float f = s_f[i];
+                const uint32_t tl_addr = tmem + ((uint32_t)(32 * warp) << 16);
+                const int cj = j * kTcCols, nc = min(kTcCols, span_cols - cj);
+                for (int c0 = 0; c0 < nc; c0 += 32) {  // warp-uniform
+                    float d[32];
+                    tc_ld32(tl_addr + c0, d);
+                    if (row < 0) continue;
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int c = c0 + 8 * g;
+                        if (c >= nc) break;
+                        float v[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) v[k] = f * d[8 * g + k];
+                        if (ADD) {
+                            float o[8];
+                            unpack8<E>(*reinterpret_cast<const uint4 *>(sOc + i * kTcOutPitch + 2 * c), o);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) v[k] += o[k];
+                        }
+                        st_global_v4(out + (int64_t)row * a.ldo + colbase + cj + c, pack8<E>(v));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncthreads();  // TMEM and this out buffer are free again
+        }
+        cp_async_wait<0>();
+        if (timed_out) break;
     }
-    cp_async_wait<0>();
-    tc_fence_after();
-    if (warp == 0) tc_dealloc(tmem, kTcCols);
+    if (have_tmem) {
+        cp_async_wait<0>();
+        // after a timed-out wait, give the MMA one more bounded wait before
+        // the accumulator columns are released
+        if (timed_out) mbar_wait_cta(&s_bar, (ncommit - 1) & 1);
+        __syncthreads();
+        tc_fence_after();
+        if (warp == 0) tc_dealloc(tmem, kTcCols);
+    }
 }
 
 template <typename E, bool ADD, bool VEC>
