@@ -1,5 +1,16 @@
 """Shared test helpers: run a workload through the CUDA path and through the
-oracle on the same seeded inputs, and compare them element by element."""
+oracle on the same seeded inputs, and compare them element by element.
+
+Three bounds are applied (each stated where it is defined):
+* end to end, out against the oracle's out: the stated tolerance of the
+  output type, |d| <= ATOL + RTOL * |ref| (TOL);
+* y, the fp32 shrink output, against the oracle's y: the fp32-accumulation
+  bound Y_REL * |scale| * sum_h |x[t,h] * A[l,j,h]| + Y_ABS (assert_y_fp32);
+* out against the oracle's expand applied to the GPU's own y: one unit in
+  the last place of the output type plus an fp32-accumulation term
+  (assert_expand_ulp), so an error in the LoRA term cannot hide behind the
+  looser end-to-end tolerance or the input-precision error of y.
+"""
 from __future__ import annotations
 
 import numpy as np
@@ -22,6 +33,84 @@ def assert_close(got, ref, dtype, what=""):
         raise AssertionError(
             f"{what}: {bad.sum()} of {bad.size} elements out of tolerance; first at {tuple(i)}: "
             f"got {got[tuple(i)]!r} ref {ref[tuple(i)]!r}; max err {err.max():.3e}")
+
+
+# fp32 accumulation: products of fp16/bf16 values are exact in fp32 and every
+# addition on the way to y (tensor-core K steps, stages, split-K partials)
+# rounds with relative error <= 2^-23 (truncation included).  A chain of d
+# additions whose rounding errors have random signs is off by about
+# sqrt(d) * 2^-23 of the sum of |terms|; the deepest chain here is one CTA's
+# H / 16 K steps (d = 1024 at H = 16384 without split-K: ~4e-6).  1e-5 of
+# the sum of |terms| bounds that with margin (measured errors are ~1e-8 of
+# it), while a y rounded to bf16 (relative error up to 2^-9 of |y|) fails it.
+Y_REL, Y_ABS = 1e-5, 1e-7
+
+
+def assert_y_fp32(y, case, rows=None, what=""):
+    """y (GPU, fp32) against the oracle's shrink within the fp32-accumulation
+    bound; the bound's sum of |terms| is the oracle's shrink of |x| and |A|."""
+    lo, _, _ = oracle_map(case)
+    x = case.x
+    if rows is not None:
+        rows = np.asarray(rows)
+        lo, x = lo[rows], x[rows]
+        y = y[rows]
+    ranks = case.ranks.numpy() if case.ranks is not None else None
+    kw = dict(num_slices=case.num_slices, ranks=ranks)
+    ref = oracle.shrink(f64(x), f64(case.A), lo, scale=case.shrink_scale, **kw)
+    mag = oracle.shrink(np.abs(f64(x)), np.abs(f64(case.A)), lo, scale=abs(case.shrink_scale),
+                        **kw)
+    got = y.double().cpu().numpy() if isinstance(y, torch.Tensor) else np.asarray(y)
+    got = got[:, :ref.shape[1]]
+    err = np.abs(got - ref)
+    bound = Y_REL * mag + Y_ABS
+    bad = err > bound
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what} y: {bad.sum()} of {bad.size} beyond the fp32 bound; first "
+                             f"at {i}: got {got[i]!r} ref {ref[i]!r} bound {bound[i]:.3e}")
+
+
+def ulp(v: np.ndarray, dtype) -> np.ndarray:
+    """Spacing of the fp16 / bf16 numbers at |v| (subnormal spacing near 0)."""
+    mant, emin = (10, -14) if dtype == torch.float16 else (7, -126)
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** emin)))
+    return 2.0 ** (e - mant)
+
+
+# Expand feeds y to the tensor cores as a hi + lo pair of the weight type after
+# a per-row power-of-two scaling (residual <= 2^-18 of the row's largest |y|
+# for bf16, below fp16's subnormal spacing otherwise) and sums <= 128 products
+# in fp32 (<= 128 * 2^-23); 2^-14 of sum |scale * y * B| covers both.
+EXPAND_REL = 2.0 ** -14
+
+
+def assert_expand_ulp(out, y, case, rows=None, what=""):
+    """out (GPU) against the oracle's expand_slice of the GPU's own y: within
+    one unit in the last place of the output type plus EXPAND_REL of the sum
+    of |scale * y * B| (one rounding of an fp32 result, plus fp32 error)."""
+    lo, _, _ = oracle_map(case)
+    out0 = case.out
+    if rows is not None:
+        rows = np.asarray(rows)
+        lo, out0 = lo[rows], out0[rows]
+        y, out = y[rows], out[rows]
+    ranks = case.ranks.numpy() if case.ranks is not None else None
+    yd = y.double().cpu().numpy()
+    Bs = [f64(b) for b in case.B]
+    kw = dict(y_stride=case.R, ranks=ranks)
+    ref = oracle.expand_slice(yd, Bs, case.slice_offsets, lo, f64(out0), scale=case.scale,
+                              add=case.add, **kw)
+    mag = oracle.expand_slice(np.abs(yd), [np.abs(b) for b in Bs], case.slice_offsets, lo,
+                              np.zeros(ref.shape), scale=abs(case.scale), add=False, **kw)
+    got = out.double().cpu().numpy()
+    err = np.abs(got - ref)
+    bound = ulp(np.maximum(np.abs(got), np.abs(ref)), case.dtype) + EXPAND_REL * mag
+    bad = err > bound
+    if bad.any():
+        i = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{what} out: {bad.sum()} of {bad.size} beyond one ulp; first at "
+                             f"{i}: got {got[i]!r} ref {ref[i]!r} bound {bound[i]:.3e}")
 
 
 def f64(t: torch.Tensor) -> np.ndarray:
@@ -80,8 +169,9 @@ def oracle_run(case, rows=None):
     return y, o
 
 
-def gpu_run_fused(lg, case, dev="cuda"):
-    """plan + fused shrink/expand_slice on the GPU.  Returns (y, out, plan)."""
+def gpu_run_chained(lg, case, dev="cuda"):
+    """plan + lora_shrink_expand_slice (shrink and expand_slice chained in one
+    call) on the GPU.  Returns (y, out, plan)."""
     plan = gpu_plan(lg, case, dev)
     x, A = case.x.to(dev), case.A.to(dev)
     Bs = [b.to(dev) for b in case.B]

@@ -8,19 +8,21 @@ import pytest
 import torch
 
 import lora_inputs as li
-from helpers import assert_close, gpu_run, gpu_run_fused, oracle_run
+from helpers import (assert_close, assert_expand_ulp, assert_y_fp32, gpu_run, gpu_run_chained,
+                     oracle_run)
 from test_gpu_ops import make_case
 
 pytestmark = pytest.mark.gpu
 
 
 def check(lg, case, rows=None):
-    y, out, _ = gpu_run_fused(lg, case)
+    y, out, _ = gpu_run_chained(lg, case)
     y_ref, o_ref = oracle_run(case, rows)
+    assert_y_fp32(y, case, rows, f"{case.name} chained")
+    assert_expand_ulp(out, y, case, rows, f"{case.name} chained")
     if rows is not None:
         y, out = y[rows], out[rows]
-    assert_close(y, y_ref, case.dtype, f"{case.name} fused y")
-    assert_close(out, o_ref, case.dtype, f"{case.name} fused out")
+    assert_close(out, o_ref, case.dtype, f"{case.name} chained out")
     return y, out
 
 
@@ -33,11 +35,16 @@ def test_bgmv_small(cuda_lib):
 
 
 @pytest.mark.parametrize("T", li.DECODE_T)
-def test_decode_qkv(cuda_lib, T):
+@pytest.mark.parametrize("add", [True, False])
+def test_decode_qkv(cuda_lib, T, add):
     c = li.decode_qkv(T)
+    c.add = add
     y, out = check(cuda_lib, c)
     m = (c.token_idx == -1).numpy()
-    assert torch.equal(out[m].view(torch.int16), c.out[m].view(torch.int16))
+    if add:
+        assert torch.equal(out[m].view(torch.int16), c.out[m].view(torch.int16))
+    else:
+        assert (out[m].float() == 0).all()
 
 
 @pytest.mark.parametrize("r", (16, 32, 64))
@@ -99,7 +106,7 @@ def test_matches_two_operator_path(cuda_lib):
     lg = cuda_lib
     c = li.decode_qkv(512, seed=99)
     y1, o1, _ = gpu_run(lg, c)
-    y2, o2, _ = gpu_run_fused(lg, c)
+    y2, o2, _ = gpu_run_chained(lg, c)
     assert torch.equal(y2, y1)
     assert torch.equal(o2.view(torch.int16), o1.view(torch.int16))
 

@@ -163,3 +163,8 @@ def test_group_golden_aaabcc(cuda_lib):
         assert v["group_lora"][:G].tolist() == c["group_lora"]
         assert v["group_start"][:G].tolist() == c["group_start"]
         assert v["group_count"][:G].tolist() == c["group_count"]
+        nt = len(c["tiles"])
+        assert v["header"][lg.HDR["NTILES"]] == nt
+        assert v["tiles"][:nt].tolist() == c["tiles"]
+        for k, (l, p0, n, grp) in enumerate(c["tiles"]):
+            assert v["tile_rows"][k].tolist() == c["perm"][p0:p0 + n] + [-1] * (lg.TILE_TOKENS - n)

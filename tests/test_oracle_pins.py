@@ -165,7 +165,8 @@ def test_group_golden_aaabcc():
             assert err == 0
             gr = oracle.group(lo, L, by_adapter=False)
         assert bad == 0
-        for k in ("perm", "count", "offset", "group_lora", "group_start", "group_count"):
+        for k in ("perm", "count", "offset", "group_lora", "group_start", "group_count",
+                  "tiles"):
             assert gr[k].tolist() == c[k], (c["name"], k)
 
 
