@@ -255,6 +255,71 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
                                        lora_stream_t stream);
 
 /*
+ * Plan-free BGMV (bgmv_shrink / bgmv_expand_slice of vLLM PR #11579; the
+ * per-input adapter of Punica issue #17; the mask-free single-adapter path
+ * and the skipping of blocks without work of vLLM PR #15655's summary list).
+ *
+ * The decode-path form for batches served by a few adapters: no plan and no
+ * grouping launch.  Tokens stay in their natural order; each block of 128
+ * consecutive tokens is contracted against the weights of every adapter that
+ * has a token in it, and each token keeps its own adapter's result.  The
+ * definitions, the meaning of y, ranks, slices, scale and add_inputs, and the
+ * results (to fp32-accumulation accuracy) are those of the grouped operators
+ * above with the plan of lora_group_tokens(token_idx).
+ *
+ *   token_idx [T]  device int32 adapter index per token (-1 = no LoRA; other
+ *                  values outside [0, L) also act as -1, and are not counted:
+ *                  lora_group_tokens counts them).  NULL means every token
+ *                  uses adapter 0: the dense single-adapter case, with no
+ *                  index read and no masking.
+ *   status         optional device int32 (NULL = none): LORA_PLANERR_TIMEOUT is
+ *                  OR-ed into it if a kernel's bounded wait expired (never
+ *                  expected; that call's outputs are then not valid).
+ *
+ * Shapes taken (LORA_ERR_UNSUPPORTED otherwise, before anything is enqueued;
+ * the grouped operators take every shape):
+ *   L <= LORA_BGMV_MAX_ADAPTERS, T <= LORA_BGMV_MAX_TOKENS;
+ *   shrink: x and A 16-byte aligned, ldx and H multiples of 8,
+ *           num_slices * R a multiple of 8;
+ *   expand: R a multiple of 8 and <= 64, L * (R rounded up to 16) <= 128,
+ *           y 16-byte aligned with ldy and y_slice_stride multiples of 4,
+ *           out 16-byte aligned with ldo, every slice width and offset
+ *           multiples of 8, every B_s 16-byte aligned.
+ * With a rank table, rows / columns >= r_l are never used in the result (the
+ * shrink reads A rows up to R and discards the extra products).
+ * Errors: as the grouped operators (no plan argument), plus
+ * LORA_ERR_UNSUPPORTED for shapes outside the list above.
+ */
+#define LORA_BGMV_MAX_ADAPTERS 8
+#define LORA_BGMV_MAX_TOKENS (65535 * 128)
+lora_status_t lora_bgmv_shrink(lora_dtype_t dtype, const int32_t *token_idx, const void *x,
+                               int64_t ldx, int32_t T, int32_t H, const void *A, int32_t L,
+                               int32_t R, int32_t num_slices, const int32_t *ranks, float *y,
+                               int64_t ldy, float scale, int add_inputs, int32_t *status,
+                               lora_stream_t stream);
+
+lora_status_t lora_bgmv_expand_slice(lora_dtype_t dtype, const int32_t *token_idx, const float *y,
+                                     int64_t ldy, int32_t T, int32_t num_slices,
+                                     const void *const *B_slices, const int32_t *slice_N,
+                                     const int32_t *slice_offset, int32_t y_slice_stride,
+                                     int32_t L, int32_t R, const int32_t *ranks, void *out,
+                                     int64_t ldo, float scale, int add_inputs, int32_t *status,
+                                     lora_stream_t stream);
+
+/* Shrink then expand_slice (y_slice_stride = R), the expand chained to the
+ * shrink by programmatic dependent launch: it stages its out tiles and B rows
+ * while the shrink runs and reads y once the shrink grid has completed. */
+lora_status_t lora_bgmv_shrink_expand_slice(lora_dtype_t dtype, const int32_t *token_idx,
+                                            const void *x, int64_t ldx, int32_t T, int32_t H,
+                                            const void *A, int32_t L, int32_t R,
+                                            const int32_t *ranks, float *y, int64_t ldy,
+                                            int32_t num_slices, const void *const *B_slices,
+                                            const int32_t *slice_N, const int32_t *slice_offset,
+                                            void *out, int64_t ldo, float scale_shrink,
+                                            float scale_expand, int add_inputs, int32_t *status,
+                                            lora_stream_t stream);
+
+/*
  * lora_shrink_expand_slice for callers that cannot allocate device memory.
  * The pages have no counterpart of this entry point: it is a convenience of
  * this library, not a step of the method.

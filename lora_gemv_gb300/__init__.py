@@ -14,6 +14,9 @@ Functions carry the C names:
 * ``lora_expand(y, B, out, plan, ...)``
 * ``lora_expand_slice(y, B_slices, out, plan, slice_offsets, ...)``
 * ``lora_shrink_expand_slice(x, A, y, B_slices, out, plan, slice_offsets, ...)``
+* ``lora_bgmv_shrink(x, A, y, token_idx, ...)``, ``lora_bgmv_expand_slice(y, B_slices, out,
+  slice_offsets, token_idx, ...)``, ``lora_bgmv_shrink_expand_slice(...)``: the plan-free
+  decode path (token_idx None = one adapter for every token)
 * ``lora_shrink_expand_slice_noalloc(token_idx, x, A, y, B_slices, out, slice_offsets, ...)``
   (the decode pair with the library's own plan array: no plan argument)
 * ``lora_get_error(plan)``
@@ -41,8 +44,10 @@ PLAN_MAGIC = 0x4C6F5241
 EXPORTS = ("lora_plan_layout", "lora_workspace_size", "lora_group_tokens",
            "lora_group_segments", "lora_shrink", "lora_expand", "lora_expand_slice",
            "lora_shrink_expand_slice", "lora_shrink_expand_slice_noalloc", "lora_get_error",
-           "lora_status_string", "lora_last_error_detail", "lora_version")
+           "lora_status_string", "lora_last_error_detail", "lora_version", "lora_bgmv_shrink",
+           "lora_bgmv_expand_slice", "lora_bgmv_shrink_expand_slice")
 NOALLOC_MAX_TOKENS = 4096
+BGMV_MAX_ADAPTERS = 8
 
 _lib = None
 
@@ -98,6 +103,18 @@ def load():
                                                      ctypes.POINTER(i32), ctypes.POINTER(i32), vp,
                                                      i64, f32, f32, ctypes.c_int, vp]
     lib.lora_shrink_expand_slice_noalloc.restype = st
+    lib.lora_bgmv_shrink.argtypes = [st, vp, vp, i64, i32, i32, vp, i32, i32, i32, vp, vp, i64,
+                                     f32, ctypes.c_int, vp, vp]
+    lib.lora_bgmv_shrink.restype = st
+    lib.lora_bgmv_expand_slice.argtypes = [st, vp, vp, i64, i32, i32, ctypes.POINTER(vp),
+                                           ctypes.POINTER(i32), ctypes.POINTER(i32), i32, i32, i32,
+                                           vp, vp, i64, f32, ctypes.c_int, vp, vp]
+    lib.lora_bgmv_expand_slice.restype = st
+    lib.lora_bgmv_shrink_expand_slice.argtypes = [st, vp, vp, i64, i32, i32, vp, i32, i32, vp, vp,
+                                                  i64, i32, ctypes.POINTER(vp),
+                                                  ctypes.POINTER(i32), ctypes.POINTER(i32), vp,
+                                                  i64, f32, f32, ctypes.c_int, vp, vp]
+    lib.lora_bgmv_shrink_expand_slice.restype = st
     lib.lora_get_error.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), vp]
     lib.lora_get_error.restype = st
     lib.lora_status_string.argtypes = [st]
@@ -354,3 +371,98 @@ def lora_shrink_expand_slice_noalloc(token_idx: torch.Tensor, x: torch.Tensor, A
         L, R, _i32(ranks, "ranks"), _dev(y, "y"), _rows(y, "y"), S, ptrs, Ns, offs,
         _dev(out, "out"), _rows(out, "out"), float(scale_shrink), float(scale_expand),
         int(bool(add_inputs)), _stream(x)))
+
+
+# ------------------------------------------------------------------ plan-free BGMV
+
+def _slices(B_slices, slice_offsets, out, L, R):
+    S = len(B_slices)
+    if S != len(slice_offsets):
+        raise ValueError("one offset per slice")
+    for b in B_slices:
+        if b.dim() != 3 or not b.is_contiguous() or b.shape[0] != L or b.shape[2] != R \
+                or b.dtype != out.dtype:
+            raise ValueError("every B_s must be a contiguous [L, N_s, R] tensor of out's dtype")
+    if any(int(o) + b.shape[1] > out.shape[1] for o, b in zip(slice_offsets, B_slices)):
+        raise ValueError("a slice ends past out's columns")
+    ptrs = (ctypes.c_void_p * S)(*[_dev(b, "B_s") for b in B_slices])
+    Ns = (ctypes.c_int32 * S)(*[b.shape[1] for b in B_slices])
+    offs = (ctypes.c_int32 * S)(*[int(o) for o in slice_offsets])
+    return S, ptrs, Ns, offs
+
+
+def lora_bgmv_shrink(x: torch.Tensor, A: torch.Tensor, y: torch.Tensor,
+                     token_idx: Optional[torch.Tensor], *, num_slices: int = 1,
+                     ranks: Optional[torch.Tensor] = None, scale: float = 1.0,
+                     add_inputs: bool = False, status: Optional[torch.Tensor] = None) -> None:
+    """Plan-free y[:, :S*R] (+)= scale * x @ A[idx]^T.  token_idx [T] int32 or None
+    (every token uses adapter 0); status: optional int32 device word."""
+    T, H = x.shape
+    if A.dim() != 3 or not A.is_contiguous() or A.shape[2] != H or A.dtype != x.dtype:
+        raise ValueError("A must be a contiguous [L, S*R, H] tensor of x's dtype")
+    L, SR, _ = A.shape
+    if SR % num_slices:
+        raise ValueError("A rows are not a multiple of num_slices")
+    if y.dtype != torch.float32 or y.shape[0] != T or y.shape[1] < SR:
+        raise ValueError("y must be fp32 [T, >= S*R]")
+    if token_idx is not None and token_idx.numel() != T:
+        raise ValueError("token_idx must hold one index per row of x")
+    _check(load().lora_bgmv_shrink(_dtype(x), _i32(token_idx, "token_idx"), _dev(x, "x"),
+                                   _rows(x, "x"), T, H, _dev(A, "A"), L, SR // num_slices,
+                                   num_slices, _i32(ranks, "ranks"), _dev(y, "y"), _rows(y, "y"),
+                                   float(scale), int(bool(add_inputs)), _i32(status, "status"),
+                                   _stream(x)))
+
+
+def lora_bgmv_expand_slice(y: torch.Tensor, B_slices: Sequence[torch.Tensor], out: torch.Tensor,
+                           slice_offsets: Sequence[int], token_idx: Optional[torch.Tensor], *,
+                           y_slice_stride: int, ranks: Optional[torch.Tensor] = None,
+                           scale: float = 1.0, add_inputs: bool = True,
+                           status: Optional[torch.Tensor] = None) -> None:
+    """Plan-free expand_slice: every slice s, out[:, off_s:off_s+N_s] (+)=
+    scale * y[:, s*ys : s*ys+R] @ B_s[idx]^T, all slices in one launch."""
+    L, _, R = B_slices[0].shape
+    T = out.shape[0]
+    S, ptrs, Ns, offs = _slices(B_slices, slice_offsets, out, L, R)
+    if y.dtype != torch.float32 or y.shape[0] != T \
+            or y.shape[1] < (S - 1) * int(y_slice_stride) + R:
+        raise ValueError("y must be fp32 [T, >= (S-1)*y_slice_stride + R]")
+    if token_idx is not None and token_idx.numel() != T:
+        raise ValueError("token_idx must hold one index per row of out")
+    _check(load().lora_bgmv_expand_slice(_dtype(out), _i32(token_idx, "token_idx"), _dev(y, "y"),
+                                         _rows(y, "y"), T, S, ptrs, Ns, offs,
+                                         int(y_slice_stride), L, R, _i32(ranks, "ranks"),
+                                         _dev(out, "out"), _rows(out, "out"), float(scale),
+                                         int(bool(add_inputs)), _i32(status, "status"),
+                                         _stream(out)))
+
+
+def lora_bgmv_shrink_expand_slice(x: torch.Tensor, A: torch.Tensor, y: torch.Tensor,
+                                  B_slices: Sequence[torch.Tensor], out: torch.Tensor,
+                                  slice_offsets: Sequence[int],
+                                  token_idx: Optional[torch.Tensor], *,
+                                  ranks: Optional[torch.Tensor] = None,
+                                  scale_shrink: float = 1.0, scale_expand: float = 1.0,
+                                  add_inputs: bool = True,
+                                  status: Optional[torch.Tensor] = None) -> None:
+    """Plan-free shrink then expand_slice (y_slice_stride = R), chained."""
+    T, H = x.shape
+    if A.dim() != 3 or not A.is_contiguous() or A.shape[2] != H or A.dtype != x.dtype:
+        raise ValueError("A must be a contiguous [L, S*R, H] tensor of x's dtype")
+    L, SR, _ = A.shape
+    S = len(B_slices)
+    if SR % S:
+        raise ValueError("A rows must be S*R")
+    R = SR // S
+    if out.dtype != x.dtype or out.shape[0] != T:
+        raise ValueError("out must be [T, N_total] of x's dtype")
+    S, ptrs, Ns, offs = _slices(B_slices, slice_offsets, out, L, R)
+    if y.dtype != torch.float32 or y.shape[0] != T or y.shape[1] < SR:
+        raise ValueError("y must be fp32 [T, >= S*R]")
+    if token_idx is not None and token_idx.numel() != T:
+        raise ValueError("token_idx must hold one index per row of x")
+    _check(load().lora_bgmv_shrink_expand_slice(
+        _dtype(x), _i32(token_idx, "token_idx"), _dev(x, "x"), _rows(x, "x"), T, H, _dev(A, "A"),
+        L, R, _i32(ranks, "ranks"), _dev(y, "y"), _rows(y, "y"), S, ptrs, Ns, offs,
+        _dev(out, "out"), _rows(out, "out"), float(scale_shrink), float(scale_expand),
+        int(bool(add_inputs)), _i32(status, "status"), _stream(x)))

@@ -37,7 +37,8 @@ cudaError_t init_device(int dev, lora::DeviceInfo *info) {
     if (e != cudaSuccess) return e;
     if ((e = lora::configure_plan_kernels()) != cudaSuccess) return e;
     if ((e = lora::configure_shrink_kernels(info)) != cudaSuccess) return e;
-    return lora::configure_expand_kernels();
+    if ((e = lora::configure_expand_kernels()) != cudaSuccess) return e;
+    return lora::configure_bgmv_kernels(*info);
 }
 
 // Per-device kernel attributes are set once, on the first call on that device.
@@ -423,5 +424,179 @@ const char *lora_status_string(lora_status_t status) {
 const char *lora_last_error_detail(void) { return g_detail; }
 
 int32_t lora_version(void) { return 100; }
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ plan-free BGMV
+
+namespace {
+
+lora_status_t check_bgmv_shrink(lora_dtype_t dtype, const int32_t *token_idx, const void *x,
+                                int64_t ldx, int32_t T, int32_t H, const void *A, int32_t L,
+                                int32_t R, int32_t num_slices, const int32_t *ranks,
+                                const float *y, int64_t ldy) {
+    if (!valid_dtype(dtype)) return fail(LORA_ERR_INVALID_ARG, "dtype %d", (int)dtype);
+    if (T < 0 || H < 1 || L < 1) return fail(LORA_ERR_INVALID_ARG, "T=%d H=%d L=%d", T, H, L);
+    if (R < 1 || R > LORA_MAX_RANK) return fail(LORA_ERR_INVALID_ARG, "R = %d", R);
+    if (num_slices < 1 || num_slices > LORA_MAX_SLICES)
+        return fail(LORA_ERR_INVALID_ARG, "num_slices = %d", num_slices);
+    if (ldx < H) return fail(LORA_ERR_INVALID_ARG, "ldx %lld < H %d", (long long)ldx, H);
+    if (ldy < (int64_t)num_slices * R)
+        return fail(LORA_ERR_INVALID_ARG, "ldy %lld < num_slices*R", (long long)ldy);
+    if (!A || (T > 0 && (!x || !y))) return fail(LORA_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(token_idx, 4) || !aligned(y, 4) || !aligned(ranks, 4))
+        return fail(LORA_ERR_INVALID_ARG, "misaligned pointer");
+    if (T > LORA_BGMV_MAX_TOKENS)
+        return fail(LORA_ERR_UNSUPPORTED, "T = %d > %d", T, LORA_BGMV_MAX_TOKENS);
+    if (L > LORA_BGMV_MAX_ADAPTERS)
+        return fail(LORA_ERR_UNSUPPORTED, "L = %d > %d (use the grouped operators)", L,
+                    LORA_BGMV_MAX_ADAPTERS);
+    return LORA_OK;
+}
+
+lora_status_t check_bgmv_expand(lora_dtype_t dtype, const int32_t *token_idx, const float *y,
+                                int64_t ldy, int32_t T, int32_t num_slices,
+                                const void *const *B_slices, const int32_t *slice_N,
+                                const int32_t *slice_offset, int32_t y_slice_stride, int32_t L,
+                                int32_t R, const int32_t *ranks, const void *out, int64_t ldo) {
+    if (T > LORA_BGMV_MAX_TOKENS)
+        return fail(LORA_ERR_UNSUPPORTED, "T = %d > %d", T, LORA_BGMV_MAX_TOKENS);
+    if (L > LORA_BGMV_MAX_ADAPTERS)
+        return fail(LORA_ERR_UNSUPPORTED, "L = %d > %d (use the grouped operators)", L,
+                    LORA_BGMV_MAX_ADAPTERS);
+    if (!aligned(token_idx, 4)) return fail(LORA_ERR_INVALID_ARG, "token_idx misaligned");
+    // the grouped operator's checks, with a stand-in for its plan argument
+    static const int4 no_plan = {0, 0, 0, 0};
+    return check_expand(dtype, y, ldy, T, num_slices, B_slices, slice_N, slice_offset,
+                        y_slice_stride, L, R, ranks, out, ldo, &no_plan);
+}
+
+lora::BgmvShrinkArgs bgmv_shrink_args(const int32_t *token_idx, const void *x, int64_t ldx,
+                                      int32_t T, int32_t H, const void *A, int32_t L, int32_t R,
+                                      int32_t num_slices, const int32_t *ranks, float *y,
+                                      int64_t ldy, float scale, int add_inputs,
+                                      int32_t *status) {
+    lora::BgmvShrinkArgs a{};
+    a.x = x;
+    a.ldx = ldx;
+    a.T = T;
+    a.H = H;
+    a.A = A;
+    a.L = L;
+    a.R = R;
+    a.S = num_slices;
+    a.idx = token_idx;
+    a.ranks = ranks;
+    a.y = y;
+    a.ldy = ldy;
+    a.scale = scale;
+    a.add = add_inputs ? 1 : 0;
+    a.status = status;
+    return a;
+}
+
+lora::BgmvExpandArgs bgmv_expand_args(const int32_t *token_idx, const float *y, int64_t ldy,
+                                      int32_t T, int32_t num_slices,
+                                      const void *const *B_slices, const int32_t *slice_N,
+                                      const int32_t *slice_offset, int32_t y_slice_stride,
+                                      int32_t L, int32_t R, const int32_t *ranks, void *out,
+                                      int64_t ldo, float scale, int add_inputs,
+                                      int32_t *status) {
+    lora::BgmvExpandArgs a{};
+    a.y = y;
+    a.ldy = ldy;
+    a.T = T;
+    a.idx = token_idx;
+    a.ranks = ranks;
+    a.L = L;
+    a.R = R;
+    a.y_slice_stride = y_slice_stride;
+    a.scale = scale;
+    a.add = add_inputs ? 1 : 0;
+    a.num_slices = num_slices;
+    for (int k = 0; k < num_slices; ++k) {
+        a.B[k] = B_slices[k];
+        a.N[k] = slice_N[k];
+        a.off[k] = slice_offset[k];
+    }
+    a.out = out;
+    a.ldo = ldo;
+    a.status = status;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+lora_status_t lora_bgmv_shrink(lora_dtype_t dtype, const int32_t *token_idx, const void *x,
+                               int64_t ldx, int32_t T, int32_t H, const void *A, int32_t L,
+                               int32_t R, int32_t num_slices, const int32_t *ranks, float *y,
+                               int64_t ldy, float scale, int add_inputs, int32_t *status,
+                               lora_stream_t stream) {
+    lora_status_t st = check_bgmv_shrink(dtype, token_idx, x, ldx, T, H, A, L, R, num_slices,
+                                         ranks, y, ldy);
+    if (st != LORA_OK) return st;
+    const lora::BgmvShrinkArgs a = bgmv_shrink_args(token_idx, x, ldx, T, H, A, L, R, num_slices,
+                                                    ranks, y, ldy, scale, add_inputs, status);
+    if (const char *why = lora::bgmv_shrink_supported(a)) return fail(LORA_ERR_UNSUPPORTED, "%s", why);
+    if (T == 0) return LORA_OK;
+    const lora::DeviceInfo *dev;
+    if ((st = device_info(&dev)) != LORA_OK) return st;
+    cudaError_t e = lora::launch_bgmv_shrink(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LORA_OK : cuda_fail(e, "bgmv shrink launch");
+}
+
+lora_status_t lora_bgmv_expand_slice(lora_dtype_t dtype, const int32_t *token_idx, const float *y,
+                                     int64_t ldy, int32_t T, int32_t num_slices,
+                                     const void *const *B_slices, const int32_t *slice_N,
+                                     const int32_t *slice_offset, int32_t y_slice_stride,
+                                     int32_t L, int32_t R, const int32_t *ranks, void *out,
+                                     int64_t ldo, float scale, int add_inputs, int32_t *status,
+                                     lora_stream_t stream) {
+    lora_status_t st = check_bgmv_expand(dtype, token_idx, y, ldy, T, num_slices, B_slices,
+                                         slice_N, slice_offset, y_slice_stride, L, R, ranks, out,
+                                         ldo);
+    if (st != LORA_OK) return st;
+    const lora::BgmvExpandArgs a =
+        bgmv_expand_args(token_idx, y, ldy, T, num_slices, B_slices, slice_N, slice_offset,
+                         y_slice_stride, L, R, ranks, out, ldo, scale, add_inputs, status);
+    if (const char *why = lora::bgmv_expand_supported(a)) return fail(LORA_ERR_UNSUPPORTED, "%s", why);
+    if (T == 0) return LORA_OK;
+    const lora::DeviceInfo *dev;
+    if ((st = device_info(&dev)) != LORA_OK) return st;
+    cudaError_t e = lora::launch_bgmv_expand(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LORA_OK : cuda_fail(e, "bgmv expand launch");
+}
+
+lora_status_t lora_bgmv_shrink_expand_slice(
+    lora_dtype_t dtype, const int32_t *token_idx, const void *x, int64_t ldx, int32_t T, int32_t H,
+    const void *A, int32_t L, int32_t R, const int32_t *ranks, float *y, int64_t ldy,
+    int32_t num_slices, const void *const *B_slices, const int32_t *slice_N,
+    const int32_t *slice_offset, void *out, int64_t ldo, float scale_shrink, float scale_expand,
+    int add_inputs, int32_t *status, lora_stream_t stream) {
+    lora_status_t st = check_bgmv_shrink(dtype, token_idx, x, ldx, T, H, A, L, R, num_slices,
+                                         ranks, y, ldy);
+    if (st != LORA_OK) return st;
+    st = check_bgmv_expand(dtype, token_idx, y, ldy, T, num_slices, B_slices, slice_N,
+                           slice_offset, R, L, R, ranks, out, ldo);
+    if (st != LORA_OK) return st;
+    const lora::BgmvShrinkArgs sa = bgmv_shrink_args(token_idx, x, ldx, T, H, A, L, R, num_slices,
+                                                     ranks, y, ldy, scale_shrink, 0, status);
+    const lora::BgmvExpandArgs ea =
+        bgmv_expand_args(token_idx, y, ldy, T, num_slices, B_slices, slice_N, slice_offset, R, L,
+                         R, ranks, out, ldo, scale_expand, add_inputs, status);
+    if (const char *why = lora::bgmv_shrink_supported(sa)) return fail(LORA_ERR_UNSUPPORTED, "%s", why);
+    if (const char *why = lora::bgmv_expand_supported(ea)) return fail(LORA_ERR_UNSUPPORTED, "%s", why);
+    if (T == 0) return LORA_OK;
+    const lora::DeviceInfo *dev;
+    if ((st = device_info(&dev)) != LORA_OK) return st;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    // The expand is a programmatic dependent of the shrink: it stages out and
+    // B while the shrink runs and reads y after the shrink grid completes.
+    cudaError_t e = lora::launch_bgmv_shrink(dtype, sa, *dev, cs, true);
+    if (e == cudaSuccess) e = lora::launch_bgmv_expand(dtype, ea, *dev, cs, true);
+    return e == cudaSuccess ? LORA_OK : cuda_fail(e, "bgmv shrink_expand_slice launch");
+}
 
 }  // extern "C"

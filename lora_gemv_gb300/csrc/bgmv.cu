@@ -1,0 +1,731 @@
+// Plan-free BGMV: shrink and expand_slice with the tokens in their natural
+// order, each token's adapter read straight from the index array.
+//
+// Pages: vLLM PR #15655 summary list (the LoRA kernel split into a shrink and
+// an expand variant; blocks without work skipped; a mask-free path when one
+// adapter serves every token); vLLM PR #11579 (bgmv_shrink and
+// bgmv_expand(_slice), the fp32 rank buffer between them, split-K shrink
+// whose partials are added, add_inputs); Punica issue #17 (BGMV: every input
+// may use its own adapter).
+//
+// Design (GB300).  For a decode batch served by a few adapters the grouping
+// step (a sort, then a plan read ahead of every operand) costs more than the
+// contraction itself.  These kernels skip it: a block of 128 consecutive
+// tokens (the MMA's M = 128 TMEM lanes) is contracted against every adapter's
+// weights at once on the tcgen05 tensor cores, and each token lane keeps its
+// own adapter's part.
+//  - shrink: D[128, rows] = X[128, H] . A[rows, H]^T, rows = the adapters'
+//    stacked A rows of this CTA's share (all adapters, a few, or a column
+//    range of one).  X and A are staged by TMA (128-byte swizzle) through a
+//    ring of stages fed by one producer thread, one thread issues the MMAs,
+//    and H is split over a thread-block cluster.  Each token lane reads its
+//    adapter's columns from TMEM and sends them to the CTA owning that token
+//    row (st.async into its shared memory, counted on its mbarrier); owners
+//    sum the cluster's partials in rank order (deterministic) and write y.
+//  - expand: out[128, cols] (+)= Y_ext . B_ext^T, where Y_ext[t] holds
+//    token t's y in its adapter's block of K = L * r (zeros elsewhere) and
+//    B_ext stacks the adapters' B rows along K.  Adapters without a token in
+//    the block are skipped (no loads, no MMA).  The out tile is staged by TMA
+//    before the kernel waits for the shrink; y enters the tensor cores as a
+//    hi + lo pair of the weight type after a per-row power-of-two scaling.
+// The extra tensor-core work (up to L times the grouped contraction) stays
+// far below the tensor ridge; what the design saves is the grouping launch
+// and a dependent plan read in every operator.
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+#include <type_traits>
+
+#include "common.cuh"
+#include "frag.cuh"
+#include "kernels.h"
+
+namespace lora {
+namespace {
+
+constexpr int kBT = 128;        // tokens per block: MMA M and TMEM lanes
+constexpr int kBThreads = 128;  // 4 warps, one TMEM lane quadrant each
+constexpr int kBox = 64;        // K elements (128 bytes) per TMA box row
+constexpr int kMaxStages = 4;
+constexpr int kMaxCw = 64;      // y columns one shrink CTA produces, at most
+constexpr int kShrinkSmemCap = 112 * 1024;  // keeps two shrink CTAs per SM
+
+// ------------------------------------------------------------------ tensor maps (host)
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+cudaError_t get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        g_encode_err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                        cudaEnableDefault, &q);
+        if (g_encode_err == cudaSuccess && (q != cudaDriverEntryPointSuccess || fn == nullptr))
+            g_encode_err = cudaErrorNotSupported;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode_err;
+}
+
+// 2-D fp16/bf16 tensor [rows][cols] with a row stride of `ld` elements, boxes
+// of box_rows x 64 columns in the 128-byte swizzled layout, zero fill outside.
+cudaError_t make_map(CUtensorMap *m, lora_dtype_t dt, const void *base, uint64_t rows,
+                     uint64_t cols, uint64_t ld, uint32_t box_rows) {
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {(cuuint32_t)kBox, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, dt == LORA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                             : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                          2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+
+// ------------------------------------------------------------------ shrink
+// One launch's split, chosen on the host.  CTA (kc, block, z): K range
+// [kc * kc_len, ...), tokens [128 * block, ...), and of the y columns the
+// adapters [l_first, l_first + zk) x columns [c0, c0 + cw) with
+// l_first = (z / zc) * zk and c0 = (z % zc) * cw: either whole adapters
+// (zc = 1, cw = W = S * R) or one adapter's column range (zk = 1).
+struct ShrinkSplit {
+    int kc_len;  // K elements per CTA, a multiple of 64
+    int nst;     // stages in the ring
+    int zk, zc, cw;
+    int n_mma;   // MMA N: A rows staged per stage (multiple of 16, <= 256)
+    int tcols;   // TMEM columns allocated
+};
+
+template <typename E>
+__global__ void __launch_bounds__(kBThreads)
+bgmv_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a,
+                   const BgmvShrinkArgs a, const ShrinkSplit p) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ uint64_t s_full[kMaxStages], s_empty[kMaxStages], s_done, s_recv;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_l[kBT];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kc = (int)cluster_rank(), C = gridDim.x;
+    const int t0 = blockIdx.y * kBT, z = blockIdx.z;
+    const int W = a.S * a.R;
+    const int l_first = (z / p.zc) * p.zk, c0 = (z % p.zc) * p.cw;
+    const int l_count = min(p.zk, a.L - l_first);
+    const int cw = min(p.cw, W - c0);  // a multiple of 8
+    const int r0 = l_first * W + c0;   // first A row (of [L * W, H])
+    const int k_begin = kc * p.kc_len;
+    const int nk = (min(a.H, k_begin + p.kc_len) - k_begin + kBox - 1) / kBox;  // >= 1
+    const int stage_bytes = kBT * 128 + p.n_mma * 128;
+    const int RPO = kBT / C;  // token rows each cluster CTA finishes
+    unsigned char *sm = smem + ((1024 - (smem_u32(smem) & 1023)) & 1023);
+    float *recv = reinterpret_cast<float *>(sm + p.nst * stage_bytes);  // [C][RPO][cw]
+
+    // x, the index array, A (and y with add_inputs) may come from the
+    // previous kernels; a dependent expand may launch now (it reads y only
+    // after its own wait, i.e. after this grid has completed).
+    grid_dep_wait();
+    grid_dep_launch();
+
+    const int t = t0 + tid;
+    int my_l = -1;
+    if (t < a.T) {
+        const int v = a.idx ? __ldg(a.idx + t) : 0;
+        if (v >= 0 && v < a.L) my_l = v;
+    }
+    s_l[tid] = my_l;
+    if (tid == 0) {
+        for (int i = 0; i < p.nst; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 1);
+        }
+        mbar_init(&s_done, 1);
+        mbar_init(&s_recv, 1);
+        tma_prefetch_map(&tm_x);
+        tma_prefetch_map(&tm_a);
+    }
+    if (warp == 0) tc_alloc(&s_tmem, p.tcols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    // receive barriers are initialised (fence in mbar_init) before any peer
+    // stores into them: the matching wait comes before the first send
+    cluster_arrive_relaxed();
+
+    bool timed_out = false;
+    if (tid == 0) {
+        // TMA producer: stage i = x[t0 .. +128, k .. k+64] and the A rows
+        for (int i = 0; i < nk; ++i) {
+            const int b = i % p.nst;
+            if (i >= p.nst && !mbar_wait_cta(&s_empty[b], ((i / p.nst) - 1) & 1)) {
+                timed_out = true;
+                break;
+            }
+            const uint32_t st = smem_u32(sm + b * stage_bytes);
+            mbar_arrive_expect_tx(&s_full[b], (uint32_t)stage_bytes);
+            tma_load_2d(st, &tm_x, k_begin + i * kBox, t0, &s_full[b]);
+            tma_load_2d(st + kBT * 128, &tm_a, k_begin + i * kBox, r0, &s_full[b]);
+        }
+    } else if (tid == 32) {
+        // MMA issuer: four K = 16 steps per stage into the TMEM accumulator
+        const uint32_t idesc = tc_idesc_f16(std::is_same<E, __nv_bfloat16>::value, kBT, p.n_mma);
+        for (int i = 0; i < nk; ++i) {
+            const int b = i % p.nst;
+            if (!mbar_wait_cta(&s_full[b], (i / p.nst) & 1)) {
+                timed_out = true;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t xs = smem_u32(sm + b * stage_bytes), as = xs + kBT * 128;
+#pragma unroll
+            for (int k = 0; k < kBox / 16; ++k)
+                tc_mma_f16(tmem, tc_desc_sw128(xs + 32 * k), tc_desc_sw128(as + 32 * k), idesc,
+                           i > 0 || k > 0);
+            tc_commit(&s_empty[b]);
+        }
+        tc_commit(&s_done);  // arrives once every MMA issued above is complete
+    }
+    __syncwarp();
+    if (!mbar_wait_cta(&s_done, 0)) timed_out = true;
+    __syncwarp();
+    tc_fence_after();
+
+    // This lane's token: its adapter's columns of this CTA's share, 32 at a
+    // time, to the CTA that finishes its row.
+    const int nvalid = min(kBT, a.T - t0);
+    const int li = (my_l >= l_first && my_l < l_first + l_count) ? my_l - l_first : -1;
+    const int owner = tid / RPO, orow = tid - owner * RPO;
+    const int nown = max(0, min(RPO, nvalid - kc * RPO));
+    const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+    cluster_wait();
+    if (tid == 0) mbar_arrive_expect_tx(&s_recv, (uint32_t)(C * nown * cw * 4));
+    const uint32_t dst = cluster_map(smem_u32(recv), (uint32_t)owner) +
+                         (uint32_t)((kc * RPO + orow) * cw * 4);
+    const uint32_t dst_bar = cluster_map(smem_u32(&s_recv), (uint32_t)owner);
+    for (int j0 = 0; j0 < cw; j0 += 32) {  // block-uniform
+        float v[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) v[r] = 0.f;
+        for (int q = 0; q < l_count; ++q) {  // block-uniform
+            float d[32];
+            tc_ld32(taddr + (uint32_t)(q * W + j0), d);
+            if (q == li) {
+#pragma unroll
+                for (int r = 0; r < 32; ++r) v[r] = d[r];
+            }
+        }
+        if (tid < nvalid) {
+            const int nj = min(32, cw - j0);
+#pragma unroll
+            for (int r = 0; r < 32; r += 4)
+                if (r < nj)
+                    st_async_v4(dst + (uint32_t)((j0 + r) * 4),
+                                make_float4(v[r], v[r + 1], v[r + 2], v[r + 3]), dst_bar);
+        }
+    }
+    // my rows: the cluster's partials summed in rank order, then y
+    if (!mbar_wait_cluster(&s_recv, 0)) timed_out = true;
+    __syncwarp();
+    for (int it = tid; it < nown * cw; it += kBThreads) {
+        const int r = it / cw, j = it - r * cw;
+        const int trow = kc * RPO + r;
+        const int tl = s_l[trow];
+        float sum = 0.f;
+        for (int q = 0; q < C; ++q) sum += recv[(q * RPO + r) * cw + j];
+        const int col = c0 + j;
+        float val = 0.f;
+        bool write;
+        if (tl >= l_first && tl < l_first + l_count) {
+            write = true;
+            if (col % a.R < clamp_rank(a.ranks, tl, a.R)) val = a.scale * sum;
+        } else {
+            // tokens without an adapter: zeros, written by the CTAs holding adapter 0's columns
+            write = tl < 0 && l_first == 0 && !a.add;
+        }
+        if (write) {
+            float *yp = a.y + (int64_t)(t0 + trow) * a.ldy + col;
+            *yp = a.add ? *yp + val : val;
+        }
+    }
+    if (timed_out && a.status) atomicOr(a.status, LORA_PLANERR_TIMEOUT);
+    // no CTA leaves while a peer may still store into its receive buffer
+    __syncwarp();
+    cluster_arrive();
+    cluster_wait();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tc_dealloc(tmem, p.tcols);
+    }
+}
+
+// Stand-in with the shrink's block size, for the cluster-capacity queries.
+__global__ void __launch_bounds__(kBThreads) bgmv_capacity_probe() {}
+
+// ------------------------------------------------------------------ expand
+// Shared memory: the out tile (add_inputs; nc / 64 TMA boxes of 128 rows x
+// 128 bytes), B_ext [kgroups][nc rows][128 B], Y_ext hi and lo
+// [kgroups][128 rows][128 B]; 128-byte swizzled K-major, 1024-byte aligned.
+__host__ __device__ constexpr int expand_smem_bytes(int nc, int kgroups, bool add) {
+    return 1024 + (add ? nc * kBT * 2 : 0) + kgroups * nc * 128 + 2 * kgroups * kBT * 128;
+}
+
+// KSY: 16-wide K steps per adapter (ranks padded to RP = 16 * KSY).
+template <typename E, bool ADD, int KSY>
+__global__ void __launch_bounds__(kBThreads)
+bgmv_expand_kernel(const __grid_constant__ CUtensorMap tm_out, const BgmvExpandArgs a, int nc,
+                   int kgroups) {
+    constexpr int RP = 16 * KSY;
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ uint64_t s_bar_out, s_bar_mma;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_present;  // bit l: adapter l has a token (of nonzero rank) in this block
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int t0 = blockIdx.x * kBT, chunk = blockIdx.y;
+    const int t = t0 + tid;
+    int s = 0;
+    while (s + 1 < a.num_slices && chunk >= a.chunk_begin[s + 1]) ++s;
+    const int Ns = a.N[s];
+    const int n0 = (chunk - a.chunk_begin[s]) * nc;
+    const int ncols = min(nc, Ns - n0);  // > 0, a multiple of 8
+    const int64_t col0 = (int64_t)a.off[s] + n0;
+    const int R = a.R;
+    E *__restrict__ out = static_cast<E *>(a.out);
+    unsigned char *sm = smem + ((1024 - (smem_u32(smem) & 1023)) & 1023);
+    unsigned char *sOut = sm;
+    unsigned char *sB = sOut + (ADD ? nc * kBT * 2 : 0);
+    unsigned char *sYh = sB + kgroups * nc * 128;
+    unsigned char *sYl = sYh + kgroups * kBT * 128;
+
+    if (tid == 0) {
+        s_present = 0;
+        mbar_init(&s_bar_out, 1);
+        mbar_init(&s_bar_mma, 1);
+        if (ADD) tma_prefetch_map(&tm_out);
+    }
+    // this thread's token and adapter (the index array is an input of the
+    // pair: it is read before the wait for the previous kernel)
+    int l = -1, rl = 0;
+    if (t < a.T) {
+        const int v = a.idx ? __ldg(a.idx + t) : 0;
+        if (v >= 0 && v < a.L) {
+            rl = clamp_rank(a.ranks, v, R);
+            if (rl > 0) l = v;
+        }
+    }
+    __syncthreads();
+    if (l >= 0) atomicOr(&s_present, 1 << l);
+    __syncthreads();
+    const int present = s_present;
+    if (present == 0) {  // no LoRA term in this block: untouched with add_inputs, zeros without
+        if (!ADD && t < a.T)
+            for (int c = 0; c < ncols; c += 8)
+                st_global_v4(out + (int64_t)t * a.ldo + col0 + c, make_uint4(0, 0, 0, 0));
+        return;
+    }
+    // out tile (add_inputs) by TMA; rows past T are zero-filled and never stored
+    if (ADD && tid == 0) {
+        const int nbox = (ncols + kBox - 1) / kBox;
+        mbar_arrive_expect_tx(&s_bar_out, (uint32_t)(nbox * kBT * 128));
+        for (int i = 0; i < nbox; ++i)
+            tma_load_2d(smem_u32(sOut + i * kBT * 128), &tm_out, (int)(col0 + i * kBox), t0,
+                        &s_bar_out);
+    }
+    // B_ext: adapter lb's ranks at K positions [lb * RP, lb * RP + RP), 8 per
+    // 16-byte piece, ranks >= r_lb and rows past the slice zero-filled;
+    // adapters without a token here are neither loaded nor multiplied
+    {
+        const E *Bs = static_cast<const E *>(a.B[s]);
+        const int per_row = kgroups * 8;
+        for (int it = tid; it < nc * per_row; it += kBThreads) {
+            const int n = it / per_row, c = it - n * per_row;
+            const int lb = (8 * c) / RP, k = 8 * c - lb * RP;
+            if (lb >= a.L || !((present >> lb) & 1)) continue;
+            const int nv = n < ncols ? min(8, clamp_rank(a.ranks, lb, R) - k) : 0;
+            const E *src = nv > 0 ? Bs + ((int64_t)lb * Ns + n0 + n) * R + k : Bs;
+            cp_async16(smem_u32(sB + (c >> 3) * nc * 128 + n * 128 + (((c & 7) ^ (n & 7)) << 4)),
+                       src, nv > 0 ? 2 * nv : 0);
+        }
+        cp_async_commit();
+    }
+
+    // y comes from the previous kernel (the shrink).  Tensor memory is taken
+    // only after this wait: a CTA holding TMEM never waits on another grid.
+    grid_dep_wait();
+    grid_dep_launch();
+    if (tid < 32) tc_alloc(&s_tmem, (uint32_t)nc);
+
+    // Y_ext rows of this thread's token: its y as a hi/lo pair scaled by 2^-e
+    // in its adapter's K block, zeros elsewhere
+    float f = 0.f;
+    {
+        float yv[RP];
+#pragma unroll
+        for (int k = 0; k < RP; ++k) yv[k] = 0.f;
+        if (l >= 0) {
+            const float *yr = a.y + (int64_t)t * a.ldy + (int64_t)s * a.y_slice_stride;
+#pragma unroll
+            for (int k = 0; k < RP; k += 4)
+                if (k < rl) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(yr + k));
+                    yv[k] = v.x;
+                    yv[k + 1] = v.y;
+                    yv[k + 2] = v.z;
+                    yv[k + 3] = v.w;
+                }
+            float m = 0.f;
+#pragma unroll
+            for (int k = 0; k < RP; ++k) {
+                if (k >= rl) yv[k] = 0.f;
+                m = fmaxf(m, fabsf(yv[k]));
+            }
+            const int e = row_exponent(m);
+            f = a.scale * exp2i(e);
+            const float inv = exp2i(-e);
+#pragma unroll
+            for (int k = 0; k < RP; ++k) yv[k] *= inv;
+        }
+        const int cl0 = l >= 0 ? l * (RP / 8) : -RP;  // first 16-byte piece of the adapter's block
+        const int rowoff = tid * 128;
+        for (int c = 0; c < kgroups * 8; ++c) {
+            if (c >= cl0 && c < cl0 + RP / 8) continue;
+            const int off = (c >> 3) * kBT * 128 + rowoff + (((c & 7) ^ (tid & 7)) << 4);
+            *reinterpret_cast<uint4 *>(sYh + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(sYl + off) = make_uint4(0, 0, 0, 0);
+        }
+        if (l >= 0) {
+#pragma unroll
+            for (int j = 0; j < RP / 8; ++j) {
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) v[q] = yv[8 * j + q];
+                uint4 hi, lo;
+                split_hilo8<E>(v, hi, lo);
+                const int c = cl0 + j;
+                const int off = (c >> 3) * kBT * 128 + rowoff + (((c & 7) ^ (tid & 7)) << 4);
+                *reinterpret_cast<uint4 *>(sYh + off) = hi;
+                *reinterpret_cast<uint4 *>(sYl + off) = lo;
+            }
+        }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();  // Y (plain stores) and B (cp.async) -> tensor-core operand reads
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    if (tid == 0) {
+        const uint32_t idesc = tc_idesc_f16(std::is_same<E, __nv_bfloat16>::value, kBT, nc);
+        bool acc = false;
+        for (int lb = 0; lb < a.L; ++lb) {
+            if (!((present >> lb) & 1)) continue;
+#pragma unroll
+            for (int ks = 0; ks < KSY; ++ks) {
+                const int kpos = lb * RP + 16 * ks;
+                const uint32_t g = (uint32_t)(kpos >> 6), kb = (uint32_t)((kpos & 63) * 2);
+                const uint32_t yh = smem_u32(sYh) + g * kBT * 128 + kb;
+                const uint32_t yl = smem_u32(sYl) + g * kBT * 128 + kb;
+                const uint32_t bb = smem_u32(sB) + g * (uint32_t)nc * 128 + kb;
+                tc_mma_f16(tmem, tc_desc_sw128(yh), tc_desc_sw128(bb), idesc, acc);
+                tc_mma_f16(tmem, tc_desc_sw128(yl), tc_desc_sw128(bb), idesc, true);
+                acc = true;
+            }
+        }
+        tc_commit(&s_bar_mma);
+    }
+    bool to = !mbar_wait_cta(&s_bar_mma, 0);
+    if (ADD && !mbar_wait_cta(&s_bar_out, 0)) to = true;
+    const bool any_to = __syncthreads_or(to);  // also reconverges the warps
+    if (any_to) {
+        // never expected: flag it and leave out untouched
+        if (tid == 0 && a.status) atomicOr(a.status, LORA_PLANERR_TIMEOUT);
+        mbar_wait_cta(&s_bar_mma, 0);
+        if (ADD) mbar_wait_cta(&s_bar_out, 0);
+    } else {
+        tc_fence_after();
+        // rows with a LoRA term; without add_inputs every token row (zeros for the others)
+        const bool live = t < a.T && (l >= 0 || !ADD);
+        const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+        E *orow = out + (int64_t)t * a.ldo + col0;
+        for (int cc = 0; cc < ncols; cc += 32) {  // block-uniform
+            float d[32];
+            tc_ld32(taddr + (uint32_t)cc, d);
+            if (!live) continue;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const int c = cc + 8 * g;
+                if (c >= ncols) break;
+                float v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = f * d[8 * g + k];
+                if (ADD) {
+                    const int piece = (c & 63) >> 3;
+                    float o[8];
+                    unpack8<E>(*reinterpret_cast<const uint4 *>(
+                                   sOut + (c >> 6) * kBT * 128 + tid * 128 + ((piece ^ (tid & 7)) << 4)),
+                               o);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) v[k] += o[k];
+                }
+                st_global_v4(orow + c, pack8<E>(v));
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tc_dealloc(tmem, (uint32_t)nc);
+    }
+}
+
+using ExpandFn = void (*)(const CUtensorMap, const BgmvExpandArgs, int, int);
+template <typename E, bool ADD>
+ExpandFn expand_fn(int ksy) {
+    switch (ksy) {
+        case 1: return bgmv_expand_kernel<E, ADD, 1>;
+        case 2: return bgmv_expand_kernel<E, ADD, 2>;
+        case 3: return bgmv_expand_kernel<E, ADD, 3>;
+        default: return bgmv_expand_kernel<E, ADD, 4>;
+    }
+}
+ExpandFn expand_fn(int dt, bool add, int ksy) {
+    if (dt == LORA_F16) return add ? expand_fn<__half, true>(ksy) : expand_fn<__half, false>(ksy);
+    return add ? expand_fn<__nv_bfloat16, true>(ksy) : expand_fn<__nv_bfloat16, false>(ksy);
+}
+
+using ShrinkFn = void (*)(const CUtensorMap, const CUtensorMap, const BgmvShrinkArgs, const ShrinkSplit);
+ShrinkFn shrink_fn(int dt) {
+    return dt == LORA_F16 ? bgmv_shrink_kernel<__half> : bgmv_shrink_kernel<__nv_bfloat16>;
+}
+
+// Cluster capacity: CTAs of clusters of 1, 2, 4, 8, 16 resident at once,
+// [two per SM (<= kShrinkSmemCap of shared memory) or one][log2 cluster].
+int g_cluster_ctas[2][5] = {};
+int g_sm_count = 0;
+int g_smem_sm = 0, g_smem_reserved = 0, g_shrink_static = 0;
+
+// Dynamic shared memory of a shrink CTA, raised where needed so that the
+// CTAs one SM holds never ask for more than its 512 TMEM columns together: a
+// CTA waiting in tcgen05.alloc could otherwise hold up a cluster peer that
+// itself holds columns.
+int shrink_smem_for_tmem(int dyn, int tcols) {
+    const int max_ctas = 512 / tcols;
+    const int per_cta = g_smem_sm / (max_ctas + 1) + 1;  // more than this fits max_ctas at most
+    return std::max(dyn, per_cta - g_shrink_static - g_smem_reserved);
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+cudaError_t configure_bgmv_kernels(const DeviceInfo &dev) {
+    g_sm_count = dev.sm_count;
+    int devid = 0;
+    cudaError_t e = cudaGetDevice(&devid);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&g_smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, devid);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&g_smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, devid);
+    int optin = 0;
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, devid);
+    if (e == cudaSuccess) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, shrink_fn(LORA_BF16));
+        g_shrink_static = (int)fa.sharedSizeBytes;
+    }
+    // dynamic shared memory allowed per block: the opt-in limit less static use
+    const int big = optin - g_shrink_static;
+    for (int dt = 0; dt < 2 && e == cudaSuccess; ++dt) {
+        e = cudaFuncSetAttribute(shrink_fn(dt), cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+        if (e == cudaSuccess && dev.max_cluster > 8)
+            e = cudaFuncSetAttribute(shrink_fn(dt), cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        for (int add = 0; add < 2 && e == cudaSuccess; ++add)
+            for (int ksy = 1; ksy <= 4 && e == cudaSuccess; ++ksy)
+                e = cudaFuncSetAttribute(expand_fn(dt, add != 0, ksy),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         expand_smem_bytes(128, 2, true));
+    }
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(bgmv_capacity_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess && dev.max_cluster > 8)
+        e = cudaFuncSetAttribute(bgmv_capacity_probe, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (int two = 0; two < 2 && e == cudaSuccess; ++two) {
+        for (int lc = 0; lc < 5 && e == cudaSuccess; ++lc) {
+            const int C = 1 << lc;
+            if (C > dev.max_cluster) break;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(C, 1, 1);
+            cfg.blockDim = dim3(kBThreads);
+            cfg.dynamicSmemBytes = two ? kShrinkSmemCap - 8 * 1024 : big - 8 * 1024;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = C;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, bgmv_capacity_probe, &cfg);
+            g_cluster_ctas[two][lc] = n * C;
+        }
+    }
+    return e;
+}
+
+const char *bgmv_shrink_supported(const BgmvShrinkArgs &a) {
+    const int W = a.S * a.R;
+    if (!aligned16(a.x) || a.ldx % 8 != 0) return "x must be 16-byte aligned with ldx a multiple of 8";
+    if (!aligned16(a.A) || a.H % 8 != 0) return "A must be 16-byte aligned with H a multiple of 8";
+    if (W % 8 != 0) return "num_slices * R must be a multiple of 8";
+    return nullptr;
+}
+
+const char *bgmv_expand_supported(const BgmvExpandArgs &a) {
+    const int RP = (a.R + 15) / 16 * 16;
+    if (a.R % 8 != 0) return "R must be a multiple of 8";
+    if (RP > 64) return "R above 64 (use the grouped operators)";
+    if (a.L * RP > 128) return "L * R (ranks padded to 16) above 128 (use the grouped operators)";
+    if (!aligned16(a.y) || a.ldy % 4 != 0 || a.y_slice_stride % 4 != 0)
+        return "y must be 16-byte aligned with ldy and y_slice_stride multiples of 4";
+    if (!aligned16(a.out) || a.ldo % 8 != 0) return "out must be 16-byte aligned with ldo a multiple of 8";
+    for (int s = 0; s < a.num_slices; ++s)
+        if (a.N[s] > 0 && (a.N[s] % 8 != 0 || a.off[s] % 8 != 0 || !aligned16(a.B[s])))
+            return "slice widths and offsets must be multiples of 8, B_s 16-byte aligned";
+    return nullptr;
+}
+
+cudaError_t launch_bgmv_shrink(lora_dtype_t dt, const BgmvShrinkArgs &a, const DeviceInfo &dev,
+                               cudaStream_t stream, bool pdl) {
+    if (a.T == 0) return cudaSuccess;
+    const int W = a.S * a.R;
+    const int blocks = (a.T + kBT - 1) / kBT;
+    // K split over a cluster: the largest power of two leaving >= 128 K per CTA
+    int C = 1;
+    while (2 * C <= dev.max_cluster && a.H / (2 * C) >= 2 * kBox) C *= 2;
+    int kc_len = ((a.H + C - 1) / C + kBox - 1) / kBox * kBox;
+    while (C > 1 && (long long)(C - 1) * kc_len >= a.H) {  // every CTA gets some K
+        C /= 2;
+        kc_len = ((a.H + C - 1) / C + kBox - 1) / kBox * kBox;
+    }
+    int lc = 0;
+    while ((1 << lc) < C) ++lc;
+    // Shares of the y columns, coarse to fine: whole adapters (zk of them,
+    // N = zk * W <= 256), then column ranges of one adapter.  Take the
+    // finest share whose grid is still resident in one wave of clusters.
+    struct Cand {
+        int zk, zc, cw, Z;
+    } cands[24];
+    int nc = 0;
+    if (W <= kMaxCw) {
+        for (int zk = a.L; zk >= 1; zk = zk > 1 ? (zk + 1) / 2 : 0) {
+            if ((zk > 1 && W % 16 != 0) || (zk * W + 15) / 16 * 16 > 256 ||
+                (zk - 1) * W + (W + 31) / 32 * 32 > 256) {
+                if (zk == 1) break;
+                continue;
+            }
+            cands[nc++] = {zk, 1, W, (a.L + zk - 1) / zk};
+            if (zk == 1) break;
+        }
+    }
+    for (int cw = kMaxCw; cw >= 16 && nc < 24; cw /= 2)
+        if (cw < W) cands[nc++] = {1, (W + cw - 1) / cw, cw, a.L * ((W + cw - 1) / cw)};
+    if (nc == 0) return cudaErrorInvalidValue;  // unreachable: W % 8 == 0 gives a column share
+    int pick = 0;
+    const long long cap = std::max(1, g_cluster_ctas[1][lc]);
+    for (int i = 0; i < nc; ++i)
+        if ((long long)blocks * C * cands[i].Z <= cap && cands[i].Z <= 65535) pick = i;
+    ShrinkSplit p{};
+    p.kc_len = kc_len;
+    p.zk = cands[pick].zk;
+    p.zc = cands[pick].zc;
+    p.cw = cands[pick].cw;
+    p.n_mma = ((p.zk - 1) * W + p.cw + 15) / 16 * 16;
+    const int tneed = (p.zk - 1) * W + (p.cw + 31) / 32 * 32;
+    p.tcols = 32;
+    while ((int)p.tcols < tneed) p.tcols *= 2;
+    const int nk = (kc_len + kBox - 1) / kBox;
+    const int stage = kBT * 128 + p.n_mma * 128, recv = kBT * p.cw * 4;
+    const int fit = (kShrinkSmemCap - 1024 - recv) / stage;
+    p.nst = std::max(2, std::min({fit, kMaxStages, nk}));
+    if (nk == 1) p.nst = 1;
+
+    CUtensorMap tx, ta;
+    cudaError_t e = make_map(&tx, dt, a.x, (uint64_t)a.T, (uint64_t)a.H, (uint64_t)a.ldx, kBT);
+    if (e == cudaSuccess)
+        e = make_map(&ta, dt, a.A, (uint64_t)a.L * W, (uint64_t)a.H, (uint64_t)a.H, (uint32_t)p.n_mma);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C, blocks, cands[pick].Z);
+    cfg.blockDim = dim3(kBThreads);
+    cfg.dynamicSmemBytes = shrink_smem_for_tmem(1024 + p.nst * stage + recv, p.tcols);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, shrink_fn(dt), tx, ta, a, p);
+}
+
+cudaError_t launch_bgmv_expand(lora_dtype_t dt, const BgmvExpandArgs &a_in, const DeviceInfo &dev,
+                               cudaStream_t stream, bool pdl) {
+    BgmvExpandArgs a = a_in;
+    if (a.T == 0) return cudaSuccess;
+    const int RP = (a.R + 15) / 16 * 16;
+    const int kgroups = (a.L * RP + 63) / 64;
+    const int blocks = (a.T + kBT - 1) / kBT;
+    auto chunks = [&](int nc) {
+        long long n = 0;
+        for (int s = 0; s < a.num_slices; ++s) n += (a.N[s] + nc - 1) / nc;
+        return n;
+    };
+    // 128 output columns per CTA; 64 when that leaves under two CTAs per SM
+    int nc = 128;
+    if ((long long)blocks * chunks(128) < 2LL * dev.sm_count) nc = 64;
+    a.chunk_begin[0] = 0;
+    for (int s = 0; s < a.num_slices; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s] + (a.N[s] + nc - 1) / nc;
+    for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s];
+    const int total = a.chunk_begin[a.num_slices];
+    if (total == 0) return cudaSuccess;
+    if (total > 65535) return cudaErrorInvalidConfiguration;
+    CUtensorMap tm;
+    memset(&tm, 0, sizeof(tm));
+    if (a.add) {
+        int used = 0;
+        for (int s = 0; s < a.num_slices; ++s)
+            if (a.N[s] > 0) used = std::max(used, a.off[s] + a.N[s]);
+        cudaError_t e = make_map(&tm, dt, a.out, (uint64_t)a.T, (uint64_t)used, (uint64_t)a.ldo, kBT);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks, total);
+    cfg.blockDim = dim3(kBThreads);
+    cfg.dynamicSmemBytes = expand_smem_bytes(nc, kgroups, a.add != 0);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, expand_fn(dt, a.add != 0, RP / 16), tm, a, nc, kgroups);
+}
+
+}  // namespace lora

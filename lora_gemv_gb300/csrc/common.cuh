@@ -1,6 +1,7 @@
 // Device helpers shared by the plan, shrink and expand kernels (sm_103a).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -278,6 +279,26 @@ __device__ __forceinline__ bool mbar_wait_cta(uint64_t *bar, uint32_t parity) {
         if (ok) return true;
     }
     return false;
+}
+
+// ------------------------------------------------------------------ TMA
+// Tiled 2-D tensor copy global -> this CTA's shared memory (cp.async.bulk.tensor):
+// the box at (x = innermost element index, y = row) of the tensor map `map`
+// (a __grid_constant__ kernel parameter) lands at `dst` in the map's swizzled
+// layout; its bytes are counted on this CTA's mbarrier `bar`.  Elements
+// outside the tensor are filled with zeros (and still counted).  x times the
+// element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+// Starts fetching a tensor map (kernel parameter) into the descriptor cache.
+__device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // Programmatic dependent launch: wait for the previous grid's results; let

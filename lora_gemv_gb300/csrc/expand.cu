@@ -41,43 +41,6 @@ __device__ __forceinline__ int sigma(int j) {
     return (j & ~31) + 8 * ((j >> 1) & 3) + 2 * ((j >> 3) & 3) + (j & 1);
 }
 
-template <typename E>
-__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
-    uint4 r;
-    uint32_t *w = reinterpret_cast<uint32_t *>(&r);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        E lo = Elem<E>::from_f(v[2 * k]), hi = Elem<E>::from_f(v[2 * k + 1]);
-        w[k] = (uint32_t)(*reinterpret_cast<uint16_t *>(&lo)) |
-               ((uint32_t)(*reinterpret_cast<uint16_t *>(&hi)) << 16);
-    }
-    return r;
-}
-
-template <typename E>
-__device__ __forceinline__ void unpack8(uint4 r, float (&v)[8]) {
-    const uint32_t *w = reinterpret_cast<const uint32_t *>(&r);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        uint16_t lo = (uint16_t)(w[k] & 0xffffu), hi = (uint16_t)(w[k] >> 16);
-        v[2 * k] = Elem<E>::to_f(*reinterpret_cast<E *>(&lo));
-        v[2 * k + 1] = Elem<E>::to_f(*reinterpret_cast<E *>(&hi));
-    }
-}
-
-// v = hi + lo with hi = round(v) and lo = round(v - hi) in the weight type.
-template <typename E>
-__device__ __forceinline__ void split_hilo8(const float (&v)[8], uint4 &hi, uint4 &lo) {
-    float h[8], l[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        h[k] = Elem<E>::to_f(Elem<E>::from_f(v[k]));
-        l[k] = v[k] - h[k];
-    }
-    hi = pack8<E>(h);
-    lo = pack8<E>(l);
-}
-
 template <typename E, bool ADD, bool VEC>
 __global__ void __launch_bounds__(kThreads)
 expand_kernel(const ExpandArgs a) {

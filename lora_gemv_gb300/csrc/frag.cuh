@@ -32,6 +32,44 @@ template <> struct Pack<__nv_bfloat16> {
     }
 };
 
+// Eight floats <-> eight fp16/bf16 values in one 16-byte word (round to nearest even).
+template <typename E>
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+    uint4 r;
+    uint32_t *w = reinterpret_cast<uint32_t *>(&r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        E lo = Elem<E>::from_f(v[2 * k]), hi = Elem<E>::from_f(v[2 * k + 1]);
+        w[k] = (uint32_t)(*reinterpret_cast<uint16_t *>(&lo)) |
+               ((uint32_t)(*reinterpret_cast<uint16_t *>(&hi)) << 16);
+    }
+    return r;
+}
+
+template <typename E>
+__device__ __forceinline__ void unpack8(uint4 r, float (&v)[8]) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(&r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        uint16_t lo = (uint16_t)(w[k] & 0xffffu), hi = (uint16_t)(w[k] >> 16);
+        v[2 * k] = Elem<E>::to_f(*reinterpret_cast<E *>(&lo));
+        v[2 * k + 1] = Elem<E>::to_f(*reinterpret_cast<E *>(&hi));
+    }
+}
+
+// v = hi + lo with hi = round(v) and lo = round(v - hi) in the weight type.
+template <typename E>
+__device__ __forceinline__ void split_hilo8(const float (&v)[8], uint4 &hi, uint4 &lo) {
+    float h[8], l[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        h[k] = Elem<E>::to_f(Elem<E>::from_f(v[k]));
+        l[k] = v[k] - h[k];
+    }
+    hi = pack8<E>(h);
+    lo = pack8<E>(l);
+}
+
 // Power-of-two factor 2^k as a float, k in [-126, 127].
 __device__ __forceinline__ float exp2i(int k) { return __int_as_float((127 + k) << 23); }
 

@@ -56,12 +56,50 @@ struct ExpandArgs {
     int max_tiles;
 };
 
+// Plan-free BGMV (tokens in their natural order; every token's adapter read
+// straight from the index array, or adapter 0 for all when idx is NULL).
+struct BgmvShrinkArgs {
+    const void *x;
+    int64_t ldx;
+    int T, H;
+    const void *A;          // [L, S*R, H]
+    int L, R, S;
+    const int32_t *idx;     // [T] or NULL (every token uses adapter 0)
+    const int32_t *ranks;   // [L] or NULL
+    float *y;
+    int64_t ldy;
+    float scale;
+    int add;
+    int32_t *status;        // optional device word: LORA_PLANERR_TIMEOUT is OR-ed in
+};
+
+struct BgmvExpandArgs {
+    const float *y;
+    int64_t ldy;
+    int T;
+    const int32_t *idx;
+    const int32_t *ranks;
+    int L, R;
+    int y_slice_stride;
+    float scale;
+    int add;
+    int num_slices;
+    const void *B[LORA_MAX_SLICES];
+    int N[LORA_MAX_SLICES];
+    int off[LORA_MAX_SLICES];
+    int chunk_begin[LORA_MAX_SLICES + 1];  // first column chunk of each slice (set by the launcher)
+    void *out;
+    int64_t ldo;
+    int32_t *status;
+};
+
 struct DeviceInfo {
     int sm_count;
     int max_cluster;  // largest split-K cluster the shrink kernel can be launched with
 };
 
 cudaError_t configure_plan_kernels();
+cudaError_t configure_bgmv_kernels(const DeviceInfo &dev);
 cudaError_t configure_shrink_kernels(DeviceInfo *info);
 cudaError_t configure_expand_kernels();
 
@@ -76,6 +114,15 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
                           cudaStream_t stream, bool pdl = false);
 cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a, const DeviceInfo &dev,
                           cudaStream_t stream, bool pdl = false);
+
+// Plan-free BGMV launches.  The *_supported checks return nullptr when the
+// shape is taken, else a short reason (the caller reports LORA_ERR_UNSUPPORTED).
+const char *bgmv_shrink_supported(const BgmvShrinkArgs &a);
+const char *bgmv_expand_supported(const BgmvExpandArgs &a);
+cudaError_t launch_bgmv_shrink(lora_dtype_t dt, const BgmvShrinkArgs &a, const DeviceInfo &dev,
+                               cudaStream_t stream, bool pdl = false);
+cudaError_t launch_bgmv_expand(lora_dtype_t dt, const BgmvExpandArgs &a, const DeviceInfo &dev,
+                               cudaStream_t stream, bool pdl = false);
 
 // Host-side argument checks of the C ABI (api.cu): LORA_OK or the status the
 // operator would return, with lora_last_error_detail() set.

@@ -118,6 +118,10 @@ def f64(t: torch.Tensor) -> np.ndarray:
 
 
 def oracle_map(case):
+    """(adapter per token, bad-id count, segment error bits) of a case; a case
+    with neither token indices nor segments has every token on adapter 0."""
+    if case.token_idx is None and case.seg_start is None:
+        return oracle.map_tokens(np.zeros(case.T, np.int32), case.L) + (0,)
     if case.token_idx is not None:
         lo, bad = oracle.map_tokens(case.token_idx.numpy(), case.L)
         return lo, bad, 0
