@@ -287,6 +287,11 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
  *           multiples of 8, every B_s 16-byte aligned.
  * With a rank table, rows / columns >= r_l are never used in the result (the
  * shrink reads A rows up to R and discards the extra products).
+ * The expand writes out back in 64-column tiles of 128 token rows: with
+ * add_inputs, the rows of tokens without a LoRA term are rewritten with the
+ * values just read (their contents do not change, but out must not be
+ * written concurrently by other work); without add_inputs they become zero.
+ * Columns outside the slices are never written.
  * Errors: as the grouped operators (no plan argument), plus
  * LORA_ERR_UNSUPPORTED for shapes outside the list above.
  */

@@ -116,7 +116,7 @@ bgmv_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     __shared__ uint64_t s_full[kMaxStages], s_empty[kMaxStages], s_done, s_recv;
     __shared__ uint32_t s_tmem;
     __shared__ int s_l[kBT];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     const int kc = (int)cluster_rank(), C = gridDim.x;
     const int t0 = blockIdx.y * kBT, z = blockIdx.z;
     const int W = a.S * a.R;
@@ -137,13 +137,17 @@ bgmv_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
     grid_dep_wait();
     grid_dep_launch();
 
-    const int t = t0 + tid;
-    int my_l = -1;
-    if (t < a.T) {
-        const int v = a.idx ? __ldg(a.idx + t) : 0;
-        if (v >= 0 && v < a.L) my_l = v;
-    }
-    s_l[tid] = my_l;
+    // The first stages go out before anything else: their loads do not
+    // depend on the token indices.
+    const uint32_t sm_base = smem_u32(sm);
+#define BGMV_ISSUE_STAGE(i)                                                                 \
+    do {                                                                                    \
+        const int b_ = (i) % p.nst;                                                         \
+        const uint32_t st_ = sm_base + (uint32_t)(b_ * stage_bytes);                        \
+        mbar_arrive_expect_tx(&s_full[b_], (uint32_t)stage_bytes);                          \
+        tma_load_2d(st_, &tm_x, k_begin + (i) * kBox, t0, &s_full[b_]);                     \
+        tma_load_2d(st_ + kBT * 128, &tm_a, k_begin + (i) * kBox, r0, &s_full[b_]);         \
+    } while (0)
     if (tid == 0) {
         for (int i = 0; i < p.nst; ++i) {
             mbar_init(&s_full[i], 1);
@@ -151,9 +155,16 @@ bgmv_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         }
         mbar_init(&s_done, 1);
         mbar_init(&s_recv, 1);
-        tma_prefetch_map(&tm_x);
-        tma_prefetch_map(&tm_a);
+        for (int i = 0; i < min(p.nst, nk); ++i) BGMV_ISSUE_STAGE(i);
     }
+    const int t = t0 + tid;
+    int my_l = -1;
+    if (t < a.T) {
+        const int v = a.idx ? __ldg(a.idx + t) : 0;
+        if (v >= 0 && v < a.L) my_l = v;
+    }
+    s_l[tid] = my_l;
+    __syncwarp();
     if (warp == 0) tc_alloc(&s_tmem, p.tcols);
     tc_fence_before();
     __syncthreads();
@@ -165,17 +176,14 @@ bgmv_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
 
     bool timed_out = false;
     if (tid == 0) {
-        // TMA producer: stage i = x[t0 .. +128, k .. k+64] and the A rows
-        for (int i = 0; i < nk; ++i) {
-            const int b = i % p.nst;
-            if (i >= p.nst && !mbar_wait_cta(&s_empty[b], ((i / p.nst) - 1) & 1)) {
+        // TMA producer: stage i = x[t0 .. +128, k .. k+64] and the A rows;
+        // stages past the ring's depth wait for the MMAs that read their buffer
+        for (int i = p.nst; i < nk; ++i) {
+            if (!mbar_wait_cta(&s_empty[i % p.nst], ((i / p.nst) - 1) & 1)) {
                 timed_out = true;
                 break;
             }
-            const uint32_t st = smem_u32(sm + b * stage_bytes);
-            mbar_arrive_expect_tx(&s_full[b], (uint32_t)stage_bytes);
-            tma_load_2d(st, &tm_x, k_begin + i * kBox, t0, &s_full[b]);
-            tma_load_2d(st + kBT * 128, &tm_a, k_begin + i * kBox, r0, &s_full[b]);
+            BGMV_ISSUE_STAGE(i);
         }
     } else if (tid == 32) {
         // MMA issuer: four K = 16 steps per stage into the TMEM accumulator
@@ -196,6 +204,7 @@ bgmv_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
         }
         tc_commit(&s_done);  // arrives once every MMA issued above is complete
     }
+#undef BGMV_ISSUE_STAGE
     __syncwarp();
     if (!mbar_wait_cta(&s_done, 0)) timed_out = true;
     __syncwarp();
@@ -275,214 +284,310 @@ bgmv_shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_consta
 __global__ void __launch_bounds__(kBThreads) bgmv_capacity_probe() {}
 
 // ------------------------------------------------------------------ expand
-// Shared memory: the out tile (add_inputs; nc / 64 TMA boxes of 128 rows x
-// 128 bytes), B_ext [kgroups][nc rows][128 B], Y_ext hi and lo
-// [kgroups][128 rows][128 B]; 128-byte swizzled K-major, 1024-byte aligned.
-__host__ __device__ constexpr int expand_smem_bytes(int nc, int kgroups, bool add) {
-    return 1024 + (add ? nc * kBT * 2 : 0) + kgroups * nc * 128 + 2 * kgroups * kBT * 128;
+// Persistent, double-buffered: every CTA walks a contiguous range of work
+// items (token block x column chunk, block-major), and while item k is
+// contracted and written back, the out tile and B rows of item k+1 are
+// already in flight.  Y_ext is rebuilt only when the token block or the slice
+// (whose y columns it holds) changes.  8 warps: warps w and w + 4 own TMEM
+// lanes 32 (w % 4) .. + 31 (the block's tokens) and split the chunk's columns.
+//  - out: loaded by TMA (add_inputs), updated in place in shared memory and
+//    written back by TMA stores (one per 64-column box: a warp storing one
+//    16-byte piece per token row would touch 32 rows per instruction);
+//    rows without a LoRA term keep the values read (with add_inputs) or
+//    become zeros (without); a ragged last box is stored by the threads;
+//  - B_ext: cp.async pieces of 8 ranks, ranks past r_l and columns past the
+//    slice zero-filled.
+constexpr int kEThreads = 256;
+
+
+// Shared memory: two stages of (out tile: nc / 64 boxes of 128 rows x 128 B;
+// B_ext [kgroups][nc rows][128 B]), then Y_ext hi and lo [kgroups][128 rows]
+// [128 B]; 128-byte swizzled K-major, 1024-byte aligned.
+__host__ __device__ constexpr int expand_stage_bytes(int nc, int kgroups) {
+    return nc * kBT * 2 + kgroups * nc * 128;
+}
+__host__ __device__ constexpr int expand_smem_bytes(int nc, int kgroups) {
+    return 1024 + 2 * expand_stage_bytes(nc, kgroups) + 2 * kgroups * kBT * 128;
+}
+
+struct ExpandItem {
+    int t0, s, n0, ncols;
+    int64_t col0;
+};
+
+__device__ __forceinline__ ExpandItem expand_item(const BgmvExpandArgs &a, int item, int nchunks,
+                                                  int nc) {
+    ExpandItem it;
+    const int blk = item / nchunks, chunk = item - blk * nchunks;
+    int s = 0;
+    while (s + 1 < a.num_slices && chunk >= a.chunk_begin[s + 1]) ++s;
+    it.t0 = blk * kBT;
+    it.s = s;
+    it.n0 = (chunk - a.chunk_begin[s]) * nc;
+    it.ncols = min(nc, a.N[s] - it.n0);  // > 0, a multiple of 8
+    it.col0 = (int64_t)a.off[s] + it.n0;
+    return it;
 }
 
 // KSY: 16-wide K steps per adapter (ranks padded to RP = 16 * KSY).
 template <typename E, bool ADD, int KSY>
-__global__ void __launch_bounds__(kBThreads)
+__global__ void __launch_bounds__(kEThreads)
 bgmv_expand_kernel(const __grid_constant__ CUtensorMap tm_out, const BgmvExpandArgs a, int nc,
-                   int kgroups) {
+                   int kgroups, int n_items, int nchunks) {
     constexpr int RP = 16 * KSY;
     extern __shared__ __align__(16) unsigned char smem[];
-    __shared__ uint64_t s_bar_out, s_bar_mma;
+    __shared__ uint64_t s_full[2], s_mma;
     __shared__ uint32_t s_tmem;
-    __shared__ int s_present;  // bit l: adapter l has a token (of nonzero rank) in this block
+    __shared__ int s_present;  // bit l: adapter l has a token (of nonzero rank) in the block
+    __shared__ int s_l[kBT];   // adapter of each row of the block (-1: no LoRA term)
+    __shared__ float s_f[kBT]; // per-row scale * 2^e of the y scaling
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int t0 = blockIdx.x * kBT, chunk = blockIdx.y;
-    const int t = t0 + tid;
-    int s = 0;
-    while (s + 1 < a.num_slices && chunk >= a.chunk_begin[s + 1]) ++s;
-    const int Ns = a.N[s];
-    const int n0 = (chunk - a.chunk_begin[s]) * nc;
-    const int ncols = min(nc, Ns - n0);  // > 0, a multiple of 8
-    const int64_t col0 = (int64_t)a.off[s] + n0;
     const int R = a.R;
     E *__restrict__ out = static_cast<E *>(a.out);
+    const int i0 = (int)((int64_t)blockIdx.x * n_items / gridDim.x);
+    const int i1 = (int)((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
+    const int count = i1 - i0;
     unsigned char *sm = smem + ((1024 - (smem_u32(smem) & 1023)) & 1023);
-    unsigned char *sOut = sm;
-    unsigned char *sB = sOut + (ADD ? nc * kBT * 2 : 0);
-    unsigned char *sYh = sB + kgroups * nc * 128;
+    const int stage = expand_stage_bytes(nc, kgroups);
+    unsigned char *sYh = sm + 2 * stage;
     unsigned char *sYl = sYh + kgroups * kBT * 128;
+    auto sOut = [&](int b) { return sm + b * stage; };
+    auto sB = [&](int b) { return sm + b * stage + nc * kBT * 2; };
 
-    if (tid == 0) {
-        s_present = 0;
-        mbar_init(&s_bar_out, 1);
-        mbar_init(&s_bar_mma, 1);
-        if (ADD) tma_prefetch_map(&tm_out);
-    }
-    // this thread's token and adapter (the index array is an input of the
-    // pair: it is read before the wait for the previous kernel)
-    int l = -1, rl = 0;
-    if (t < a.T) {
-        const int v = a.idx ? __ldg(a.idx + t) : 0;
-        if (v >= 0 && v < a.L) {
-            rl = clamp_rank(a.ranks, v, R);
-            if (rl > 0) l = v;
+    // Item j's out tile (add_inputs; rows past T zero-filled) and B rows into
+    // stage b.  Thread 0 first waits until the TMA stores of the stage's
+    // previous item have read it.  cp.async B pieces: one group per call and
+    // thread.
+    auto issue = [&](int j, int b, bool stored_before) {
+        const ExpandItem it = expand_item(a, j, nchunks, nc);
+        if (tid == 0) {
+            if (stored_before) tma_store_wait_read();
+            if (ADD) {
+                const int nbox = (it.ncols + kBox - 1) / kBox;
+                mbar_arrive_expect_tx(&s_full[b], (uint32_t)(nbox * kBT * 128));
+                for (int i = 0; i < nbox; ++i)
+                    tma_load_2d(smem_u32(sOut(b) + i * kBT * 128), &tm_out,
+                                (int)(it.col0 + i * kBox), it.t0, &s_full[b]);
+            }
         }
-    }
-    __syncthreads();
-    if (l >= 0) atomicOr(&s_present, 1 << l);
-    __syncthreads();
-    const int present = s_present;
-    if (present == 0) {  // no LoRA term in this block: untouched with add_inputs, zeros without
-        if (!ADD && t < a.T)
-            for (int c = 0; c < ncols; c += 8)
-                st_global_v4(out + (int64_t)t * a.ldo + col0 + c, make_uint4(0, 0, 0, 0));
-        return;
-    }
-    // out tile (add_inputs) by TMA; rows past T are zero-filled and never stored
-    if (ADD && tid == 0) {
-        const int nbox = (ncols + kBox - 1) / kBox;
-        mbar_arrive_expect_tx(&s_bar_out, (uint32_t)(nbox * kBT * 128));
-        for (int i = 0; i < nbox; ++i)
-            tma_load_2d(smem_u32(sOut + i * kBT * 128), &tm_out, (int)(col0 + i * kBox), t0,
-                        &s_bar_out);
-    }
-    // B_ext: adapter lb's ranks at K positions [lb * RP, lb * RP + RP), 8 per
-    // 16-byte piece, ranks >= r_lb and rows past the slice zero-filled;
-    // adapters without a token here are neither loaded nor multiplied
-    {
-        const E *Bs = static_cast<const E *>(a.B[s]);
-        const int per_row = kgroups * 8;
-        for (int it = tid; it < nc * per_row; it += kBThreads) {
-            const int n = it / per_row, c = it - n * per_row;
-            const int lb = (8 * c) / RP, k = 8 * c - lb * RP;
-            if (lb >= a.L || !((present >> lb) & 1)) continue;
-            const int nv = n < ncols ? min(8, clamp_rank(a.ranks, lb, R) - k) : 0;
-            const E *src = nv > 0 ? Bs + ((int64_t)lb * Ns + n0 + n) * R + k : Bs;
-            cp_async16(smem_u32(sB + (c >> 3) * nc * 128 + n * 128 + (((c & 7) ^ (n & 7)) << 4)),
-                       src, nv > 0 ? 2 * nv : 0);
+        {
+            const E *Bs = static_cast<const E *>(a.B[it.s]);
+            const int Ns = a.N[it.s];
+            const int per_row = kgroups * 8;
+            unsigned char *dstB = sB(b);
+            for (int q = tid; q < nc * per_row; q += kEThreads) {
+                const int n = q / per_row, c = q - n * per_row;
+                const int lb = (8 * c) / RP, k = 8 * c - lb * RP;
+                if (lb >= a.L) continue;
+                const int nv = n < it.ncols ? min(8, clamp_rank(a.ranks, lb, R) - k) : 0;
+                const E *src = nv > 0 ? Bs + ((int64_t)lb * Ns + it.n0 + n) * R + k : Bs;
+                cp_async16(smem_u32(dstB + (c >> 3) * nc * 128 + n * 128 + (((c & 7) ^ (n & 7)) << 4)),
+                           src, nv > 0 ? 2 * nv : 0);
+            }
         }
         cp_async_commit();
-    }
+    };
 
-    // y comes from the previous kernel (the shrink).  Tensor memory is taken
-    // only after this wait: a CTA holding TMEM never waits on another grid.
+    if (tid == 0) {
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(&s_mma, 1);
+        tma_prefetch_map(&tm_out);
+    }
+    // The first two items' loads go out before the wait for the previous
+    // kernel: out and B are not written by it (y is).
+    if (count > 0) issue(i0, 0, false);
+    if (count > 1) issue(i0 + 1, 1, false);
     grid_dep_wait();
     grid_dep_launch();
-    if (tid < 32) tc_alloc(&s_tmem, (uint32_t)nc);
-
-    // Y_ext rows of this thread's token: its y as a hi/lo pair scaled by 2^-e
-    // in its adapter's K block, zeros elsewhere
-    float f = 0.f;
-    {
-        float yv[RP];
-#pragma unroll
-        for (int k = 0; k < RP; ++k) yv[k] = 0.f;
-        if (l >= 0) {
-            const float *yr = a.y + (int64_t)t * a.ldy + (int64_t)s * a.y_slice_stride;
-#pragma unroll
-            for (int k = 0; k < RP; k += 4)
-                if (k < rl) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4 *>(yr + k));
-                    yv[k] = v.x;
-                    yv[k + 1] = v.y;
-                    yv[k + 2] = v.z;
-                    yv[k + 3] = v.w;
-                }
-            float m = 0.f;
-#pragma unroll
-            for (int k = 0; k < RP; ++k) {
-                if (k >= rl) yv[k] = 0.f;
-                m = fmaxf(m, fabsf(yv[k]));
-            }
-            const int e = row_exponent(m);
-            f = a.scale * exp2i(e);
-            const float inv = exp2i(-e);
-#pragma unroll
-            for (int k = 0; k < RP; ++k) yv[k] *= inv;
-        }
-        const int cl0 = l >= 0 ? l * (RP / 8) : -RP;  // first 16-byte piece of the adapter's block
-        const int rowoff = tid * 128;
-        for (int c = 0; c < kgroups * 8; ++c) {
-            if (c >= cl0 && c < cl0 + RP / 8) continue;
-            const int off = (c >> 3) * kBT * 128 + rowoff + (((c & 7) ^ (tid & 7)) << 4);
-            *reinterpret_cast<uint4 *>(sYh + off) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4 *>(sYl + off) = make_uint4(0, 0, 0, 0);
-        }
-        if (l >= 0) {
-#pragma unroll
-            for (int j = 0; j < RP / 8; ++j) {
-                float v[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) v[q] = yv[8 * j + q];
-                uint4 hi, lo;
-                split_hilo8<E>(v, hi, lo);
-                const int c = cl0 + j;
-                const int off = (c >> 3) * kBT * 128 + rowoff + (((c & 7) ^ (tid & 7)) << 4);
-                *reinterpret_cast<uint4 *>(sYh + off) = hi;
-                *reinterpret_cast<uint4 *>(sYl + off) = lo;
-            }
-        }
-    }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();  // Y (plain stores) and B (cp.async) -> tensor-core operand reads
+    // Tensor memory is taken only after that wait: a CTA holding TMEM never
+    // waits on another grid.
+    if (warp == 0) tc_alloc(&s_tmem, (uint32_t)nc);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    if (tid == 0) {
-        const uint32_t idesc = tc_idesc_f16(std::is_same<E, __nv_bfloat16>::value, kBT, nc);
-        bool acc = false;
-        for (int lb = 0; lb < a.L; ++lb) {
-            if (!((present >> lb) & 1)) continue;
-#pragma unroll
-            for (int ks = 0; ks < KSY; ++ks) {
-                const int kpos = lb * RP + 16 * ks;
-                const uint32_t g = (uint32_t)(kpos >> 6), kb = (uint32_t)((kpos & 63) * 2);
-                const uint32_t yh = smem_u32(sYh) + g * kBT * 128 + kb;
-                const uint32_t yl = smem_u32(sYl) + g * kBT * 128 + kb;
-                const uint32_t bb = smem_u32(sB) + g * (uint32_t)nc * 128 + kb;
-                tc_mma_f16(tmem, tc_desc_sw128(yh), tc_desc_sw128(bb), idesc, acc);
-                tc_mma_f16(tmem, tc_desc_sw128(yl), tc_desc_sw128(bb), idesc, true);
-                acc = true;
-            }
-        }
-        tc_commit(&s_bar_mma);
-    }
-    bool to = !mbar_wait_cta(&s_bar_mma, 0);
-    if (ADD && !mbar_wait_cta(&s_bar_out, 0)) to = true;
-    const bool any_to = __syncthreads_or(to);  // also reconverges the warps
-    if (any_to) {
-        // never expected: flag it and leave out untouched
-        if (tid == 0 && a.status) atomicOr(a.status, LORA_PLANERR_TIMEOUT);
-        mbar_wait_cta(&s_bar_mma, 0);
-        if (ADD) mbar_wait_cta(&s_bar_out, 0);
-    } else {
-        tc_fence_after();
-        // rows with a LoRA term; without add_inputs every token row (zeros for the others)
-        const bool live = t < a.T && (l >= 0 || !ADD);
-        const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
-        E *orow = out + (int64_t)t * a.ldo + col0;
-        for (int cc = 0; cc < ncols; cc += 32) {  // block-uniform
-            float d[32];
-            tc_ld32(taddr + (uint32_t)cc, d);
-            if (!live) continue;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const int c = cc + 8 * g;
-                if (c >= ncols) break;
-                float v[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) v[k] = f * d[8 * g + k];
-                if (ADD) {
-                    const int piece = (c & 63) >> 3;
-                    float o[8];
-                    unpack8<E>(*reinterpret_cast<const uint4 *>(
-                                   sOut + (c >> 6) * kBT * 128 + tid * 128 + ((piece ^ (tid & 7)) << 4)),
-                               o);
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) v[k] += o[k];
+
+    const uint32_t idesc = tc_idesc_f16(std::is_same<E, __nv_bfloat16>::value, kBT, nc);
+    const int r = tid & (kBT - 1), half = tid >> 7;
+    int yblk = -1, yslice = -1, present = 0;
+    int nmma = 0;     // phases completed on s_mma (items with MMAs)
+    int waited = 0;   // items whose loads have been waited for
+    bool timed_out = false;
+    for (int k = 0; k < count; ++k) {
+        const int b = k & 1;
+        const ExpandItem it = expand_item(a, i0 + k, nchunks, nc);
+        if (it.t0 != yblk || it.s != yslice) {  // block-uniform
+            // Y_ext rows of the block for this slice's y columns: each token's
+            // y as a hi (threads < 128) or lo (threads >= 128) part scaled by
+            // 2^-e in its adapter's K block, zeros elsewhere.  The previous
+            // item's MMAs are complete.
+            yblk = it.t0;
+            yslice = it.s;
+            if (tid == 0) s_present = 0;
+            const int t = it.t0 + r;
+            int l = -1, rl = 0;
+            if (t < a.T) {
+                const int v = a.idx ? __ldg(a.idx + t) : 0;
+                if (v >= 0 && v < a.L) {
+                    rl = clamp_rank(a.ranks, v, R);
+                    if (rl > 0) l = v;
                 }
-                st_global_v4(orow + c, pack8<E>(v));
+            }
+            float yv[RP];
+#pragma unroll
+            for (int q = 0; q < RP; ++q) yv[q] = 0.f;
+            float f = 0.f;
+            if (l >= 0) {
+                const float *yr = a.y + (int64_t)t * a.ldy + (int64_t)it.s * a.y_slice_stride;
+#pragma unroll
+                for (int q = 0; q < RP; q += 4)
+                    if (q < rl) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(yr + q));
+                        yv[q] = v.x;
+                        yv[q + 1] = v.y;
+                        yv[q + 2] = v.z;
+                        yv[q + 3] = v.w;
+                    }
+                float m = 0.f;
+#pragma unroll
+                for (int q = 0; q < RP; ++q) {
+                    if (q >= rl) yv[q] = 0.f;
+                    m = fmaxf(m, fabsf(yv[q]));
+                }
+                const int e = row_exponent(m);
+                f = a.scale * exp2i(e);
+                const float inv = exp2i(-e);
+#pragma unroll
+                for (int q = 0; q < RP; ++q) yv[q] *= inv;
+            }
+            __syncthreads();  // s_present reset; nobody reads the previous rows now
+            if (half == 0) {
+                s_l[r] = l;
+                s_f[r] = f;
+                if (l >= 0) atomicOr(&s_present, 1 << l);
+            }
+            unsigned char *dstY = half ? sYl : sYh;
+            const int cl0 = l >= 0 ? l * (RP / 8) : -RP;  // first 16-byte piece of the block
+            for (int c = 0; c < kgroups * 8; ++c) {
+                if (c >= cl0 && c < cl0 + RP / 8) continue;
+                *reinterpret_cast<uint4 *>(dstY + (c >> 3) * kBT * 128 + r * 128 +
+                                           (((c & 7) ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+            }
+            if (l >= 0) {
+#pragma unroll
+                for (int j = 0; j < RP / 8; ++j) {
+                    float v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = yv[8 * j + q];
+                    uint4 hi, lo;
+                    split_hilo8<E>(v, hi, lo);
+                    const int c = cl0 + j;
+                    *reinterpret_cast<uint4 *>(dstY + (c >> 3) * kBT * 128 + r * 128 +
+                                               (((c & 7) ^ (r & 7)) << 4)) = half ? lo : hi;
+                }
             }
         }
+        // this item's B pieces (cp.async; one newer group may be in flight)
+        if (k + 1 < count) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        fence_proxy_async_smem();  // Y (plain stores) and B (cp.async) -> tensor-core reads
+        __syncthreads();
+        present = s_present;
+        bool to = false;
+        if (ADD && !mbar_wait_cta(&s_full[b], (k >> 1) & 1)) to = true;
+        if (!to) waited = k + 1;
+        if (tid == 0 && present) {
+            tc_fence_after();
+            bool acc = false;
+            for (int lb = 0; lb < a.L; ++lb) {
+                if (!((present >> lb) & 1)) continue;
+#pragma unroll
+                for (int ks = 0; ks < KSY; ++ks) {
+                    const int kpos = lb * RP + 16 * ks;
+                    const uint32_t g = (uint32_t)(kpos >> 6), kb = (uint32_t)((kpos & 63) * 2);
+                    const uint32_t yh = smem_u32(sYh) + g * kBT * 128 + kb;
+                    const uint32_t yl = smem_u32(sYl) + g * kBT * 128 + kb;
+                    const uint32_t bb = smem_u32(sB(b)) + g * (uint32_t)nc * 128 + kb;
+                    tc_mma_f16(tmem, tc_desc_sw128(yh), tc_desc_sw128(bb), idesc, acc);
+                    tc_mma_f16(tmem, tc_desc_sw128(yl), tc_desc_sw128(bb), idesc, true);
+                    acc = true;
+                }
+            }
+            tc_commit(&s_mma);
+        }
+        // the MMA barrier completes one phase per item that has MMAs
+        if (present) {
+            if (!mbar_wait_cta(&s_mma, (uint32_t)(nmma & 1))) to = true;
+            ++nmma;
+        }
+        if (__syncthreads_or(to)) {  // never expected: flag it and leave out untouched
+            if (tid == 0 && a.status) atomicOr(a.status, LORA_PLANERR_TIMEOUT);
+            timed_out = true;
+            break;
+        }
+        tc_fence_after();
+        // epilogue: this thread's token row, its half of the chunk's columns;
+        // full 64-column boxes are updated in shared memory for the TMA
+        // stores, the columns of a ragged last box are stored directly
+        const int full_cols = (it.ncols / kBox) * kBox;
+        {
+            const int t = it.t0 + r, l = s_l[r];
+            const bool live = t < a.T && (l >= 0 || !ADD);
+            const float f = s_f[r];
+            const int cbeg = half * (nc / 2);
+            const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)cbeg;
+            E *orow = out + (int64_t)t * a.ldo + it.col0;
+            unsigned char *so = sOut(b);
+            for (int cc = 0; cc < nc / 2 && cbeg + cc < it.ncols; cc += 32) {  // warp-uniform
+                float d[32];
+                if (present) {
+                    tc_ld32(taddr + (uint32_t)cc, d);
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) d[q] = 0.f;
+                }
+                if (!live) continue;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const int c = cbeg + cc + 8 * g;
+                    if (c >= it.ncols) break;
+                    float v[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) v[q] = f * d[8 * g + q];
+                    uint4 *slot = reinterpret_cast<uint4 *>(
+                        so + (c >> 6) * kBT * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4));
+                    if (ADD) {
+                        float o[8];
+                        unpack8<E>(*slot, o);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) v[q] += o[q];
+                    }
+                    if (c < full_cols) *slot = pack8<E>(v);
+                    else st_global_v4(orow + c, pack8<E>(v));
+                }
+            }
+        }
+        fence_proxy_async_smem();  // the updated tile -> the TMA stores
+        tc_fence_before();
+        __syncthreads();  // stage b's B, TMEM and the block's rows are free again
+        if (tid == 0 && full_cols > 0) {
+            for (int i = 0; i < full_cols / kBox; ++i)
+                tma_store_2d(&tm_out, (int)(it.col0 + i * kBox), it.t0,
+                             smem_u32(sOut(b) + i * kBT * 128));
+            tma_store_commit();
+        }
+        if (k + 2 < count) issue(i0 + k + 2, b, full_cols > 0);
     }
+    // no copy into or out of this CTA's shared memory may be in flight when it
+    // exits (after a timed-out wait: one more bounded wait per load not yet seen)
+    cp_async_wait<0>();
+    if (ADD && timed_out) {
+        const int issued = min(count, waited + 2);
+        for (int k = waited; k < issued; ++k) mbar_wait_cta(&s_full[k & 1], (k >> 1) & 1);
+    }
+    if (timed_out && nmma > 0) mbar_wait_cta(&s_mma, (uint32_t)((nmma - 1) & 1));
+    if (tid == 0) tma_store_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -491,7 +596,7 @@ bgmv_expand_kernel(const __grid_constant__ CUtensorMap tm_out, const BgmvExpandA
     }
 }
 
-using ExpandFn = void (*)(const CUtensorMap, const BgmvExpandArgs, int, int);
+using ExpandFn = void (*)(const CUtensorMap, const BgmvExpandArgs, int, int, int, int);
 template <typename E, bool ADD>
 ExpandFn expand_fn(int ksy) {
     switch (ksy) {
@@ -557,7 +662,7 @@ cudaError_t configure_bgmv_kernels(const DeviceInfo &dev) {
             for (int ksy = 1; ksy <= 4 && e == cudaSuccess; ++ksy)
                 e = cudaFuncSetAttribute(expand_fn(dt, add != 0, ksy),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         expand_smem_bytes(128, 2, true));
+                                         expand_smem_bytes(128, 2));
     }
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(bgmv_capacity_probe, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
@@ -624,8 +729,10 @@ cudaError_t launch_bgmv_shrink(lora_dtype_t dt, const BgmvShrinkArgs &a, const D
     int lc = 0;
     while ((1 << lc) < C) ++lc;
     // Shares of the y columns, coarse to fine: whole adapters (zk of them,
-    // N = zk * W <= 256), then column ranges of one adapter.  Take the
-    // finest share whose grid is still resident in one wave of clusters.
+    // N = zk * W <= 256), then column ranges of one adapter.  Measured on the
+    // decode q/k/v batches (T = 16 .. 1024), the coarsest share is the best or
+    // within 2 %: finer shares re-read x from L2 and, for large batches,
+    // overflow the wave of clusters the GPU holds.
     struct Cand {
         int zk, zc, cw, Z;
     } cands[24];
@@ -644,10 +751,8 @@ cudaError_t launch_bgmv_shrink(lora_dtype_t dt, const BgmvShrinkArgs &a, const D
     for (int cw = kMaxCw; cw >= 16 && nc < 24; cw /= 2)
         if (cw < W) cands[nc++] = {1, (W + cw - 1) / cw, cw, a.L * ((W + cw - 1) / cw)};
     if (nc == 0) return cudaErrorInvalidValue;  // unreachable: W % 8 == 0 gives a column share
-    int pick = 0;
-    const long long cap = std::max(1, g_cluster_ctas[1][lc]);
-    for (int i = 0; i < nc; ++i)
-        if ((long long)blocks * C * cands[i].Z <= cap && cands[i].Z <= 65535) pick = i;
+    const int pick = 0;
+    if (cands[pick].Z > 65535) return cudaErrorInvalidConfiguration;
     ShrinkSplit p{};
     p.kc_len = kc_len;
     p.zk = cands[pick].zk;
@@ -657,11 +762,18 @@ cudaError_t launch_bgmv_shrink(lora_dtype_t dt, const BgmvShrinkArgs &a, const D
     const int tneed = (p.zk - 1) * W + (p.cw + 31) / 32 * 32;
     p.tcols = 32;
     while ((int)p.tcols < tneed) p.tcols *= 2;
+    // Stage ring: the deepest (up to the CTA's whole K range, at most 4
+    // stages in flight) whose shared memory still lets the whole grid of
+    // clusters be resident at once (one CTA per SM above kShrinkSmemCap)
     const int nk = (kc_len + kBox - 1) / kBox;
     const int stage = kBT * 128 + p.n_mma * 128, recv = kBT * p.cw * 4;
-    const int fit = (kShrinkSmemCap - 1024 - recv) / stage;
-    p.nst = std::max(2, std::min({fit, kMaxStages, nk}));
-    if (nk == 1) p.nst = 1;
+    const long long ctas = (long long)blocks * C * cands[pick].Z;
+    int smem = 0;
+    for (p.nst = std::min(kMaxStages, nk); ; --p.nst) {
+        smem = shrink_smem_for_tmem(1024 + p.nst * stage + recv, p.tcols);
+        const int cap = g_cluster_ctas[smem <= kShrinkSmemCap ? 1 : 0][lc];
+        if (ctas <= cap || p.nst <= std::min(2, nk)) break;
+    }
 
     CUtensorMap tx, ta;
     cudaError_t e = make_map(&tx, dt, a.x, (uint64_t)a.T, (uint64_t)a.H, (uint64_t)a.ldx, kBT);
@@ -671,7 +783,7 @@ cudaError_t launch_bgmv_shrink(lora_dtype_t dt, const BgmvShrinkArgs &a, const D
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C, blocks, cands[pick].Z);
     cfg.blockDim = dim3(kBThreads);
-    cfg.dynamicSmemBytes = shrink_smem_for_tmem(1024 + p.nst * stage + recv, p.tcols);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -691,41 +803,45 @@ cudaError_t launch_bgmv_expand(lora_dtype_t dt, const BgmvExpandArgs &a_in, cons
     if (a.T == 0) return cudaSuccess;
     const int RP = (a.R + 15) / 16 * 16;
     const int kgroups = (a.L * RP + 63) / 64;
-    const int blocks = (a.T + kBT - 1) / kBT;
+    const long long blocks = (a.T + kBT - 1) / kBT;
     auto chunks = [&](int nc) {
         long long n = 0;
         for (int s = 0; s < a.num_slices; ++s) n += (a.N[s] + nc - 1) / nc;
         return n;
     };
-    // 128 output columns per CTA; 64 when that leaves under two CTAs per SM
+    // 128 output columns per work item; 64 when there are fewer 128-column
+    // items than SMs (more, smaller items spread a small batch wider)
     int nc = 128;
-    if ((long long)blocks * chunks(128) < 2LL * dev.sm_count) nc = 64;
+    if (blocks * chunks(128) < dev.sm_count) nc = 64;
     a.chunk_begin[0] = 0;
     for (int s = 0; s < a.num_slices; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s] + (a.N[s] + nc - 1) / nc;
     for (int s = a.num_slices; s < LORA_MAX_SLICES; ++s) a.chunk_begin[s + 1] = a.chunk_begin[s];
-    const int total = a.chunk_begin[a.num_slices];
-    if (total == 0) return cudaSuccess;
-    if (total > 65535) return cudaErrorInvalidConfiguration;
-    CUtensorMap tm;
-    memset(&tm, 0, sizeof(tm));
-    if (a.add) {
-        int used = 0;
-        for (int s = 0; s < a.num_slices; ++s)
-            if (a.N[s] > 0) used = std::max(used, a.off[s] + a.N[s]);
-        cudaError_t e = make_map(&tm, dt, a.out, (uint64_t)a.T, (uint64_t)used, (uint64_t)a.ldo, kBT);
-        if (e != cudaSuccess) return e;
-    }
+    const int nchunks = a.chunk_begin[a.num_slices];
+    if (nchunks == 0) return cudaSuccess;
+    const long long items = blocks * nchunks;
+    if (items > INT_MAX) return cudaErrorInvalidConfiguration;
+    const int smem = expand_smem_bytes(nc, kgroups);
+    // persistent: as many CTAs as the GPU holds at once, at most one per item
+    const int per_sm = std::max(1, std::min(2, (g_smem_sm - 2048) / (smem + g_smem_reserved)));
+    const int grid = (int)std::min<long long>(items, (long long)per_sm * dev.sm_count);
+    CUtensorMap tm_out;
+    int used = 0;
+    for (int s = 0; s < a.num_slices; ++s)
+        if (a.N[s] > 0) used = std::max(used, a.off[s] + a.N[s]);
+    cudaError_t e = make_map(&tm_out, dt, a.out, (uint64_t)a.T, (uint64_t)used, (uint64_t)a.ldo, kBT);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(blocks, total);
-    cfg.blockDim = dim3(kBThreads);
-    cfg.dynamicSmemBytes = expand_smem_bytes(nc, kgroups, a.add != 0);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kEThreads);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, expand_fn(dt, a.add != 0, RP / 16), tm, a, nc, kgroups);
+    return cudaLaunchKernelEx(&cfg, expand_fn(dt, a.add != 0, RP / 16), tm_out, a, nc, kgroups,
+                              (int)items, nchunks);
 }
 
 }  // namespace lora

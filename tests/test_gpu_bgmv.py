@@ -65,11 +65,13 @@ def inactive_rows_ok(case, y, out):
 
 # ---------------------------------------------------------------- workloads
 
-@pytest.mark.parametrize("T", li.DECODE_T)
+@pytest.mark.parametrize("T", li.DECODE_T + (333, 700, 2000))
 @pytest.mark.parametrize("add", [True, False])
 @pytest.mark.parametrize("chained", [True, False])
 def test_decode_qkv(cuda_lib, T, add, chained):
-    c = li.decode_qkv(T)
+    """The decode q/k/v batches, plus batch sizes whose per-CTA work ranges
+    of the persistent expand cross slice and token-block boundaries."""
+    c = li.decode_qkv(T) if T in li.DECODE_T else li.decode_qkv(T, seed=T)
     c.add = add
     y, out = check(cuda_lib, c, chained=chained)
     inactive_rows_ok(c, y, out)
