@@ -290,6 +290,174 @@ def next_rows(lg, dev, hbm_gbs: float):
     return res
 
 
+def _device_normal(shape, std, dtype, dev, gen):
+    return (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32) * std).to(dtype)
+
+
+def sweep_work(T: int, Hm: int, N: int, r: int, U: int):
+    """Algorithmic bytes of one sweep point (every token active, add_inputs):
+    shrink = x + the U used adapters' A rows + y written; expand = y read +
+    the used B rows + out read and written."""
+    sh_b = T * Hm * 2 + U * r * Hm * 2 + T * r * 4
+    ex_b = T * r * 4 + U * N * r * 2 + 2 * T * N * 2
+    return sh_b, ex_b
+
+
+def sweep_rows(lg, dev, hbm_gbs: float, max_sets: int = 256, reps: int = 3):
+    """The microbenchmark sweep (vLLM PR #11579's list_bench commands): hidden
+    sizes {1024, 2048, 2049, 4096, 8192, 16384} x batch {16 .. 8192} at seq-len
+    1 (BGMV, one token per request) and 8 (SGMV, one 8-token segment per
+    request), r = 16, 4 adapters drawn uniformly and sorted by id, fp16,
+    expand to N = H with add_inputs.  Shrink and expand are timed separately:
+    the average launch over a rotating pool of argument sets (>= 4x L2, at
+    most `max_sets` sets; `pool_MB` says how much), inputs drawn on the device.
+    Seq-len 1 runs the plan-free BGMV operators where they take the shape
+    (H % 8 == 0), the grouped ones otherwise; seq-len 8 runs the grouped
+    operators on a segment plan built once (outside the timing)."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(li.SEED_BASE + 5)
+    r, Ls = 16, 4
+    rows = []
+    for Hm in li.SWEEP_H:
+        for batch in li.SWEEP_BATCH:
+            for sl in (1, 8):
+                T, N = batch * sl, Hm
+                ids_req, _ = torch.sort(torch.randint(0, Ls, (batch,), generator=gen, device=dev,
+                                                      dtype=torch.int32))
+                U = int(torch.unique(ids_req).numel())
+                set_bytes = T * Hm * 2 + T * N * 2 + T * r * 4 + 2 * Ls * r * Hm * 2
+                nsets = int(min(max_sets, max(1, -(-4 * l2 // set_bytes))))
+                sets = [{"x": _device_normal((T, Hm), 1.0, torch.float16, dev, gen),
+                         "A": _device_normal((Ls, r, Hm), 0.02, torch.float16, dev, gen),
+                         "B": _device_normal((Ls, N, r), 0.02, torch.float16, dev, gen),
+                         "out": _device_normal((T, N), 1.0, torch.float16, dev, gen),
+                         "y": torch.empty(T, r, device=dev)} for _ in range(nsets)]
+                if sl == 1:
+                    idx = ids_req.contiguous()
+                    path = "bgmv" if Hm % 8 == 0 else "grouped"
+                    if path == "grouped":
+                        plan = lg.new_plan(T, Ls, dev)
+                        lg.lora_group_tokens(idx, Ls, plan)
+                else:
+                    path = "grouped"
+                    plan = lg.new_plan(T, Ls, dev)
+                    starts = torch.arange(batch, dtype=torch.int32, device=dev) * sl
+                    lens = torch.full((batch,), sl, dtype=torch.int32, device=dev)
+                    lg.lora_group_segments(starts, lens, ids_req, T, Ls, plan)
+                if path == "bgmv":
+                    sh = lambda a: lg.lora_bgmv_shrink(a["x"], a["A"], a["y"], idx)
+                    ex = lambda a: lg.lora_bgmv_expand_slice(a["y"], [a["B"]], a["out"], [0], idx,
+                                                             y_slice_stride=0, add_inputs=True)
+                else:
+                    sh = lambda a: lg.lora_shrink(a["x"], a["A"], a["y"], plan)
+                    ex = lambda a: lg.lora_expand(a["y"], a["B"], a["out"], plan, add_inputs=True)
+                t_sh = _graph_avg_us(sets, sh, reps)
+                t_ex = _graph_avg_us(sets, ex, reps)
+                sh_b, ex_b = sweep_work(T, Hm, N, r, U)
+                rows.append({"H": Hm, "batch": batch, "seq_len": sl, "T": T, "path": path,
+                             "shrink_us": round(t_sh, 3),
+                             "shrink_frac": round(sh_b / (hbm_gbs * 1e3) / t_sh, 4),
+                             "expand_us": round(t_ex, 3),
+                             "expand_GBps": round(ex_b / t_ex / 1e3, 1),
+                             "expand_frac": round(ex_b / (hbm_gbs * 1e3) / t_ex, 4),
+                             "pool_MB": round(nsets * set_bytes / 1e6, 1)})
+                del sets
+    torch.cuda.synchronize()
+    return {"unit": "us per launch; frac = algorithmic bytes / measured HBM bandwidth / time",
+            "points": rows}
+
+
+def _graph_avg_us(sets, launch, reps: int) -> float:
+    """Average launch duration: one launch per argument set captured in one
+    CUDA graph, replayed `reps` times between two events on its stream."""
+    launch(sets[0])
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for a in sets:
+            launch(a)
+    g.replay()
+    # the replays run on torch's current stream, which the events bracket
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(reps):
+        g.replay()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) * 1e3 / (reps * len(sets))
+
+
+def mixed_rank_rows(lg, dev, hbm_gbs: float, reps: int = 3):
+    """The mixed-rank Llama-3-70B-shaped workload: T = 2048, H = 8192, 32
+    adapters with ranks from {2, 8, 16, 20, 64, 128} (stored at R = 128), Zipf(1.1)
+    adapter per token, 5 % without an adapter, bf16, expand to N in {8192,
+    28672}, BGMV (token order) and SGMV (tokens sorted into segments).  The
+    rank-aware call (the ranks table: rows / columns past a rank never read)
+    is timed against padding every adapter to rank 128 (no ranks table, the
+    padding zero-filled), the workaround Punica issue #17 describes.  Each
+    figure: average launch over a rotating pool >= 4x L2; tensors on the
+    device."""
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(li.SEED_BASE + 4)
+    T, Hm, L = 2048, 8192, 32
+    res = {}
+    for sgmv in (False, True):
+        ranks, mp = li.mixed_rank_map(T=T, L=L, sgmv=sgmv)
+        R = int(ranks.max())
+        plan = lg.new_plan(T, L, dev)
+        if sgmv:
+            ss, sl_, so = (t.to(dev) for t in mp)
+            lg.lora_group_segments(ss, sl_, so, T, L, plan)
+            lora_of = torch.repeat_interleave(so.cpu(), sl_.cpu())
+        else:
+            lg.lora_group_tokens(mp.to(dev), L, plan)
+            lora_of = mp
+        act = lora_of >= 0
+        Ta = int(act.sum())
+        used = torch.unique(lora_of[act]).long()
+        r_used = int(ranks[used].sum())
+        r_tok = int(ranks[lora_of[act].long()].sum())
+        ranks_d = ranks.to(dev)
+        keep = (torch.arange(R)[None, :] < ranks[:, None]).to(dev)  # [L, R]
+        for N in (8192, 28672):
+            set_bytes = T * Hm * 2 + L * R * Hm * 2 + L * N * R * 2 + T * N * 2 + T * R * 4
+            nsets = int(max(1, -(-4 * l2 // set_bytes)))
+            sets = []
+            for _ in range(nsets):
+                A = _device_normal((L, R, Hm), 0.02, torch.bfloat16, dev, gen) * keep[:, :, None]
+                B = _device_normal((L, N, R), 0.02, torch.bfloat16, dev, gen) * keep[:, None, :]
+                sets.append({"x": _device_normal((T, Hm), 1.0, torch.bfloat16, dev, gen),
+                             "A": A.contiguous(), "B": B.contiguous(),
+                             "out": _device_normal((T, N), 1.0, torch.bfloat16, dev, gen),
+                             "y": torch.zeros(T, R, device=dev)})
+            row = {"N": N, "pool_sets": nsets}
+            for tag, rk in (("rank_aware", ranks_d), ("padded_to_128", None)):
+                t_sh = _graph_avg_us(sets, lambda a: lg.lora_shrink(a["x"], a["A"], a["y"], plan,
+                                                                     ranks=rk), reps)
+                t_ex = _graph_avg_us(sets, lambda a: lg.lora_expand(a["y"], a["B"], a["out"], plan,
+                                                                     ranks=rk, add_inputs=True),
+                                     reps)
+                ru, rt = (r_used, r_tok) if rk is not None else (len(used) * R, Ta * R)
+                sh_b = Ta * Hm * 2 + ru * Hm * 2 + T * R * 4
+                ex_b = rt * 4 + ru * N * 2 + 2 * Ta * N * 2
+                row[tag] = {"shrink_us": round(t_sh, 2),
+                            "shrink_frac": round(sh_b / (hbm_gbs * 1e3) / t_sh, 4),
+                            "expand_us": round(t_ex, 2),
+                            "expand_frac": round(ex_b / (hbm_gbs * 1e3) / t_ex, 4),
+                            "bytes": {"shrink": sh_b, "expand": ex_b}}
+            row["speedup_rank_aware"] = round(
+                (row["padded_to_128"]["shrink_us"] + row["padded_to_128"]["expand_us"]) /
+                (row["rank_aware"]["shrink_us"] + row["rank_aware"]["expand_us"]), 3)
+            res[f"{'sgmv' if sgmv else 'bgmv'}_N{N}"] = row
+            del sets
+    torch.cuda.synchronize()
+    res["ranks"] = ranks.tolist()
+    return res
+
+
 def algorithmic_fused(idx: torch.Tensor):
     """Fused shrink + expand_slice: x, live A rows, y written once, live B
     rows, out read and written (y is not re-read from HBM)."""
@@ -387,7 +555,6 @@ def make_pool(dev, rank: int, l2_bytes: int, only_T=None):
     return pool, nsets * per_set
 
 
-FUSED_STEP = True  # shrink + expand_slice through the chained (PDL) entry point
 
 # DRAM bytes (read + write) of one launch of each kernel for the T=1024 batch,
 # from an ncu capture of `bench.py --profile --T 1024` (summaries under
@@ -400,94 +567,169 @@ NCU_TRAFFIC = {
 }
 
 
-def run_step(lg, batches, fused: bool = FUSED_STEP):
-    """One decode step: per batch, BGMV grouping, then the stacked q/k/v
-    shrink and the three-slice expand (fused into one launch by default)."""
+# The decode step's path: "bgmv" = the plan-free operators (no grouping; the
+# stacked q/k/v shrink and the three-slice expand chained in one call),
+# "grouped" = BGMV grouping into a plan, then the chained grouped operators.
+STEP_PATH = "bgmv"
+LAUNCHES_PER_BATCH = {"bgmv": 2, "grouped": 3}
+
+
+def run_step(lg, batches, path: str = STEP_PATH):
+    """One decode step over `batches` (q/k/v shrink and expand_slice per batch)."""
     for b in batches:
-        lg.lora_group_tokens(b["idx"], L, b["plan"])
-        if fused:
+        if path == "bgmv":
+            lg.lora_bgmv_shrink_expand_slice(b["x"], b["A"], b["y"], b["B"], b["out"],
+                                             b["case"].slice_offsets, b["idx"], add_inputs=True)
+        else:
+            lg.lora_group_tokens(b["idx"], L, b["plan"])
             lg.lora_shrink_expand_slice(b["x"], b["A"], b["y"], b["B"], b["out"], b["plan"],
                                         b["case"].slice_offsets, add_inputs=True)
-        else:
-            lg.lora_shrink(b["x"], b["A"], b["y"], b["plan"], num_slices=len(SLICES))
-            lg.lora_expand_slice(b["y"], b["B"], b["out"], b["plan"], b["case"].slice_offsets,
-                                 y_slice_stride=R, add_inputs=True)
 
 
-def e2e_run(lg, dev, steps: int, warmup: int):
-    """Through the public API with host buffers: every step copies the batch's
-    x, token indices and base output from pinned host memory, runs the path
-    and copies the updated output back."""
-    host, devb = [], []
-    for T in li.DECODE_T:
-        c = li.decode_qkv(T, seed=li.SEED_BASE + 2 + 5 * T)
-        host.append({"x": c.x.pin_memory(), "idx": c.token_idx.pin_memory(),
-                     "out": c.out.pin_memory(), "res": torch.empty_like(c.out).pin_memory()})
-        devb.append({"T": T, "case": c, "A": c.A.to(dev), "B": [b.to(dev) for b in c.B],
-                     "x": torch.empty_like(c.x, device=dev),
-                     "idx": torch.empty_like(c.token_idx, device=dev),
-                     "out": torch.empty_like(c.out, device=dev),
-                     "y": torch.empty(T, len(SLICES) * R, dtype=torch.float32, device=dev),
-                     "plan": lg.new_plan(T, L, dev)})
-    h2d = sum(h["x"].numel() * 2 + h["idx"].numel() * 4 + h["out"].numel() * 2 for h in host)
-    d2h = sum(h["out"].numel() * 2 for h in host)
+def e2e_run(lg, dev, steps: int, warmup: int, path: str = "bgmv"):
+    """Through the public API with host buffers.  Every step uploads the five
+    batches' inputs (x, token indices, base output) from pinned host memory,
+    runs the path and downloads the updated outputs.  The inputs are packed
+    in one pinned buffer and one device buffer laid out [all x | all
+    indices | all out], so a step is one host-to-device copy, the path's
+    calls on views of that buffer, and one device-to-host copy of the out
+    region.  Two such buffers alternate: the upload of step k+1 (copy stream)
+    overlaps the compute of step k, and the download of step k (a second
+    copy stream) overlaps both.  Returns tokens/s from CUDA events around the
+    timed steps, the bytes each way per step, wall-clock tokens/s and the
+    host link's copy bandwidth measured alone (same buffers)."""
+    align = 256
+    cases = [li.decode_qkv(T, seed=li.SEED_BASE + 2 + 5 * T) for T in li.DECODE_T]
+    offs, pos = [], 0
 
-    def step():
-        for h, d in zip(host, devb):
-            d["x"].copy_(h["x"], non_blocking=True)
-            d["idx"].copy_(h["idx"], non_blocking=True)
-            d["out"].copy_(h["out"], non_blocking=True)
-        run_step(lg, devb)
-        for h, d in zip(host, devb):
-            h["res"].copy_(d["out"], non_blocking=True)
+    def take(nbytes):
+        nonlocal pos
+        o = pos
+        pos = (pos + nbytes + align - 1) // align * align
+        return o
 
-    for _ in range(warmup):
-        step()
+    x_off = [take(c.x.numel() * 2) for c in cases]
+    i_off = [take(c.token_idx.numel() * 4) for c in cases]
+    out_begin = pos
+    o_off = [take(c.out.numel() * 2) for c in cases]
+    total, out_bytes = pos, pos - out_begin
+    slots = []
+    for _ in range(2):
+        hin = torch.empty(total, dtype=torch.uint8).pin_memory()
+        for c, xo, io, oo in zip(cases, x_off, i_off, o_off):
+            hin[xo:xo + c.x.numel() * 2].copy_(c.x.reshape(-1).view(torch.uint8))
+            hin[io:io + c.token_idx.numel() * 4].copy_(c.token_idx.view(torch.uint8))
+            hin[oo:oo + c.out.numel() * 2].copy_(c.out.reshape(-1).view(torch.uint8))
+        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+        batches = []
+        for c, xo, io, oo in zip(cases, x_off, i_off, o_off):
+            T = c.T
+            batches.append({
+                "T": T, "case": c,
+                "x": dbuf[xo:xo + T * H * 2].view(torch.bfloat16).view(T, H),
+                "idx": dbuf[io:io + T * 4].view(torch.int32),
+                "out": dbuf[oo:oo + T * NTOT * 2].view(torch.bfloat16).view(T, NTOT),
+                "y": torch.empty(T, len(SLICES) * R, dtype=torch.float32, device=dev),
+                "plan": lg.new_plan(T, L, dev)})
+        slots.append({"hin": hin, "hout": torch.empty(out_bytes, dtype=torch.uint8).pin_memory(),
+                      "dbuf": dbuf, "batches": batches,
+                      "up": torch.cuda.Event(), "done": torch.cuda.Event(),
+                      "down": torch.cuda.Event()})
+    weights = [{"A": c.A.to(dev), "B": [b.to(dev) for b in c.B]} for c in cases]
+    for sl in slots:
+        for b, w in zip(sl["batches"], weights):
+            b.update(w)
+    comp = torch.cuda.current_stream(dev)
+    up_s, down_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    for sl in slots:
+        sl["down"].record(down_s)
+
+    def step(k):
+        sl = slots[k % 2]
+        up_s.wait_event(sl["down"])       # the slot's previous outputs are downloaded
+        with torch.cuda.stream(up_s):
+            sl["dbuf"].copy_(sl["hin"], non_blocking=True)
+        sl["up"].record(up_s)
+        comp.wait_event(sl["up"])
+        run_step(lg, sl["batches"], path=path)
+        sl["done"].record(comp)
+        down_s.wait_event(sl["done"])
+        with torch.cuda.stream(down_s):
+            sl["hout"].copy_(sl["dbuf"][out_begin:], non_blocking=True)
+        sl["down"].record(down_s)
+
+    for k in range(warmup):
+        step(k)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     w0 = time.perf_counter()
-    t0.record()
-    for _ in range(steps):
-        step()
-    t1.record()
+    t0.record(up_s)
+    for k in range(steps):
+        step(warmup + k)
+    t1.record(down_s)
     torch.cuda.synchronize()
     wall = time.perf_counter() - w0
     ms = t0.elapsed_time(t1)
     tokens = steps * sum(li.DECODE_T)
-    return tokens / (ms / 1e3), h2d, d2h, tokens / wall
+    # the host link alone: the same upload and download, back to back
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(up_s):
+        c0.record(up_s)
+        for k in range(20):
+            slots[k % 2]["dbuf"].copy_(slots[k % 2]["hin"], non_blocking=True)
+        c1.record(up_s)
+    torch.cuda.synchronize()
+    h2d_gbs = 20 * total / (c0.elapsed_time(c1) / 1e3) / 1e9
+    with torch.cuda.stream(down_s):
+        c0.record(down_s)
+        for k in range(20):
+            slots[k % 2]["hout"].copy_(slots[k % 2]["dbuf"][out_begin:], non_blocking=True)
+        c1.record(down_s)
+    torch.cuda.synchronize()
+    d2h_gbs = 20 * out_bytes / (c0.elapsed_time(c1) / 1e3) / 1e9
+    return tokens / (ms / 1e3), total, out_bytes, tokens / wall, h2d_gbs, d2h_gbs
 
 
 def cpu_baseline(target_s: float = 10.0):
-    """The oracle, as it stands, on the same decode batches on the host cores."""
+    """The oracle, as it stands, on the same decode batches on the host cores:
+    with every core (OpenMP over tokens; the reported figure) and on one
+    thread (beside it), each for about target_s / 2 seconds of whole steps."""
     import oracle
-    import numpy as np
     prepared = []
     for T in li.DECODE_T:
         c = li.decode_qkv(T)
         prepared.append((T, c.token_idx.numpy(), c.x.double().numpy(), c.A.double().numpy(),
                          [b.double().numpy() for b in c.B], c.out.double().numpy(),
                          c.slice_offsets))
-    tokens, reps = 0, 0
-    t0 = time.perf_counter()
-    while True:
-        for T, idx, x, A, Bs, out, offs in prepared:
-            lo, _ = oracle.map_tokens(idx, L)
-            y = oracle.shrink(x, A, lo, num_slices=len(SLICES))
-            oracle.expand_slice(y, Bs, offs, lo, out, y_stride=R, add=True)
-            tokens += T
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= target_s:
-            break
-    del np
-    return {"value": tokens / el, "unit": "tokens/s", "cores": oracle.num_threads(),
-            "kind": "oracle",
+
+    def run(seconds):
+        tokens, reps = 0, 0
+        t0 = time.perf_counter()
+        while True:
+            for T, idx, x, A, Bs, out, offs in prepared:
+                lo, _ = oracle.map_tokens(idx, L)
+                y = oracle.shrink(x, A, lo, num_slices=len(SLICES))
+                oracle.expand_slice(y, Bs, offs, lo, out, y_stride=R, add=True)
+                tokens += T
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                return tokens, reps, el
+
+    cores = oracle.num_threads()
+    tokens, reps, el = run(target_s / 2)
+    oracle.set_threads(1)
+    t1, r1, e1 = run(target_s / 2)
+    oracle.set_threads(cores)
+    return {"value": tokens / el, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "one_thread": {"value": t1 / e1, "unit": "tokens/s", "cores": 1,
+                           "sample": f"{r1} full steps, {e1:.1f} s"},
             "sample": f"{reps} full steps ({tokens} tokens of the same five decode batches), "
                       f"fp64 C loops, OpenMP over tokens, {el:.1f} s"}
 
 
-def capture_steps(lg, pool, concurrent: bool):
+def capture_steps(lg, pool, concurrent: bool, path: str = STEP_PATH):
     """One CUDA graph per pool set holding a whole step (launch overhead off
     the timed path, as the pages time their kernels).  With `concurrent` the
     step's independent decode batches are parallel branches of the graph
@@ -508,14 +750,14 @@ def capture_steps(lg, pool, concurrent: bool):
                 for b, st in zip(batches, side):
                     st.wait_event(fork)
                     with torch.cuda.stream(st):
-                        run_step(lg, [b])
+                        run_step(lg, [b], path=path)
                     ev = torch.cuda.Event()
                     ev.record(st)
                     joins.append(ev)
                 for ev in joins:
                     stream.wait_event(ev)
             else:
-                run_step(lg, batches)
+                run_step(lg, batches, path=path)
         graphs.append(g)
     torch.cuda.synchronize()
     return graphs
@@ -597,9 +839,11 @@ def main_ours(args):
 
     for w in range(max(W, 1)):  # eager warm-up also configures the kernels before capture
         run_step(lg, pool[w % nsets])
+        run_step(lg, pool[w % nsets], path="grouped")
     torch.cuda.synchronize()
     graphs = capture_steps(lg, pool, concurrent=True)
     seq_graphs = capture_steps(lg, pool, concurrent=False)
+    grp_graphs = capture_steps(lg, pool, concurrent=True, path="grouped")
     for w in range(W):
         graphs[w % nsets].replay()
     torch.cuda.synchronize()
@@ -627,15 +871,22 @@ def main_ours(args):
 
     ms = start.elapsed_time(end)
     seq_ms = time_graphs(seq_graphs, W, K)  # the same steps with the batches in sequence
+    grp_ms = time_graphs(grp_graphs, W, K)  # the same steps through the grouped operators
 
-    # dominant kernel (fused shrink + expand_slice), timed right after the step
-    # loop on the same stream; the separate operators are timed for reference
-    fu_ms = op_only_ms(pool, lambda b: lg.lora_shrink_expand_slice(
-        b["x"], b["A"], b["y"], b["B"], b["out"], b["plan"], b["case"].slice_offsets,
-        add_inputs=True))
-    ex_ms = expand_only_ms(lg, pool)
-    sh_ms = op_only_ms(pool, lambda b: lg.lora_shrink(b["x"], b["A"], b["y"], b["plan"],
-                                                      num_slices=len(SLICES)))
+    # per batch size: the chained pair and its two kernels alone, on the
+    # plan-free path and (for reference) on the grouped one
+    offs = pool[0][0]["case"].slice_offsets
+    pair_ms = op_only_ms(pool, lambda b: lg.lora_bgmv_shrink_expand_slice(
+        b["x"], b["A"], b["y"], b["B"], b["out"], offs, b["idx"], add_inputs=True))
+    sh_ms = op_only_ms(pool, lambda b: lg.lora_bgmv_shrink(b["x"], b["A"], b["y"], b["idx"],
+                                                           num_slices=len(SLICES)))
+    ex_ms = op_only_ms(pool, lambda b: lg.lora_bgmv_expand_slice(
+        b["y"], b["B"], b["out"], offs, b["idx"], y_slice_stride=R, add_inputs=True))
+    gpair_ms = op_only_ms(pool, lambda b: lg.lora_shrink_expand_slice(
+        b["x"], b["A"], b["y"], b["B"], b["out"], b["plan"], offs, add_inputs=True))
+    gsh_ms = op_only_ms(pool, lambda b: lg.lora_shrink(b["x"], b["A"], b["y"], b["plan"],
+                                                       num_slices=len(SLICES)))
+    gex_ms = expand_only_ms(lg, pool)
     gr_ms = op_only_ms(pool, lambda b: lg.lora_group_tokens(b["idx"], L, b["plan"]))
     ex_src = (f"CUDA events around graphs of back-to-back launches, one per pool set "
               f"({nsets} sets, inputs from HBM), per batch size")
@@ -643,39 +894,37 @@ def main_ours(args):
     ms, _, value = aggregate(ms, tokens_rank, ws, dev)
 
     per_T = {}
-    fu_bytes = 0
-    fu_time = 0.0
+    pair_bytes = 0
     for i, T in enumerate(li.DECODE_T):
         idx = pool[0][i]["case"].token_idx
         sb, sf, eb, ef = algorithmic(idx)
         fb, ff = algorithmic_fused(idx)
-        fu_bytes += fb
-        fu_time += fu_ms[i] / 1e3
-        per_T[str(T)] = {"fused_us": fu_ms[i] * 1e3,
-                         "fused_GBps": fb / (fu_ms[i] / 1e3) / 1e9,
-                         "group_us": gr_ms[i] * 1e3,
+        pair_bytes += fb
+        per_T[str(T)] = {"pair_us": pair_ms[i] * 1e3,
+                         "pair_GBps": fb / (pair_ms[i] / 1e3) / 1e9,
                          "shrink_us": sh_ms[i] * 1e3,
                          "shrink_GBps": sb / (sh_ms[i] / 1e3) / 1e9,
                          "expand_us": ex_ms[i] * 1e3,
                          "expand_GBps": eb / (ex_ms[i] / 1e3) / 1e9,
-                         "fused_bytes": fb, "shrink_bytes": sb, "expand_bytes": eb}
+                         "grouped": {"group_us": gr_ms[i] * 1e3, "pair_us": gpair_ms[i] * 1e3,
+                                     "shrink_us": gsh_ms[i] * 1e3, "expand_us": gex_ms[i] * 1e3},
+                         "pair_bytes": fb, "shrink_bytes": sb, "expand_bytes": eb}
     hbm, tf, src = peaks()
-    # dominant kernel: the largest summed per-step time among the three
+    # dominant kernel: the larger summed per-step time of the step's two
     # kernels; its roofline is taken on its launch for the largest batch
     # (algorithmic bytes of that launch / its measured duration), with the
     # all-batch figure beside it
-    kern = {"shrink": (sh_ms, "shrink_bytes"), "expand_slice": (ex_ms, "expand_bytes"),
-            "grouping": (gr_ms, None)}
-    dom = max(("shrink", "expand_slice"), key=lambda k: sum(kern[k][0]))
+    kern = {"bgmv_shrink": (sh_ms, "shrink_bytes"), "bgmv_expand_slice": (ex_ms, "expand_bytes")}
+    dom = max(kern, key=lambda k: sum(kern[k][0]))
     dom_ms, dom_key = kern[dom]
     Tmax = str(li.DECODE_T[-1])
     achieved = per_T[Tmax][dom_key] / (dom_ms[-1] / 1e3) / 1e9
     all_achieved = sum(v[dom_key] for v in per_T.values()) / (sum(dom_ms) / 1e3) / 1e9
     step_s = ms / 1e3 / K
-    path_frac = (fu_bytes / (hbm * 1e9)) / step_s
+    path_frac = (pair_bytes / (hbm * 1e9)) / step_s
     traffic = NCU_TRAFFIC.get(dom)
 
-    e2e_v, h2d, d2h, e2e_wall = e2e_run(lg, dev, max(10, min(K, 300)), 3)
+    e2e_v, h2d, d2h, e2e_wall, h2d_gbs, d2h_gbs = e2e_run(lg, dev, max(10, min(K, 300)), 3)
 
     res = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
@@ -686,29 +935,40 @@ def main_ours(args):
                    "l2": f"rotating argument pool of {nsets} sets ({pool_bytes / 1e6:.0f} MB "
                          f">= 4x L2 {props.L2_cache_size / 1e6:.0f} MB): inputs larger than L2",
                    "launch": "each step replayed from a CUDA graph (one per pool set); the "
-                             "five independent batches are concurrent branches of the graph"},
+                             "five independent batches are concurrent branches of the graph",
+                   "path": "plan-free BGMV: per batch one lora_bgmv_shrink_expand_slice call "
+                           "(shrink and expand_slice kernels chained, no grouping)"},
         "sequential_batches": {"value": tokens_rank * ws / (seq_ms / 1e3), "unit": "tokens/s",
                                "ms_per_step": seq_ms / K},
+        "grouped_path": {"value": tokens_rank * ws / (grp_ms / 1e3), "unit": "tokens/s",
+                         "ms_per_step": grp_ms / K,
+                         "how": "the same steps through lora_group_tokens + the chained grouped "
+                                "operators (3 launches per batch)"},
         "roofline": {"kernel": dom, "launch": f"T={Tmax} batch", "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"{src} hbm_gbs",
                      "traffic": traffic["bytes"] if traffic else None,
                      "traffic_source": traffic["source"] if traffic else None,
                      "all_batches_achieved": all_achieved, "timing": ex_src},
-        "step_time_share": {k: sum(v[0]) / (sum(sh_ms) + sum(ex_ms) + sum(gr_ms))
-                            for k, v in kern.items()},
+        "step_time_share": {k: sum(v[0]) / (sum(sh_ms) + sum(ex_ms)) for k, v in kern.items()},
         "path_roofline_frac": path_frac,
-        # per batch: grouping, then shrink and expand_slice (chained or not)
-        "gpu_launches": K * nb * 3,
+        # per batch: the shrink and the expand_slice kernel
+        "gpu_launches": K * nb * LAUNCHES_PER_BATCH[STEP_PATH],
         "e2e": {"value": e2e_v, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "wall_tokens_per_s": e2e_wall,
-                "how": "public Python API per call (no graph), pinned host buffers"},
+                "host_link_GBps": {"h2d": h2d_gbs, "d2h": d2h_gbs},
+                "how": "public Python API per call (no graph); each step one packed upload "
+                       "from pinned memory and one download of the outputs, double-buffered "
+                       "on copy streams"},
         "clocks": clk,
         "per_T": per_T,
         "prefill_sgmv": prefill_sgmv(lg, dev, hbm, tf),
         "next_rows": next_rows(lg, dev, hbm),
         "wall_s_timed": wall,
     }
+    if not args.quick:
+        res["mixed_rank"] = mixed_rank_rows(lg, dev, hbm)
+        res["sweep"] = sweep_rows(lg, dev, hbm)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if rank == 0:
@@ -810,6 +1070,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="skip the mixed-rank and sweep sections")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-budget-s", type=float, default=90.0)
     ap.add_argument("--profile", action="store_true",

@@ -235,6 +235,25 @@ def mixed_rank_70b(N: int = 8192, seed: Optional[int] = None, T: int = 2048, H: 
     return case
 
 
+def mixed_rank_map(T: int = 2048, L: int = 32, seed: Optional[int] = None,
+                   inactive: float = 0.05, sgmv: bool = False):
+    """The token -> adapter structure of the mixed-rank workload without its
+    tensors (for timing runs that draw the tensors on the device): ranks [L]
+    uniform over MIXED_RANKS, Zipf(1.1) adapter per token with exactly
+    round(inactive * T) tokens at -1.  Same recipe as ``mixed_rank_70b``, own
+    random stream.  Returns (ranks, token_idx) or, with sgmv, (ranks,
+    (seg_start, seg_len, seg_lora)) over the tokens sorted by adapter."""
+    g = _gen(SEED_BASE + 40 if seed is None else seed)
+    choices = torch.tensor(MIXED_RANKS, dtype=torch.int32)
+    ranks = choices[torch.randint(0, len(MIXED_RANKS), (L,), generator=g)]
+    ids = zipf_ids(g, T, L)
+    ids[_exact_inactive(g, T, inactive)] = -1
+    if not sgmv:
+        return ranks, ids
+    sid, _ = torch.sort(ids.to(torch.int64), stable=True)
+    return ranks, _segments_from_sorted(sid.to(torch.int32))
+
+
 def sweep(H: int, batch: int, seq_len: int, seed: Optional[int] = None, r: int = 16,
           L: int = 4, dtype=torch.float16, which: str = "both") -> Case:
     """One point of the microbenchmark sweep: N = H, add_inputs=True, sorted ids."""
