@@ -562,22 +562,32 @@ def make_pool(dev, rank: int, l2_bytes: int, only_T=None):
 NCU_TRAFFIC = {
     "shrink": {"bytes": 9177344, "source": "ncu --set full, dram__bytes_read.sum 9.177 MB + "
                "dram__bytes_write.sum 0 (y stays in L2), T=1024 launch (tcgen05 variant)"},
-    "expand_slice": {"bytes": 12329984, "source": "ncu --set full, dram__bytes_read.sum 12.33 MB + "
-                     "dram__bytes_write.sum 0 (out written back after the launch), T=1024 launch"},
 }
 
 
-# The decode step's path: "bgmv" = the plan-free operators (no grouping; the
-# stacked q/k/v shrink and the three-slice expand chained in one call),
-# "grouped" = BGMV grouping into a plan, then the chained grouped operators.
-STEP_PATH = "bgmv"
+# The decode step's path: "grouped" = BGMV grouping into a plan, then the
+# chained grouped operators (the faster of the two on the decode step);
+# "bgmv" = the plan-free operators (no grouping; the stacked q/k/v shrink and
+# the three-slice expand chained in one call), timed beside it.
+STEP_PATH = "grouped"
+# "hybrid": the plan-free operators for batches of at most HYBRID_MAX_T tokens
+# (where they match the grouped path and save the grouping launch), the
+# grouped ones above
+HYBRID_MAX_T = 256
 LAUNCHES_PER_BATCH = {"bgmv": 2, "grouped": 3}
+
+
+def step_launches(path: str) -> int:
+    """Kernel launches of one decode step (all five batches) on `path`."""
+    if path == "hybrid":
+        return sum(2 if T <= HYBRID_MAX_T else 3 for T in li.DECODE_T)
+    return LAUNCHES_PER_BATCH[path] * len(li.DECODE_T)
 
 
 def run_step(lg, batches, path: str = STEP_PATH):
     """One decode step over `batches` (q/k/v shrink and expand_slice per batch)."""
     for b in batches:
-        if path == "bgmv":
+        if path == "bgmv" or (path == "hybrid" and b["T"] <= HYBRID_MAX_T):
             lg.lora_bgmv_shrink_expand_slice(b["x"], b["A"], b["y"], b["B"], b["out"],
                                              b["case"].slice_offsets, b["idx"], add_inputs=True)
         else:
@@ -837,13 +847,15 @@ def main_ours(args):
     nsets = len(pool)
     K, W = args.steps, args.warmup
 
+    others = [p for p in ("grouped", "bgmv", "hybrid") if p != STEP_PATH]
     for w in range(max(W, 1)):  # eager warm-up also configures the kernels before capture
         run_step(lg, pool[w % nsets])
-        run_step(lg, pool[w % nsets], path="grouped")
+        for p_ in others:
+            run_step(lg, pool[w % nsets], path=p_)
     torch.cuda.synchronize()
     graphs = capture_steps(lg, pool, concurrent=True)
     seq_graphs = capture_steps(lg, pool, concurrent=False)
-    grp_graphs = capture_steps(lg, pool, concurrent=True, path="grouped")
+    other_graphs = {p_: capture_steps(lg, pool, concurrent=True, path=p_) for p_ in others}
     for w in range(W):
         graphs[w % nsets].replay()
     torch.cuda.synchronize()
@@ -870,24 +882,30 @@ def main_ours(args):
     clk = clocks.stop()
 
     ms = start.elapsed_time(end)
-    seq_ms = time_graphs(seq_graphs, W, K)  # the same steps with the batches in sequence
-    grp_ms = time_graphs(grp_graphs, W, K)  # the same steps through the grouped operators
+    seq_ms = time_graphs(seq_graphs, W, K)      # the same steps with the batches in sequence
+    # the same steps through the other paths
+    other_ms = {p_: time_graphs(g_, W, K) for p_, g_ in other_graphs.items()}
 
-    # per batch size: the chained pair and its two kernels alone, on the
-    # plan-free path and (for reference) on the grouped one
+    # per batch size: the chained pair and its kernels alone, on both paths
     offs = pool[0][0]["case"].slice_offsets
-    pair_ms = op_only_ms(pool, lambda b: lg.lora_bgmv_shrink_expand_slice(
-        b["x"], b["A"], b["y"], b["B"], b["out"], offs, b["idx"], add_inputs=True))
-    sh_ms = op_only_ms(pool, lambda b: lg.lora_bgmv_shrink(b["x"], b["A"], b["y"], b["idx"],
-                                                           num_slices=len(SLICES)))
-    ex_ms = op_only_ms(pool, lambda b: lg.lora_bgmv_expand_slice(
-        b["y"], b["B"], b["out"], offs, b["idx"], y_slice_stride=R, add_inputs=True))
-    gpair_ms = op_only_ms(pool, lambda b: lg.lora_shrink_expand_slice(
-        b["x"], b["A"], b["y"], b["B"], b["out"], b["plan"], offs, add_inputs=True))
-    gsh_ms = op_only_ms(pool, lambda b: lg.lora_shrink(b["x"], b["A"], b["y"], b["plan"],
-                                                       num_slices=len(SLICES)))
-    gex_ms = expand_only_ms(lg, pool)
-    gr_ms = op_only_ms(pool, lambda b: lg.lora_group_tokens(b["idx"], L, b["plan"]))
+    times = {
+        "grouped": {
+            "pair": op_only_ms(pool, lambda b: lg.lora_shrink_expand_slice(
+                b["x"], b["A"], b["y"], b["B"], b["out"], b["plan"], offs, add_inputs=True)),
+            "shrink": op_only_ms(pool, lambda b: lg.lora_shrink(b["x"], b["A"], b["y"], b["plan"],
+                                                                num_slices=len(SLICES))),
+            "expand_slice": expand_only_ms(lg, pool),
+            "grouping": op_only_ms(pool, lambda b: lg.lora_group_tokens(b["idx"], L, b["plan"])),
+        },
+        "bgmv": {
+            "pair": op_only_ms(pool, lambda b: lg.lora_bgmv_shrink_expand_slice(
+                b["x"], b["A"], b["y"], b["B"], b["out"], offs, b["idx"], add_inputs=True)),
+            "shrink": op_only_ms(pool, lambda b: lg.lora_bgmv_shrink(
+                b["x"], b["A"], b["y"], b["idx"], num_slices=len(SLICES))),
+            "expand_slice": op_only_ms(pool, lambda b: lg.lora_bgmv_expand_slice(
+                b["y"], b["B"], b["out"], offs, b["idx"], y_slice_stride=R, add_inputs=True)),
+        },
+    }
     ex_src = (f"CUDA events around graphs of back-to-back launches, one per pool set "
               f"({nsets} sets, inputs from HBM), per batch size")
     tokens_rank = K * sum(li.DECODE_T)
@@ -900,29 +918,30 @@ def main_ours(args):
         sb, sf, eb, ef = algorithmic(idx)
         fb, ff = algorithmic_fused(idx)
         pair_bytes += fb
-        per_T[str(T)] = {"pair_us": pair_ms[i] * 1e3,
-                         "pair_GBps": fb / (pair_ms[i] / 1e3) / 1e9,
-                         "shrink_us": sh_ms[i] * 1e3,
-                         "shrink_GBps": sb / (sh_ms[i] / 1e3) / 1e9,
-                         "expand_us": ex_ms[i] * 1e3,
-                         "expand_GBps": eb / (ex_ms[i] / 1e3) / 1e9,
-                         "grouped": {"group_us": gr_ms[i] * 1e3, "pair_us": gpair_ms[i] * 1e3,
-                                     "shrink_us": gsh_ms[i] * 1e3, "expand_us": gex_ms[i] * 1e3},
-                         "pair_bytes": fb, "shrink_bytes": sb, "expand_bytes": eb}
+        row = {"shrink_bytes": sb, "expand_bytes": eb, "pair_bytes": fb}
+        for path, tk in times.items():
+            row[path] = {f"{k}_us": v[i] * 1e3 for k, v in tk.items()}
+            row[path]["shrink_GBps"] = sb / (tk["shrink"][i] / 1e3) / 1e9
+            row[path]["expand_GBps"] = eb / (tk["expand_slice"][i] / 1e3) / 1e9
+        per_T[str(T)] = row
     hbm, tf, src = peaks()
-    # dominant kernel: the larger summed per-step time of the step's two
-    # kernels; its roofline is taken on its launch for the largest batch
-    # (algorithmic bytes of that launch / its measured duration), with the
-    # all-batch figure beside it
-    kern = {"bgmv_shrink": (sh_ms, "shrink_bytes"), "bgmv_expand_slice": (ex_ms, "expand_bytes")}
-    dom = max(kern, key=lambda k: sum(kern[k][0]))
-    dom_ms, dom_key = kern[dom]
+    # dominant kernel: the largest summed per-step time among the operators of
+    # the path that runs the largest batch; its roofline is taken on its launch
+    # for the largest batch (algorithmic bytes of that launch / its measured
+    # duration), with the all-batch figure beside it
+    big_path = "grouped" if STEP_PATH in ("grouped", "hybrid") else "bgmv"
+    tk = times[big_path]
+    byte_key = {"shrink": "shrink_bytes", "expand_slice": "expand_bytes"}
+    dom = max(byte_key, key=lambda k: sum(tk[k]))
+    dom_ms, dom_key = tk[dom], byte_key[dom]
     Tmax = str(li.DECODE_T[-1])
     achieved = per_T[Tmax][dom_key] / (dom_ms[-1] / 1e3) / 1e9
     all_achieved = sum(v[dom_key] for v in per_T.values()) / (sum(dom_ms) / 1e3) / 1e9
     step_s = ms / 1e3 / K
     path_frac = (pair_bytes / (hbm * 1e9)) / step_s
-    traffic = NCU_TRAFFIC.get(dom)
+    dom_name = dom if big_path == "grouped" else f"bgmv_{dom}"
+    traffic = NCU_TRAFFIC.get(dom_name)
+    kernels = [k for k in tk if k != "pair"]
 
     e2e_v, h2d, d2h, e2e_wall, h2d_gbs, d2h_gbs = e2e_run(lg, dev, max(10, min(K, 300)), 3)
 
@@ -936,24 +955,25 @@ def main_ours(args):
                          f">= 4x L2 {props.L2_cache_size / 1e6:.0f} MB): inputs larger than L2",
                    "launch": "each step replayed from a CUDA graph (one per pool set); the "
                              "five independent batches are concurrent branches of the graph",
-                   "path": "plan-free BGMV: per batch one lora_bgmv_shrink_expand_slice call "
-                           "(shrink and expand_slice kernels chained, no grouping)"},
+                   "path": STEP_PATH},
         "sequential_batches": {"value": tokens_rank * ws / (seq_ms / 1e3), "unit": "tokens/s",
                                "ms_per_step": seq_ms / K},
-        "grouped_path": {"value": tokens_rank * ws / (grp_ms / 1e3), "unit": "tokens/s",
-                         "ms_per_step": grp_ms / K,
-                         "how": "the same steps through lora_group_tokens + the chained grouped "
-                                "operators (3 launches per batch)"},
-        "roofline": {"kernel": dom, "launch": f"T={Tmax} batch", "bound": "hbm",
+        "other_paths": {p_: {"value": tokens_rank * ws / (m_ / 1e3), "unit": "tokens/s",
+                             "ms_per_step": m_ / K} for p_, m_ in other_ms.items()},
+        "paths": {"grouped": "lora_group_tokens + the chained grouped operators, 3 launches "
+                             "per batch",
+                  "bgmv": "the chained plan-free operators, 2 launches per batch",
+                  "hybrid": f"bgmv for T <= {HYBRID_MAX_T}, grouped above"},
+        "roofline": {"kernel": dom_name, "launch": f"T={Tmax} batch", "bound": "hbm",
                      "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"{src} hbm_gbs",
                      "traffic": traffic["bytes"] if traffic else None,
                      "traffic_source": traffic["source"] if traffic else None,
                      "all_batches_achieved": all_achieved, "timing": ex_src},
-        "step_time_share": {k: sum(v[0]) / (sum(sh_ms) + sum(ex_ms)) for k, v in kern.items()},
+        "step_time_share": {k: sum(tk[k]) / sum(sum(tk[q]) for q in kernels) for k in kernels},
         "path_roofline_frac": path_frac,
-        # per batch: the shrink and the expand_slice kernel
-        "gpu_launches": K * nb * LAUNCHES_PER_BATCH[STEP_PATH],
+        # per batch: (grouping,) shrink and expand_slice
+        "gpu_launches": K * step_launches(STEP_PATH),
         "e2e": {"value": e2e_v, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "wall_tokens_per_s": e2e_wall,
                 "host_link_GBps": {"h2d": h2d_gbs, "d2h": d2h_gbs},

@@ -329,6 +329,53 @@ __device__ __forceinline__ ExpandItem expand_item(const BgmvExpandArgs &a, int i
     return it;
 }
 
+// One thread's part of the expand epilogue: NCOL columns (a multiple of 32)
+// from column cbeg of its token row.  `so` is the row's 128-byte slice of the
+// staged tile (box stride kBT * 128), `swz` the row's 16-byte swizzle.  All
+// TMEM loads are issued before one wait and all staged values are read
+// before the arithmetic, so the pieces are independent chains.
+template <typename E, bool ADD, int NCOL>
+__device__ __forceinline__ void epilogue_cols(uint32_t taddr, bool has_mma, bool live, float f,
+                                              unsigned char *so, int swz, int cbeg, int ncols,
+                                              int full_cols, E *orow) {
+    constexpr int NP = NCOL / 8;  // 16-byte pieces
+    uint32_t d[NCOL];
+    if (has_mma) {
+#pragma unroll
+        for (int j = 0; j < NCOL / 32; ++j)
+            tc_ld32_nowait(taddr + 32 * j, reinterpret_cast<uint32_t (&)[32]>(d[32 * j]));
+        tc_wait_ld();
+    } else {
+#pragma unroll
+        for (int q = 0; q < NCOL; ++q) d[q] = 0u;
+    }
+    if (!live) return;
+    uint4 *slot[NP];
+    uint4 old[NP];
+#pragma unroll
+    for (int g = 0; g < NP; ++g) {
+        const int c = cbeg + 8 * g;
+        slot[g] = reinterpret_cast<uint4 *>(so + (c >> 6) * kBT * 128 + ((((c & 63) >> 3) ^ swz) << 4));
+        if (ADD) old[g] = *slot[g];
+    }
+#pragma unroll
+    for (int g = 0; g < NP; ++g) {
+        const int c = cbeg + 8 * g;
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = f * __uint_as_float(d[8 * g + q]);
+        if (ADD) {
+            float o[8];
+            unpack8<E>(old[g], o);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] += o[q];
+        }
+        const uint4 w = pack8<E>(v);
+        if (c < full_cols) *slot[g] = w;
+        else if (c < ncols) st_global_v4(orow + c, w);
+    }
+}
+
 // KSY: 16-wide K steps per adapter (ranks padded to RP = 16 * KSY).
 template <typename E, bool ADD, int KSY>
 __global__ void __launch_bounds__(kEThreads)
@@ -395,9 +442,16 @@ bgmv_expand_kernel(const __grid_constant__ CUtensorMap tm_out, const BgmvExpandA
         tma_prefetch_map(&tm_out);
     }
     // The first two items' loads go out before the wait for the previous
-    // kernel: out and B are not written by it (y is).
+    // kernel: out and B are not written by it (y is), nor is the index array
+    // (the first block's entry of this thread is read now too).
     if (count > 0) issue(i0, 0, false);
     if (count > 1) issue(i0 + 1, 1, false);
+    int idx_pre = -1, idx_blk = -1;
+    if (count > 0) {
+        idx_blk = expand_item(a, i0, nchunks, nc).t0;
+        const int t = idx_blk + (tid & (kBT - 1));
+        if (t < a.T) idx_pre = a.idx ? __ldg(a.idx + t) : 0;
+    }
     grid_dep_wait();
     grid_dep_launch();
     // Tensor memory is taken only after that wait: a CTA holding TMEM never
@@ -428,7 +482,7 @@ bgmv_expand_kernel(const __grid_constant__ CUtensorMap tm_out, const BgmvExpandA
             const int t = it.t0 + r;
             int l = -1, rl = 0;
             if (t < a.T) {
-                const int v = a.idx ? __ldg(a.idx + t) : 0;
+                const int v = it.t0 == idx_blk ? idx_pre : (a.idx ? __ldg(a.idx + t) : 0);
                 if (v >= 0 && v < a.L) {
                     rl = clamp_rank(a.ranks, v, R);
                     if (rl > 0) l = v;
@@ -527,7 +581,8 @@ bgmv_expand_kernel(const __grid_constant__ CUtensorMap tm_out, const BgmvExpandA
             break;
         }
         tc_fence_after();
-        // epilogue: this thread's token row, its half of the chunk's columns;
+        // epilogue: this thread's token row, its half of the chunk's columns
+        // (32 or 64), all TMEM loads and staged values in flight at once;
         // full 64-column boxes are updated in shared memory for the TMA
         // stores, the columns of a ragged last box are stored directly
         const int full_cols = (it.ncols / kBox) * kBox;
@@ -537,35 +592,15 @@ bgmv_expand_kernel(const __grid_constant__ CUtensorMap tm_out, const BgmvExpandA
             const float f = s_f[r];
             const int cbeg = half * (nc / 2);
             const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)cbeg;
-            E *orow = out + (int64_t)t * a.ldo + it.col0;
-            unsigned char *so = sOut(b);
-            for (int cc = 0; cc < nc / 2 && cbeg + cc < it.ncols; cc += 32) {  // warp-uniform
-                float d[32];
-                if (present) {
-                    tc_ld32(taddr + (uint32_t)cc, d);
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) d[q] = 0.f;
-                }
-                if (!live) continue;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const int c = cbeg + cc + 8 * g;
-                    if (c >= it.ncols) break;
-                    float v[8];
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) v[q] = f * d[8 * g + q];
-                    uint4 *slot = reinterpret_cast<uint4 *>(
-                        so + (c >> 6) * kBT * 128 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4));
-                    if (ADD) {
-                        float o[8];
-                        unpack8<E>(*slot, o);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) v[q] += o[q];
-                    }
-                    if (c < full_cols) *slot = pack8<E>(v);
-                    else st_global_v4(orow + c, pack8<E>(v));
-                }
+            unsigned char *so = sOut(b) + r * 128;
+            const int swz = r & 7;
+            if (nc == 128) {
+                if (cbeg < it.ncols)
+                    epilogue_cols<E, ADD, 64>(taddr, present != 0, live, f, so, swz, cbeg,
+                                              it.ncols, full_cols, out + (int64_t)t * a.ldo + it.col0);
+            } else if (cbeg < it.ncols) {
+                epilogue_cols<E, ADD, 32>(taddr, present != 0, live, f, so, swz, cbeg, it.ncols,
+                                          full_cols, out + (int64_t)t * a.ldo + it.col0);
             }
         }
         fence_proxy_async_smem();  // the updated tile -> the TMA stores
