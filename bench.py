@@ -23,6 +23,7 @@ import subprocess
 import sys
 import threading
 import time
+from typing import Optional
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -228,6 +229,12 @@ def next_rows(lg, dev, hbm_gbs: float):
 
         t_ex, n = pool_op_us(mk, lambda a: lg.lora_expand(a["y"], a["B"], a["out"], plan,
                                                           add_inputs=False), sb, l2)
+        # the plan-free operator on the same batch: per-token indices, or none
+        # at all when one adapter serves every token (the mask-free case)
+        single = U == 1 and int(c.seg_lora[0]) == 0 and int(c.seg_len.sum()) == T
+        idx_d = None if single else c.lora_of_token().to(dev)
+        t_bg, _ = pool_op_us(mk, lambda a: lg.lora_bgmv_expand_slice(
+            a["y"], [a["B"]], a["out"], [0], idx_d, y_slice_stride=0, add_inputs=False), sb, l2)
         a16 = y0.to(torch.float16)
         b16 = B0[0].t().contiguous()
 
@@ -239,6 +246,9 @@ def next_rows(lg, dev, hbm_gbs: float):
         t_mm, _ = pool_op_us(mk_mm, lambda a: torch.mm(a["a"], a["b"], out=a["c"]), mm_bytes, l2)
         return {"workload": tag, "expand_us": t_ex, "expand_GBps": ex_bytes / t_ex / 1e3,
                 "expand_roofline_frac": ex_bytes / (hbm_gbs * 1e3) / t_ex,
+                "plan_free_expand_us": t_bg,
+                "plan_free_form": "no index (one adapter, mask-free)" if single
+                                  else "per-token index",
                 "torch_mm_us": t_mm, "torch_mm_roofline_frac": mm_bytes / (hbm_gbs * 1e3) / t_mm,
                 "pool_sets": n}
 
@@ -787,13 +797,17 @@ def time_graphs(graphs, W: int, K: int):
     return start.elapsed_time(end)
 
 
-def op_only_ms(pool, launch, reps: int = 20):
+def op_only_ms(pool, launch, reps: int = 20, max_T: Optional[int] = None):
     """Average duration of one operator per batch size: a graph of one launch
     per pool set (each on a different set, so inputs come from HBM), replayed
-    `reps` times between two events on the launching stream."""
+    `reps` times between two events on the launching stream.  Batch sizes
+    above `max_T` get None."""
     res = []
     stream = torch.cuda.Stream()
     for i in range(len(li.DECODE_T)):
+        if max_T is not None and li.DECODE_T[i] > max_T:
+            res.append(None)
+            continue
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for batches in pool:
@@ -906,6 +920,10 @@ def main_ours(args):
                 b["y"], b["B"], b["out"], offs, b["idx"], y_slice_stride=R, add_inputs=True)),
         },
     }
+    # the same decode pair as one cooperative launch (batches of at most 256 tokens)
+    fused_ms = op_only_ms(pool, lambda b: lg.lora_bgmv_fused_shrink_expand_slice(
+        b["x"], b["A"], b["y"], b["B"], b["out"], offs, b["idx"], add_inputs=True),
+        max_T=lg.FUSED_MAX_TOKENS)
     ex_src = (f"CUDA events around graphs of back-to-back launches, one per pool set "
               f"({nsets} sets, inputs from HBM), per batch size")
     tokens_rank = K * sum(li.DECODE_T)
@@ -923,6 +941,9 @@ def main_ours(args):
             row[path] = {f"{k}_us": v[i] * 1e3 for k, v in tk.items()}
             row[path]["shrink_GBps"] = sb / (tk["shrink"][i] / 1e3) / 1e9
             row[path]["expand_GBps"] = eb / (tk["expand_slice"][i] / 1e3) / 1e9
+        if fused_ms[i] is not None:
+            row["fused_one_launch"] = {"pair_us": fused_ms[i] * 1e3,
+                                       "pair_GBps": fb / (fused_ms[i] / 1e3) / 1e9}
         per_T[str(T)] = row
     hbm, tf, src = peaks()
     # dominant kernel: the largest summed per-step time among the operators of

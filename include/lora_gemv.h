@@ -287,10 +287,12 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
  *           multiples of 8, every B_s 16-byte aligned.
  * With a rank table, rows / columns >= r_l are never used in the result (the
  * shrink reads A rows up to R and discards the extra products).
- * The expand writes out back in 64-column tiles of 128 token rows: with
- * add_inputs, the rows of tokens without a LoRA term are rewritten with the
- * values just read (their contents do not change, but out must not be
- * written concurrently by other work); without add_inputs they become zero.
+ * For R > 32 or T > 256 the expand writes out back in 64-column tiles of 128
+ * token rows: with add_inputs, the rows of tokens without a LoRA term are
+ * rewritten with the values just read (their contents do not change, but out
+ * must not be written concurrently by other work); without add_inputs they
+ * become zero.  For R <= 32 and T <= 256 (the fp32 FMA expand) those rows
+ * are left alone with add_inputs.
  * Columns outside the slices are never written.
  * Errors: as the grouped operators (no plan argument), plus
  * LORA_ERR_UNSUPPORTED for shapes outside the list above.
@@ -323,6 +325,34 @@ lora_status_t lora_bgmv_shrink_expand_slice(lora_dtype_t dtype, const int32_t *t
                                             void *out, int64_t ldo, float scale_shrink,
                                             float scale_expand, int add_inputs, int32_t *status,
                                             lora_stream_t stream);
+
+/*
+ * The same result as lora_bgmv_shrink_expand_slice (y included) from ONE
+ * kernel launch: a cooperative launch of clusters of 8 CTAs (at most one CTA
+ * per SM) in two phases separated by a grid-wide barrier.  Phase one: the
+ * shrink, one (adapter, slice) per cluster, K split over the cluster's CTAs
+ * and the partial products added in distributed shared memory in a fixed
+ * order; phase two: the expand.  It answers the fixed cost of the two
+ * launches a decode step otherwise pays per layer, the cost the split into
+ * shrink and expand kernels brings (vLLM PR #15655, the summary list).
+ *
+ * Arguments, layouts and ownership are those of lora_bgmv_shrink_expand_slice
+ * (there is no status word: the kernel has no bounded waits).  Shapes taken,
+ * in addition to those of the two halves: T <= LORA_FUSED_MAX_TOKENS,
+ * R <= 32.  y and out do not change from run to run and stay within the
+ * bounds of the two-launch form.  With add_inputs, rows without a LoRA term
+ * are never written.
+ * Errors: as lora_bgmv_shrink_expand_slice, plus LORA_ERR_UNSUPPORTED for
+ * shapes outside the list and on devices where the kernel's clusters do not
+ * fit; LORA_ERR_CUDA if the cooperative launch is refused.
+ */
+#define LORA_FUSED_MAX_TOKENS 256
+lora_status_t lora_bgmv_fused_shrink_expand_slice(
+    lora_dtype_t dtype, const int32_t *token_idx, const void *x, int64_t ldx, int32_t T, int32_t H,
+    const void *A, int32_t L, int32_t R, const int32_t *ranks, float *y, int64_t ldy,
+    int32_t num_slices, const void *const *B_slices, const int32_t *slice_N,
+    const int32_t *slice_offset, void *out, int64_t ldo, float scale_shrink, float scale_expand,
+    int add_inputs, lora_stream_t stream);
 
 /*
  * lora_shrink_expand_slice for callers that cannot allocate device memory.

@@ -45,9 +45,11 @@ EXPORTS = ("lora_plan_layout", "lora_workspace_size", "lora_group_tokens",
            "lora_group_segments", "lora_shrink", "lora_expand", "lora_expand_slice",
            "lora_shrink_expand_slice", "lora_shrink_expand_slice_noalloc", "lora_get_error",
            "lora_status_string", "lora_last_error_detail", "lora_version", "lora_bgmv_shrink",
-           "lora_bgmv_expand_slice", "lora_bgmv_shrink_expand_slice")
+           "lora_bgmv_expand_slice", "lora_bgmv_shrink_expand_slice",
+           "lora_bgmv_fused_shrink_expand_slice")
 NOALLOC_MAX_TOKENS = 4096
 BGMV_MAX_ADAPTERS = 8
+FUSED_MAX_TOKENS = 256
 
 _lib = None
 
@@ -115,6 +117,11 @@ def load():
                                                   ctypes.POINTER(i32), ctypes.POINTER(i32), vp,
                                                   i64, f32, f32, ctypes.c_int, vp, vp]
     lib.lora_bgmv_shrink_expand_slice.restype = st
+    lib.lora_bgmv_fused_shrink_expand_slice.argtypes = [st, vp, vp, i64, i32, i32, vp, i32, i32, vp,
+                                                        vp, i64, i32, ctypes.POINTER(vp),
+                                                        ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                                        vp, i64, f32, f32, ctypes.c_int, vp]
+    lib.lora_bgmv_fused_shrink_expand_slice.restype = st
     lib.lora_get_error.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32), vp]
     lib.lora_get_error.restype = st
     lib.lora_status_string.argtypes = [st]
@@ -446,6 +453,32 @@ def lora_bgmv_shrink_expand_slice(x: torch.Tensor, A: torch.Tensor, y: torch.Ten
                                   add_inputs: bool = True,
                                   status: Optional[torch.Tensor] = None) -> None:
     """Plan-free shrink then expand_slice (y_slice_stride = R), chained."""
+    T, H, L, R, S, ptrs, Ns, offs = _pair_args(x, A, y, B_slices, out, slice_offsets, token_idx)
+    _check(load().lora_bgmv_shrink_expand_slice(
+        _dtype(x), _i32(token_idx, "token_idx"), _dev(x, "x"), _rows(x, "x"), T, H, _dev(A, "A"),
+        L, R, _i32(ranks, "ranks"), _dev(y, "y"), _rows(y, "y"), S, ptrs, Ns, offs,
+        _dev(out, "out"), _rows(out, "out"), float(scale_shrink), float(scale_expand),
+        int(bool(add_inputs)), _i32(status, "status"), _stream(x)))
+
+
+def lora_bgmv_fused_shrink_expand_slice(x: torch.Tensor, A: torch.Tensor, y: torch.Tensor,
+                                        B_slices: Sequence[torch.Tensor], out: torch.Tensor,
+                                        slice_offsets: Sequence[int],
+                                        token_idx: Optional[torch.Tensor], *,
+                                        ranks: Optional[torch.Tensor] = None,
+                                        scale_shrink: float = 1.0, scale_expand: float = 1.0,
+                                        add_inputs: bool = True) -> None:
+    """lora_bgmv_shrink_expand_slice as one cooperative kernel launch
+    (T <= FUSED_MAX_TOKENS, R <= 32)."""
+    T, H, L, R, S, ptrs, Ns, offs = _pair_args(x, A, y, B_slices, out, slice_offsets, token_idx)
+    _check(load().lora_bgmv_fused_shrink_expand_slice(
+        _dtype(x), _i32(token_idx, "token_idx"), _dev(x, "x"), _rows(x, "x"), T, H, _dev(A, "A"),
+        L, R, _i32(ranks, "ranks"), _dev(y, "y"), _rows(y, "y"), S, ptrs, Ns, offs,
+        _dev(out, "out"), _rows(out, "out"), float(scale_shrink), float(scale_expand),
+        int(bool(add_inputs)), _stream(x)))
+
+
+def _pair_args(x, A, y, B_slices, out, slice_offsets, token_idx):
     T, H = x.shape
     if A.dim() != 3 or not A.is_contiguous() or A.shape[2] != H or A.dtype != x.dtype:
         raise ValueError("A must be a contiguous [L, S*R, H] tensor of x's dtype")
@@ -461,8 +494,4 @@ def lora_bgmv_shrink_expand_slice(x: torch.Tensor, A: torch.Tensor, y: torch.Ten
         raise ValueError("y must be fp32 [T, >= S*R]")
     if token_idx is not None and token_idx.numel() != T:
         raise ValueError("token_idx must hold one index per row of x")
-    _check(load().lora_bgmv_shrink_expand_slice(
-        _dtype(x), _i32(token_idx, "token_idx"), _dev(x, "x"), _rows(x, "x"), T, H, _dev(A, "A"),
-        L, R, _i32(ranks, "ranks"), _dev(y, "y"), _rows(y, "y"), S, ptrs, Ns, offs,
-        _dev(out, "out"), _rows(out, "out"), float(scale_shrink), float(scale_expand),
-        int(bool(add_inputs)), _i32(status, "status"), _stream(x)))
+    return T, H, L, R, S, ptrs, Ns, offs

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblora_gemv.so")
-SOURCES = ["api.cu", "plan.cu", "shrink.cu", "expand.cu", "bgmv.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "plan.cu", "shrink.cu", "expand.cu", "bgmv.cu", "decode_fused.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -38,7 +38,8 @@ cudaError_t init_device(int dev, lora::DeviceInfo *info) {
     if ((e = lora::configure_plan_kernels()) != cudaSuccess) return e;
     if ((e = lora::configure_shrink_kernels(info)) != cudaSuccess) return e;
     if ((e = lora::configure_expand_kernels()) != cudaSuccess) return e;
-    return lora::configure_bgmv_kernels(*info);
+    if ((e = lora::configure_bgmv_kernels(*info)) != cudaSuccess) return e;
+    return lora::configure_fused_kernels(*info);
 }
 
 // Per-device kernel attributes are set once, on the first call on that device.
@@ -543,7 +544,9 @@ lora_status_t lora_bgmv_shrink(lora_dtype_t dtype, const int32_t *token_idx, con
     if (T == 0) return LORA_OK;
     const lora::DeviceInfo *dev;
     if ((st = device_info(&dev)) != LORA_OK) return st;
-    cudaError_t e = lora::launch_bgmv_shrink(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream));
+    // programmatic launch: only the launch overlaps the previous kernel's
+    // tail; every read waits for it
+    cudaError_t e = lora::launch_bgmv_shrink(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream), true);
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "bgmv shrink launch");
 }
 
@@ -565,7 +568,9 @@ lora_status_t lora_bgmv_expand_slice(lora_dtype_t dtype, const int32_t *token_id
     if (T == 0) return LORA_OK;
     const lora::DeviceInfo *dev;
     if ((st = device_info(&dev)) != LORA_OK) return st;
-    cudaError_t e = lora::launch_bgmv_expand(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream));
+    // programmatic launch with early = 0: only the launch overlaps the
+    // previous kernel's tail; every read waits for it
+    cudaError_t e = lora::launch_bgmv_expand(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream), true);
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "bgmv expand launch");
 }
 
@@ -583,9 +588,10 @@ lora_status_t lora_bgmv_shrink_expand_slice(
     if (st != LORA_OK) return st;
     const lora::BgmvShrinkArgs sa = bgmv_shrink_args(token_idx, x, ldx, T, H, A, L, R, num_slices,
                                                      ranks, y, ldy, scale_shrink, 0, status);
-    const lora::BgmvExpandArgs ea =
+    lora::BgmvExpandArgs ea =
         bgmv_expand_args(token_idx, y, ldy, T, num_slices, B_slices, slice_N, slice_offset, R, L,
                          R, ranks, out, ldo, scale_expand, add_inputs, status);
+    ea.early = 1;  // the shrink writes only y
     if (const char *why = lora::bgmv_shrink_supported(sa)) return fail(LORA_ERR_UNSUPPORTED, "%s", why);
     if (const char *why = lora::bgmv_expand_supported(ea)) return fail(LORA_ERR_UNSUPPORTED, "%s", why);
     if (T == 0) return LORA_OK;
@@ -597,6 +603,33 @@ lora_status_t lora_bgmv_shrink_expand_slice(
     cudaError_t e = lora::launch_bgmv_shrink(dtype, sa, *dev, cs, true);
     if (e == cudaSuccess) e = lora::launch_bgmv_expand(dtype, ea, *dev, cs, true);
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "bgmv shrink_expand_slice launch");
+}
+
+lora_status_t lora_bgmv_fused_shrink_expand_slice(
+    lora_dtype_t dtype, const int32_t *token_idx, const void *x, int64_t ldx, int32_t T, int32_t H,
+    const void *A, int32_t L, int32_t R, const int32_t *ranks, float *y, int64_t ldy,
+    int32_t num_slices, const void *const *B_slices, const int32_t *slice_N,
+    const int32_t *slice_offset, void *out, int64_t ldo, float scale_shrink, float scale_expand,
+    int add_inputs, lora_stream_t stream) {
+    lora_status_t st = check_bgmv_shrink(dtype, token_idx, x, ldx, T, H, A, L, R, num_slices,
+                                         ranks, y, ldy);
+    if (st != LORA_OK) return st;
+    st = check_bgmv_expand(dtype, token_idx, y, ldy, T, num_slices, B_slices, slice_N,
+                           slice_offset, R, L, R, ranks, out, ldo);
+    if (st != LORA_OK) return st;
+    const lora::BgmvShrinkArgs sa = bgmv_shrink_args(token_idx, x, ldx, T, H, A, L, R, num_slices,
+                                                     ranks, y, ldy, scale_shrink, 0, nullptr);
+    const lora::BgmvExpandArgs ea =
+        bgmv_expand_args(token_idx, y, ldy, T, num_slices, B_slices, slice_N, slice_offset, R, L,
+                         R, ranks, out, ldo, scale_expand, add_inputs, nullptr);
+    if (const char *why = lora::bgmv_shrink_supported(sa)) return fail(LORA_ERR_UNSUPPORTED, "%s", why);
+    if (const char *why = lora::bgmv_expand_supported(ea)) return fail(LORA_ERR_UNSUPPORTED, "%s", why);
+    const lora::DeviceInfo *dev;
+    if ((st = device_info(&dev)) != LORA_OK) return st;
+    if (const char *why = lora::bgmv_fused_supported(sa, ea)) return fail(LORA_ERR_UNSUPPORTED, "%s", why);
+    if (T == 0) return LORA_OK;
+    cudaError_t e = lora::launch_bgmv_fused(dtype, sa, ea, *dev, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? LORA_OK : cuda_fail(e, "bgmv fused shrink_expand_slice launch");
 }
 
 }  // extern "C"

@@ -116,6 +116,12 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
 }
+// This CTA's rank within its cluster.
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
 // The shared::cluster address of `addr` (a shared::cta address) in CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
     uint32_t r;

@@ -91,6 +91,10 @@ struct BgmvExpandArgs {
     void *out;
     int64_t ldo;
     int32_t *status;
+    // 1 when the previous kernel in the stream writes nothing the expand
+    // reads but y (the chained shrink): the token indices, B and out may be
+    // read before the wait for it.  0: every read waits.
+    int early;
 };
 
 struct DeviceInfo {
@@ -123,6 +127,14 @@ cudaError_t launch_bgmv_shrink(lora_dtype_t dt, const BgmvShrinkArgs &a, const D
                                cudaStream_t stream, bool pdl = false);
 cudaError_t launch_bgmv_expand(lora_dtype_t dt, const BgmvExpandArgs &a, const DeviceInfo &dev,
                                cudaStream_t stream, bool pdl = false);
+
+// One-launch decode pair (decode_fused.cu): a cooperative launch of clusters
+// of 8 CTAs.  Takes what both halves take plus T <= 256, R <= 32, a shrink
+// without add_inputs and packed y slices.
+cudaError_t configure_fused_kernels(const DeviceInfo &dev);
+const char *bgmv_fused_supported(const BgmvShrinkArgs &s, const BgmvExpandArgs &e);
+cudaError_t launch_bgmv_fused(lora_dtype_t dt, const BgmvShrinkArgs &s, const BgmvExpandArgs &e,
+                              const DeviceInfo &dev, cudaStream_t stream);
 
 // Host-side argument checks of the C ABI (api.cu): LORA_OK or the status the
 // operator would return, with lora_last_error_detail() set.

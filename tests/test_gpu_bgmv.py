@@ -134,6 +134,28 @@ def test_single_adapter_no_index(cuda_lib):
                 * abs(c.shrink_scale) + 1e-7).all()
 
 
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("T,R,rank,Ns,add", [
+    (200, 16, 7, [2048], True),         # rank below R, not a multiple of 4
+    (64, 24, 24, [96, 40], False),      # two slices, ragged 64-column chunks
+    (300, 32, 0, [512], True),          # rank 0 with add_inputs: out left alone
+    (130, 32, 0, [512], False),         # rank 0 without: zeros
+    (5000, 8, 8, [1024], True),         # many 64-token tiles
+])
+def test_single_adapter_ranks_and_slices(cuda_lib, dtype, T, R, rank, Ns, add):
+    """The one-adapter expand (no token index) with a rank table, several
+    slices and ragged column chunks."""
+    c = make_case(T, 512, R, 1, Ns, dtype, seed=T + R + rank, add=add, p_neg=0.0, ranks=[rank])
+    c.token_idx = None
+    rows = None if T <= 512 else np.sort(np.random.default_rng(T).choice(T, 256, replace=False))
+    y, out = check(cuda_lib, c, rows)
+    if rank == 0:
+        if add:
+            assert torch.equal(out.view(torch.int16), (c.out if rows is None else c.out[rows]).view(torch.int16))
+        else:
+            assert (out.float() == 0).all()
+
+
 # ---------------------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
@@ -146,6 +168,8 @@ def test_single_adapter_no_index(cuda_lib):
     (200, 4096, 64, 2, [384, 8], [64, 33]), # rank 64, a slice of 8 columns
     (65, 8192, 8, 8, [136], None),          # long K per CTA, ragged 8-column tail
     (256, 128, 32, 2, [64, 64], None),      # H below one cluster split
+    (2000, 1024, 64, 2, [4096], [64, 40]),  # rank 64: tensor-core expand, several items per CTA
+    (700, 512, 40, 2, [1024, 128], None),   # rank 40: tensor-core expand, ragged rows
 ])
 @pytest.mark.parametrize("add", [False, True])
 def test_edge_shapes(cuda_lib, dtype, T, H, R, L, Ns, ranks, add):
