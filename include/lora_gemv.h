@@ -100,6 +100,11 @@ enum {
 #define LORA_PLANERR_MISMATCH 4     /* an operator got a plan built for another T or L: it wrote nothing */
 #define LORA_PLANERR_TIMEOUT 8      /* a kernel's bounded wait for its cluster peers expired: its
                                        outputs for that call are not valid (never expected) */
+#define LORA_PLANERR_BOUNDS 16      /* LORA_DEBUG builds only: a plan entry read by an operator was
+                                       outside its range (a token row outside [-1, T), an adapter
+                                       id outside [-1, L), a tile row count outside [0, 64]).
+                                       Every build skips such entries (the row or the tile gets no
+                                       term); debug builds also count them here. */
 
 /*
  * Plan layout: byte offsets of each array inside the caller's plan buffer.

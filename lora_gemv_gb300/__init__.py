@@ -31,6 +31,7 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "liblora_gemv.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "liblora_gemv_debug.so")  # the LORA_DEBUG build
 
 LORA_F16, LORA_BF16 = 0, 1
 TILE_TOKENS = 64
@@ -39,6 +40,7 @@ MAX_SLICES = 8
 HDR_WORDS = 16
 HDR = dict(MAGIC=0, T=1, L=2, KIND=3, NACTIVE=4, NGROUPS=5, NTILES=6, BAD_IDS=7, ERR=8)
 PLANERR_SEG_RANGE, PLANERR_SEG_ORDER, PLANERR_MISMATCH, PLANERR_TIMEOUT = 1, 2, 4, 8
+PLANERR_BOUNDS = 16
 PLAN_MAGIC = 0x4C6F5241
 
 EXPORTS = ("lora_plan_layout", "lora_workspace_size", "lora_group_tokens",
@@ -52,6 +54,7 @@ BGMV_MAX_ADAPTERS = 8
 FUSED_MAX_TOKENS = 256
 
 _lib = None
+_lib_path = None
 
 
 class LoraError(RuntimeError):
@@ -66,15 +69,24 @@ class _Layout(ctypes.Structure):
                                              "max_tiles", "bytes")]
 
 
+def use_library(path: Optional[str] = None) -> None:
+    """Route every following call through the library at `path` (None: the
+    default build, LIB_PATH).  The LORA_DEBUG variant is DEBUG_LIB_PATH."""
+    global _lib, _lib_path
+    _lib_path = path or LIB_PATH
+    _lib = None
+
+
 def load():
     """Load the CUDA library (raises if it was not built)."""
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"{LIB_PATH} is missing: build it with lora_gemv_gb300.build.build() "
+    path = _lib_path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with lora_gemv_gb300.build.build() "
                            "(there is no CPU fallback)")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
     st = ctypes.c_int
     lib.lora_plan_layout.argtypes = [i32, i32, ctypes.POINTER(_Layout)]

@@ -2,7 +2,10 @@
 
 Each translation unit is compiled by nvcc in parallel, then linked into one
 shared library next to this file.  Sources newer than the library trigger a
-rebuild; ``force=True`` always rebuilds.
+rebuild; ``force=True`` always rebuilds.  ``debug=True`` builds the
+``LORA_DEBUG`` variant, ``liblora_gemv_debug.so``: the same kernels with
+device-side bounds checks on every plan entry they read, counted into the
+plan's error word (LORA_PLANERR_BOUNDS) instead of trapping.
 """
 from __future__ import annotations
 
@@ -17,6 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblora_gemv.so")
+OBJDIR_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "liblora_gemv_debug.so")
 SOURCES = ["api.cu", "plan.cu", "shrink.cu", "expand.cu", "bgmv.cu", "decode_fused.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
@@ -39,22 +44,25 @@ def _deps():
     return files
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(debug: bool = False) -> bool:
+    lib = LIB_DEBUG if debug else LIB
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not stale():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    lib, objdir = (LIB_DEBUG, OBJDIR_DEBUG) if debug else (LIB, OBJDIR)
+    flags = FLAGS + (["-DLORA_DEBUG"] if debug else [])
+    if not force and not stale(debug):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, src.replace(".cu", ".o"))
-        cmd = [cc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
+        cmd = [cc, *ARCH, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -64,13 +72,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -364,6 +364,27 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap *map) {
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;\n"); }
 
+// Plan entries outside their ranges (a token row outside [-1, T), an adapter
+// id outside [-1, L), a tile row count outside [0, kTile]) are skipped by
+// every build: the row reads as -1, the adapter as rank 0.  Builds with
+// LORA_DEBUG defined also count them, as LORA_PLANERR_BOUNDS in the plan's
+// error word (device-side bounds checks that neither trap nor stop).
+__device__ __forceinline__ void plan_check_row(int row, int T, int32_t *hdr) {
+#ifdef LORA_DEBUG
+    if (row < -1 || row >= T) atomicOr(hdr + LORA_HDR_ERR, LORA_PLANERR_BOUNDS);
+#else
+    (void)row, (void)T, (void)hdr;
+#endif
+}
+__device__ __forceinline__ void plan_check_tile(int4 tl, int L, int32_t *hdr) {
+#ifdef LORA_DEBUG
+    if (tl.x < -1 || tl.x >= L || tl.z < 0 || tl.z > kTile)
+        atomicOr(hdr + LORA_HDR_ERR, LORA_PLANERR_BOUNDS);
+#else
+    (void)tl, (void)L, (void)hdr;
+#endif
+}
+
 __device__ __forceinline__ int clamp_rank(const int32_t *ranks, int l, int R) {
     if (ranks == nullptr) return R;
     int r = __ldg(ranks + l);

@@ -88,9 +88,11 @@ expand_kernel(const ExpandArgs a) {
         if (tile + (int)gridDim.x < n_tiles) tl_next = __ldcg(a.tiles + tile + gridDim.x);
         const int l = tl.x, n = tl.z;
         const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
+        if (threadIdx.x == 0 && blockIdx.y == 0) plan_check_tile(tl, a.L, a.hdr);
 
         if (threadIdx.x < kTile) {
             int row = __ldcg(a.tile_rows + (int64_t)tile * kTile + threadIdx.x);
+            if (blockIdx.y == 0) plan_check_row(row, a.T, a.hdr);
             if (row >= a.T) row = -1;
             s_rows[threadIdx.x] = row;
         }
@@ -389,6 +391,18 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     rl = tl.x >= 0 && tl.x < a.L ? clamp_rank(a.ranks, tl.x, a.R) : 0;
     KS = (rl + 15) / 16;
     nrow = min(kWRows, tl.z - part * kWRows);
+    if (lane == 0) plan_check_tile(tl, a.L, a.hdr);
+#ifdef LORA_DEBUG
+    // (the rows above were read before the tile count was known; checked
+    // only now that this unit's tile is one of the plan's)
+    auto check_rows = [&](int tt, int pt) {
+        for (int mm = 0; mm < MB; ++mm)
+            for (int h = 0; h < 2; ++h)
+                plan_check_row(__ldg(a.tile_rows + (int64_t)tt * kTile + pt * kWRows + mm * 16 + g + 8 * h),
+                               a.T, a.hdr);
+    };
+    check_rows(t, part);
+#endif
 
     int s, c0;
     slice_of(cbi, s, c0);
@@ -425,10 +439,14 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
         if (new_rows) {
             if (nt != t) {
                 ntl = __ldg(a.tiles + nt);
+                if (lane == 0) plan_check_tile(ntl, a.L, a.hdr);
                 nrl = ntl.x >= 0 && ntl.x < a.L ? clamp_rank(a.ranks, ntl.x, a.R) : 0;
                 nKS = (nrl + 15) / 16;
             }
             load_rows(nt, npart, nrows_);
+#ifdef LORA_DEBUG
+            check_rows(nt, npart);
+#endif
             nnrow = min(kWRows, ntl.z - npart * kWRows);
         }
         int ns = s, nc0 = c0;
@@ -583,7 +601,11 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
                                          : -1;
             __syncthreads();  // the previous tile is done with s_rows / s_f
         }
-        if (threadIdx.x < kTile) s_rows[threadIdx.x] = my_row < a.T ? my_row : -1;
+        if (threadIdx.x < kTile) {
+            plan_check_row(my_row, a.T, a.hdr);
+            s_rows[threadIdx.x] = my_row < a.T ? my_row : -1;
+        }
+        if (threadIdx.x == 0) plan_check_tile(tl, a.L, a.hdr);
         const int l = tl.x, n = tl.z;
         const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, a.R) : 0;
         __syncthreads();

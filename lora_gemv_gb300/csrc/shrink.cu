@@ -277,6 +277,8 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
     const int n_tiles = min(h1.z, a.max_tiles);
     for (int tile = blockIdx.y; tile < n_tiles; tile += gridDim.y) {
         const int4 tl = tl_next;
+        if (threadIdx.x < kTile) plan_check_row(row_next, a.T, a.hdr);
+        if (threadIdx.x == 0 && kc == 0) plan_check_tile(tl, a.L, a.hdr);
         const int my_row = row_next < a.T ? row_next : -1;
         if (tile + (int)gridDim.y < n_tiles) {  // the next tile's record and rows, a tile ahead
             tl_next = __ldcg(a.tiles + tile + gridDim.y);

@@ -38,6 +38,16 @@ def test_exports_every_declared_function(lib):
     assert set(lg.EXPORTS) == names
 
 
+def test_debug_build_exports_every_declared_function():
+    """The LORA_DEBUG variant builds (cross-compiled here) and exports the
+    same C ABI."""
+    path = lgbuild.build(debug=True)
+    assert path.endswith("liblora_gemv_debug.so") and os.path.exists(path)
+    dlib = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(dlib, n), n
+
+
 def test_version_and_status_strings(lib):
     assert lib.lora_version() == 100
     for s in range(5):
