@@ -1070,8 +1070,8 @@ def _ref_step(oracle, prepared, rows):
 
 
 def main_profile(args):
-    """A few eager launches of the path on one decode batch, for profilers
-    (e.g. ncu -k regex:expand -s 2 -c 1 python bench.py --profile --T 1024),
+    """A few eager launches of the path (--path) on one decode batch, for
+    profilers (e.g. ncu -k regex:expand -s 2 -c 1 python bench.py --profile --T 1024),
     or with --prefill-r R on the prefill gate/up workload at rank R (grouping,
     shrink, expand_slice per repetition)."""
     dev = torch.device("cuda", 0)
@@ -1096,12 +1096,31 @@ def main_profile(args):
         print(json.dumps({"profile": True, "workload": "prefill_gateup", "r": r, "T": c.T,
                           "reps": args.profile_reps}))
         return
+    if args.path == "single":
+        # one adapter, no token index (the mask-free dense expand), at T rows
+        g = torch.Generator().manual_seed(li.SEED_BASE + 77)
+        y = torch.randn(args.T, 16, generator=g).to(dev)
+        B = (torch.randn(1, 2048, 16, generator=g) * 0.02).half().to(dev)
+        out = torch.empty(args.T, 2048, dtype=torch.float16, device=dev)
+        for _ in range(args.profile_reps):
+            lg.lora_bgmv_expand_slice(y, [B], out, [0], None, y_slice_stride=0, add_inputs=False)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": True, "path": "single", "T": args.T, "N": 2048, "r": 16,
+                          "reps": args.profile_reps}))
+        return
     pool, _ = make_pool(dev, 0, 0, only_T=args.T)
+    offs = pool[0][0]["case"].slice_offsets
     for _ in range(args.profile_reps):
         for batches in pool:
-            run_step(lg, batches)
+            if args.path == "fused":
+                for b in batches:
+                    lg.lora_bgmv_fused_shrink_expand_slice(b["x"], b["A"], b["y"], b["B"], b["out"],
+                                                           offs, b["idx"], add_inputs=True)
+            else:
+                run_step(lg, batches, path=args.path)
     torch.cuda.synchronize()
-    print(json.dumps({"profile": True, "T": args.T, "reps": args.profile_reps}))
+    print(json.dumps({"profile": True, "path": args.path, "T": args.T,
+                      "reps": args.profile_reps}))
 
 
 def main():
@@ -1119,6 +1138,9 @@ def main():
                     help="run a few eager steps of one decode batch (for ncu), no timing")
     ap.add_argument("--T", type=int, default=1024, help="batch size for --profile")
     ap.add_argument("--profile-reps", type=int, default=3)
+    ap.add_argument("--path", choices=["grouped", "bgmv", "fused", "single"], default=STEP_PATH,
+                    help="with --profile: the decode pair's path (single: the one-adapter "
+                         "expand at T x 2048, r = 16)")
     ap.add_argument("--prefill-r", type=int, default=0,
                     help="with --profile: the prefill gate/up workload at this rank instead")
     args = ap.parse_args()

@@ -5,8 +5,9 @@
 // (vLLM PR #15655, the summary list) costs, on every layer, a second launch
 // and a hand-off between grids; at decode sizes those fixed costs are most of
 // the time.  Here one grid (clusters of 8 CTAs, at most one CTA per SM) runs
-// its phases separated by the grid-wide barrier of a cooperative launch (the launch makes every CTA
-// resident at once, so the barrier completes, and no CTA leaves before it):
+// its phases separated by the grid-wide barrier of a cooperative launch (the
+// launch makes every CTA resident at once, so the barrier completes, and no
+// CTA leaves before it):
 //
 //   0. each CTA reads the token indices, requests what needs none (its shrink
 //      unit's A rows, its first expand tile's old out values), groups the
@@ -124,6 +125,9 @@ bgmv_fused_kernel(const BgmvShrinkArgs sa, const BgmvExpandArgs ea, int nchunks,
     __shared__ int s_wc[LORA_BGMV_MAX_ADAPTERS][kFThreads / 32];
     __shared__ int s_cnt[LORA_BGMV_MAX_ADAPTERS], s_beg[LORA_BGMV_MAX_ADAPTERS];
     cg::grid_group grid = cg::this_grid();
+    // Launched without the cooperative attribute (not by this library), the
+    // grid barrier has no storage: write nothing rather than wait on it.
+    if (!grid.is_valid()) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = sa.T, L = sa.L, R = sa.R, H = sa.H, S = sa.S, W = sa.S * sa.R;
     const int cr = (int)cluster_rank();              // this CTA's K range
