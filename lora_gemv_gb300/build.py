@@ -22,7 +22,8 @@ OBJDIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblora_gemv.so")
 OBJDIR_DEBUG = os.path.join(HERE, "_build_debug")
 LIB_DEBUG = os.path.join(HERE, "liblora_gemv_debug.so")
-SOURCES = ["api.cu", "plan.cu", "shrink.cu", "expand.cu", "bgmv.cu", "decode_fused.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "plan.cu", "shrink.cu", "expand.cu", "bgmv.cu", "decode_fused.cu", "noalloc.cu",
+           "tmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -1,6 +1,7 @@
 // Internal interface between the C ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -101,6 +102,12 @@ struct DeviceInfo {
     int sm_count;
     int max_cluster;  // largest split-K cluster the shrink kernel can be launched with
 };
+
+// 2-D fp16/bf16 tensor [rows][cols] with a row stride of `ld` elements: a TMA
+// map with boxes of box_rows x 64 columns (128 bytes) in the 128-byte
+// swizzled layout, zero fill outside (tmap.cu).
+cudaError_t make_tensor_map_2d(CUtensorMap *m, lora_dtype_t dt, const void *base, uint64_t rows,
+                               uint64_t cols, uint64_t ld, uint32_t box_rows);
 
 cudaError_t configure_plan_kernels();
 cudaError_t configure_bgmv_kernels(const DeviceInfo &dev);

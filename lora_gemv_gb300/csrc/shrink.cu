@@ -39,6 +39,8 @@
 //    zeroed unless add_inputs.
 #include <cooperative_groups.h>
 
+#include <string.h>
+
 #include <algorithm>
 #include <type_traits>
 
@@ -200,15 +202,21 @@ __device__ __forceinline__ void store_stage(const uint4 (&ld)[kMaxLd], unsigned 
 // push: reduce over the cluster through the receive buffers (ksplit > 1).
 // TC: the contraction on the tcgen05 tensor cores (aligned rows; D = X . A^T
 // with M = 128 token lanes, N = rows_cap, accumulated in TMEM), else mma.sync.
+// tma (TC only): tm_x maps x [T][H] in boxes of 64 rows, tm_a maps A [L*S*R][H]
+// in boxes of rows_cap rows; tiles whose token rows are consecutive and whose
+// adapter has rank R are staged by one thread's TMA copies instead of every
+// thread's cp.async.
 template <typename E, bool VEC, int NTMAX, bool KS, bool TC>
 __global__ void __launch_bounds__(kThreads)
-shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
+shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a,
+              const ShrinkArgs a, int kchunk, int rows_cap, int push, int tma) {
     static_assert(!TC || (VEC && !KS), "the tensor-core path takes aligned rows, no warp split");
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
     __shared__ int s_arow[kRows];
     __shared__ uint64_t s_bar;     // push: the cluster's partials of this CTA's rows have arrived
     __shared__ uint64_t s_mma[2];  // TC: the MMAs reading stage buffer b are done
+    __shared__ uint64_t s_full[2]; // TC with TMA: stage buffer b's copies have landed
     __shared__ uint32_t s_tmem;    // TC: TMEM base address
     constexpr int PP = part_pitch(NTMAX);
 
@@ -261,12 +269,18 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
     }
     // TC: TMEM for D (>= rows_cap fp32 columns), stage-buffer barriers
     const uint32_t tcols = rows_cap <= 32 ? 32 : (rows_cap <= 64 ? 64 : 128);
-    uint32_t tmem = 0, ncommit0 = 0, ncommit1 = 0;
+    uint32_t tmem = 0, ncommit0 = 0, ncommit1 = 0, nfull0 = 0, nfull1 = 0;
     if constexpr (TC) {
         if (warp == 0) tc_alloc(&s_tmem, tcols);
         if (threadIdx.x == 0) {
             mbar_init(&s_mma[0], 1);
             mbar_init(&s_mma[1], 1);
+            mbar_init(&s_full[0], 1);
+            mbar_init(&s_full[1], 1);
+            if (tma) {
+                tma_prefetch_map(&tm_x);
+                tma_prefetch_map(&tm_a);
+            }
         }
         tc_fence_before();
         __syncthreads();
@@ -308,8 +322,34 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
             s_arow[threadIdx.x] = (int)threadIdx.x < nrows ? (c / rl) * R + c % rl : 0;
         }
         __syncthreads();
+        // TMA staging: the tile's token rows are consecutive (segments of one
+        // adapter that follow each other, as in sorted SGMV batches) and the
+        // adapter has rank R (its A rows are consecutive too)
+        bool tma_tile = false;
+        int xrow0 = 0;
+        if constexpr (TC) {
+            xrow0 = s_rows[0];
+            const bool mine = (int)threadIdx.x >= n || (int)threadIdx.x >= kTile ||
+                              s_rows[threadIdx.x] == xrow0 + (int)threadIdx.x;
+            tma_tile = __syncthreads_and(tma && rl == R && xrow0 >= 0 && mine) != 0;
+        }
 
         const E *Al = static_cast<const E *>(a.A) + (int64_t)l * S * R * H;
+        // one thread's TMA copies of stage st into buffer b: per 64-wide K
+        // half the 64 x rows and rows_cap A rows, in the same swizzled layout
+        // as async_stage_tc (past H both read as zeros; stages never cross
+        // this CTA's K range, which is a whole number of stages)
+        auto tma_stage = [&](int st, int b) {
+            unsigned char *stg = sm + b * stage_bytes;
+            const int h0 = h_begin + st * kK;
+            mbar_arrive_expect_tx(&s_full[b], (uint32_t)(2 * tc_half_bytes(rows_cap)));
+            for (int hh = 0; hh < 2; ++hh) {
+                unsigned char *region = stg + hh * tc_half_bytes(rows_cap);
+                tma_load_2d(smem_u32(region), &tm_x, h0 + 64 * hh, xrow0, &s_full[b]);
+                tma_load_2d(smem_u32(region + kTile * 128), &tm_a, h0 + 64 * hh,
+                            l * S * R + row0, &s_full[b]);
+            }
+        };
         const int NT = (nrows + 7) / 8;
         const int nmb = (n + 15) / 16;
         // warp -> (16-row block mb, n-tile share ns, k share kp)
@@ -335,14 +375,21 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
         // through registers one stage ahead.
         uint4 ld[VEC ? 1 : kMaxLd];
         if constexpr (TC) {
-            if (nstages > 0)
-                async_stage_tc<E>(sm, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, rows_cap, h_begin,
-                                  h_end);
-            cp_async_commit();
-            if (nstages > 1)
-                async_stage_tc<E>(sm + stage_bytes, x, a.ldx, Al, H, s_rows, s_arow, n, nrows,
-                                  rows_cap, h_begin + kK, h_end);
-            cp_async_commit();
+            if (tma_tile) {
+                if (threadIdx.x == 0) {
+                    fence_proxy_async_smem();  // (the last tile's generic accesses came first)
+                    for (int st = 0; st < min(2, nstages); ++st) tma_stage(st, st);
+                }
+            } else {
+                if (nstages > 0)
+                    async_stage_tc<E>(sm, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, rows_cap,
+                                      h_begin, h_end);
+                cp_async_commit();
+                if (nstages > 1)
+                    async_stage_tc<E>(sm + stage_bytes, x, a.ldx, Al, H, s_rows, s_arow, n, nrows,
+                                      rows_cap, h_begin + kK, h_end);
+                cp_async_commit();
+            }
         } else if (VEC) {
             if (nstages > 0)
                 async_stage<E>(smem, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, h_begin, h_end);
@@ -361,9 +408,19 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
             // tcgen05: one thread issues the stage's 8 K steps once every
             // thread's copies have landed and been handed to the async proxy
             unsigned char *cur = sm + (st & 1) * stage_bytes;
-            cp_async_wait<1>();
-            fence_proxy_async_smem();
-            __syncthreads();
+            if (tma_tile) {  // only the issuing thread waits for the copies
+                if (threadIdx.x == 0) {
+                    const uint32_t nf = (st & 1) ? nfull1 : nfull0;
+                    if (!mbar_wait_cta(&s_full[st & 1], nf & 1))
+                        atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+                }
+                if (st & 1) ++nfull1;
+                else ++nfull0;
+            } else {
+                cp_async_wait<1>();
+                fence_proxy_async_smem();
+                __syncthreads();
+            }
             if (threadIdx.x == 0) {
                 tc_fence_after();
                 const uint32_t idesc =
@@ -381,12 +438,21 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
             else ++ncommit0;
             if (st + 2 < nstages) {  // refill this buffer once its MMAs have read it
                 const uint32_t nc = (st & 1) ? ncommit1 : ncommit0;
-                if (!mbar_wait_cta(&s_mma[st & 1], (nc - 1) & 1) && threadIdx.x == 0)
-                    atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
-                async_stage_tc<E>(cur, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, rows_cap,
-                                  h_begin + (st + 2) * kK, h_end);
+                if (tma_tile) {
+                    // every thread waits for each commit in turn: a parity wait
+                    // cannot tell a phase from the one two commits later, so
+                    // no thread may fall more than one phase behind
+                    if (!mbar_wait_cta(&s_mma[st & 1], (nc - 1) & 1) && threadIdx.x == 0)
+                        atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+                    if (threadIdx.x == 0) tma_stage(st + 2, st & 1);
+                } else {
+                    if (!mbar_wait_cta(&s_mma[st & 1], (nc - 1) & 1) && threadIdx.x == 0)
+                        atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+                    async_stage_tc<E>(cur, x, a.ldx, Al, H, s_rows, s_arow, n, nrows, rows_cap,
+                                      h_begin + (st + 2) * kK, h_end);
+                }
             }
-            cp_async_commit();
+            if (!tma_tile) cp_async_commit();
         }
         for (int st = 0; st < nstages && !TC; ++st) {
             unsigned char *cur = smem + (st & 1) * stage_bytes;
@@ -563,7 +629,8 @@ shrink_kernel(const ShrinkArgs a, int kchunk, int rows_cap, int push) {
     }
 }
 
-using ShrinkFn = void (*)(const ShrinkArgs, int, int, int);
+using ShrinkFn = void (*)(const CUtensorMap, const CUtensorMap, const ShrinkArgs, int, int, int,
+                          int);
 
 // Kernel variants: mma.sync with n-split warps, mma.sync with k-split warps,
 // tcgen05 (aligned rows only).
@@ -762,7 +829,19 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, kernel_for(dt, vec, ntc, var), a, kchunk, rows_cap, push);
+    // tensor maps for the tensor-core path's TMA staging of consecutive tiles
+    CUtensorMap tm_x, tm_a;
+    memset(&tm_x, 0, sizeof(tm_x));
+    memset(&tm_a, 0, sizeof(tm_a));
+    int tma = 0;
+    if (var == kTensor &&
+        make_tensor_map_2d(&tm_x, dt, a.x, (uint64_t)a.T, (uint64_t)a.H, (uint64_t)a.ldx, kTile) ==
+            cudaSuccess &&
+        make_tensor_map_2d(&tm_a, dt, a.A, (uint64_t)a.L * a.S * a.R, (uint64_t)a.H, (uint64_t)a.H,
+                           (uint32_t)rows_cap) == cudaSuccess)
+        tma = 1;
+    return cudaLaunchKernelEx(&cfg, kernel_for(dt, vec, ntc, var), tm_x, tm_a, a, kchunk, rows_cap,
+                              push, tma);
 }
 
 }  // namespace lora
