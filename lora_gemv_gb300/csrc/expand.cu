@@ -529,6 +529,7 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
 // and 3 while warps 0 and 1 run the epilogue (one B buffer, free once the
 // MMA is done).
 constexpr int kTcCols = 128;                    // output columns per chunk (N)
+constexpr int kTcThreads = 256;                 // 8 warps: two per TMEM lane quadrant
 constexpr int kTcWaves = 3;                     // least waves of CTAs a span size leaves
 constexpr int kTcMaxSpan = 256;                 // chunks per span at most
 constexpr int kTcOutPitch = kTcCols * 2 + 16;   // bytes per staged out row
@@ -548,7 +549,7 @@ __host__ __device__ constexpr int tc_expand_smem(int R) {
 }
 
 template <typename E, bool ADD>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kTcThreads)
 expand_tc_kernel(const ExpandArgs a, int cpb) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
@@ -614,7 +615,7 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
             grid_dep_wait();
             grid_dep_launch();
             if (!ADD)
-                for (int it = threadIdx.x; it < n * (span_cols / 8); it += kThreads) {
+                for (int it = threadIdx.x; it < n * (span_cols / 8); it += kTcThreads) {
                     const int i = it / (span_cols / 8), c8 = it - i * (span_cols / 8);
                     const int row = s_rows[i];
                     if (row >= 0)
@@ -655,15 +656,15 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
         }
 
         // first chunk's out and B blocks (neither written by the previous kernel)
-        if (ADD) load_out(sO0, 0, threadIdx.x, kThreads);
-        load_b(0, threadIdx.x, kThreads);
+        if (ADD) load_out(sO0, 0, threadIdx.x, kTcThreads);
+        load_b(0, threadIdx.x, kTcThreads);
         cp_async_commit();
 
         // y rows: produced by the previous kernel
         grid_dep_wait();
         grid_dep_launch();
         const float *ys = a.y + (int64_t)s * a.y_slice_stride;
-        for (int it = threadIdx.x; it < n * KS * 4; it += kThreads) {  // 4 ranks per chunk
+        for (int it = threadIdx.x; it < n * KS * 4; it += kTcThreads) {  // 4 ranks per chunk
             const int i = it / (KS * 4), k4 = it - i * (KS * 4);
             const int row = s_rows[i];
             const int nv = row >= 0 ? min(4, rl - 4 * k4) : 0;
@@ -680,7 +681,7 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
         // inside one warp) reduce its max; padding chunks hold zeros.
         {
             const int G = KS <= 1 ? 2 : (KS <= 2 ? 4 : (KS <= 4 ? 8 : 16));
-            for (int it = threadIdx.x; it < kTile * G; it += kThreads) {
+            for (int it = threadIdx.x; it < kTile * G; it += kTcThreads) {
                 const int i = it / G, k8 = it - i * G;
                 const bool live = i < n && k8 < KS * 2;
                 float v[8];
@@ -715,7 +716,7 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
         for (int j = 0; j < nsub; ++j) {
             unsigned char *sOc = (j & 1) ? sO1 : sO0;
             // next chunk's out block into the other buffer (its epilogue is over)
-            if (ADD && j + 1 < nsub) load_out((j & 1) ? sO0 : sO1, j + 1, threadIdx.x, kThreads);
+            if (ADD && j + 1 < nsub) load_out((j & 1) ? sO0 : sO1, j + 1, threadIdx.x, kTcThreads);
             cp_async_commit();
             cp_async_wait<1>();          // this chunk's out and B blocks are in
             fence_proxy_async_smem();    // ... and visible to the tensor cores
@@ -742,18 +743,23 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
             }
             tc_fence_after();
 
-            if (warp >= 2) {
-                // the MMA has read B: next chunk's B block
-                if (j + 1 < nsub) load_b(j + 1, threadIdx.x - 64, kThreads - 64);
+            if ((warp & 3) >= 2) {
+                // the MMA has read B: next chunk's B block (warps 2, 3, 6, 7)
+                if (j + 1 < nsub)
+                    load_b(j + 1, ((warp >> 2) * 2 + (warp & 1)) * 32 + lane, kTcThreads / 2);
                 cp_async_commit();
             } else {
-                // epilogue: warps 0 and 1 own the tile's 64 token lanes
-                const int i = 32 * warp + lane;
+                // epilogue: TMEM lane quadrants 0 and 1 hold the tile's 64
+                // token lanes; warps w and w + 4 share a quadrant and split
+                // the chunk's columns in halves
+                const int q = warp & 3, half = warp >> 2;
+                const int i = 32 * q + lane;
                 const int row = i < n ? s_rows[i] : -1;
                 const float f = s_f[i];
-                const uint32_t tl_addr = tmem + ((uint32_t)(32 * warp) << 16);
+                const uint32_t tl_addr = tmem + ((uint32_t)(32 * q) << 16);
                 const int cj = j * kTcCols, nc = min(kTcCols, span_cols - cj);
-                for (int c0 = 0; c0 < nc; c0 += 32) {  // warp-uniform
+                for (int c0 = half * (kTcCols / 2); c0 < min(nc, (half + 1) * (kTcCols / 2));
+                     c0 += 32) {  // warp-uniform
                     float d[32];
                     tc_ld32(tl_addr + c0, d);
                     if (row < 0) continue;
@@ -827,7 +833,7 @@ template <typename E>
 cudaError_t launch_tc(const ExpandArgs &a, dim3 grid, int cpb, cudaStream_t st, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = tc_expand_smem(a.R);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
