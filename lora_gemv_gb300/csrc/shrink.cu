@@ -203,13 +203,18 @@ __device__ __forceinline__ void store_stage(const uint4 (&ld)[kMaxLd], unsigned 
 // TC: the contraction on the tcgen05 tensor cores (aligned rows; D = X . A^T
 // with M = 128 token lanes, N = rows_cap, accumulated in TMEM), else mma.sync.
 // tma (TC only): tm_x maps x [T][H] in boxes of 64 rows, tm_a maps A [L*S*R][H]
-// in boxes of rows_cap rows; tiles whose token rows are consecutive and whose
-// adapter has rank R are staged by one thread's TMA copies instead of every
-// thread's cp.async.
+// in boxes of rows_cap rows and tm_ab in boxes of 16, 32, 64 and 128 rows;
+// tiles whose token rows are consecutive are staged by one thread's TMA
+// copies instead of every thread's cp.async.
+struct ABoxMaps {
+    CUtensorMap m[4];  // boxes of 16, 32, 64, 128 rows
+};
+
 template <typename E, bool VEC, int NTMAX, bool KS, bool TC>
 __global__ void __launch_bounds__(kThreads)
 shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a,
-              const ShrinkArgs a, int kchunk, int rows_cap, int push, int tma) {
+              const __grid_constant__ ABoxMaps tm_ab, const ShrinkArgs a, int kchunk,
+              int rows_cap, int push, int tma) {
     static_assert(!TC || (VEC && !KS), "the tensor-core path takes aligned rows, no warp split");
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
@@ -280,6 +285,7 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             if (tma) {
                 tma_prefetch_map(&tm_x);
                 tma_prefetch_map(&tm_a);
+                for (int i = 0; i < 4; ++i) tma_prefetch_map(&tm_ab.m[i]);
             }
         }
         tc_fence_before();
@@ -302,52 +308,88 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         const int l = tl.x, n = tl.z;
         const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
 
+        if (threadIdx.x < kTile) s_rows[threadIdx.x] = my_row;
+        __syncthreads();
         // y columns that get no term: every column of inactive tokens, the
-        // columns i >= r_l of each slice otherwise.  Written by one CTA.
-        if (!a.add && kc == 0 && rc == 0 && rl < R) {
-            for (int it = threadIdx.x; it < n * S * R; it += kThreads) {
-                const int i = it / (S * R), j = it % (S * R);
-                if (j % R < rl) continue;
-                const int row = __ldcg(a.tile_rows + (int64_t)tile * kTile + i);
-                if (row >= 0 && row < a.T) a.y[(int64_t)row * a.ldy + j] = 0.f;
+        // columns i >= r_l of each slice otherwise.  The cluster's CTAs share
+        // the tile's rows (row i by CTA i mod ksplit).
+        if (!a.add && rc == 0 && rl < R) {
+            const int ksplit = gridDim.x, zr = R - rl, zc = S * zr;
+            const int nmine = (min(n, kTile) - kc + ksplit - 1) / ksplit;
+            for (int it = threadIdx.x; it < nmine * zc; it += kThreads) {
+                const int ii = it / zc, z = it - ii * zc, sl = z / zr;
+                const int row = s_rows[kc + ii * ksplit];
+                if (row >= 0) a.y[(int64_t)row * a.ldy + sl * R + rl + (z - sl * zr)] = 0.f;
             }
+            __syncthreads();  // s_rows is read here and may be rewritten by the next tile
         }
         const int row0 = rc * kRows;
-        const int nrows = min(kRows, S * rl - row0);
-        if (nrows <= 0) continue;
-
-        if (threadIdx.x < kTile) s_rows[threadIdx.x] = my_row;
-        if (threadIdx.x < kRows) {
-            const int c = row0 + threadIdx.x;
-            s_arow[threadIdx.x] = (int)threadIdx.x < nrows ? (c / rl) * R + c % rl : 0;
-        }
-        __syncthreads();
+        const int nrows_c = min(kRows, S * rl - row0);  // compacted A rows of this CTA
+        if (nrows_c <= 0) continue;
         // TMA staging: the tile's token rows are consecutive (segments of one
-        // adapter that follow each other, as in sorted SGMV batches) and the
-        // adapter has rank R (its A rows are consecutive too)
+        // adapter that follow each other, as in sorted SGMV batches).  A's
+        // live rows are then copied in boxes of 16 rows per slice: the CTA's
+        // columns run over slices of rl16 = r_l rounded up to 16 (columns
+        // past r_l in a slice are computed and dropped), which must fit the
+        // launch's column range (one z-chunk holding every slice, or full
+        // rank R that is a multiple of 16, where the two orders coincide).
         bool tma_tile = false;
         int xrow0 = 0;
+        const int rl16 = (rl + 15) & ~15;
         if constexpr (TC) {
             xrow0 = s_rows[0];
+            const bool cols_ok = ((int)gridDim.z == 1 && S * rl16 <= rows_cap) ||
+                                 (rl == R && R % 16 == 0);
             const bool mine = (int)threadIdx.x >= n || (int)threadIdx.x >= kTile ||
                               s_rows[threadIdx.x] == xrow0 + (int)threadIdx.x;
-            tma_tile = __syncthreads_and(tma && rl == R && xrow0 >= 0 && mine) != 0;
+            tma_tile = __syncthreads_and(tma && cols_ok && xrow0 >= 0 && mine) != 0;
         }
+        const int nrows = tma_tile ? min(kRows, S * rl16 - row0) : nrows_c;
+        if (threadIdx.x < kRows) {
+            const int c = row0 + threadIdx.x;
+            int ar = 0;
+            if (tma_tile)  // -1: a column past r_l, never stored
+                ar = (int)threadIdx.x < nrows && c % rl16 < rl ? (c / rl16) * R + c % rl16 : -1;
+            else if ((int)threadIdx.x < nrows)
+                ar = (c / rl) * R + c % rl;
+            s_arow[threadIdx.x] = ar;
+        }
+        __syncthreads();
 
         const E *Al = static_cast<const E *>(a.A) + (int64_t)l * S * R * H;
         // one thread's TMA copies of stage st into buffer b: per 64-wide K
-        // half the 64 x rows and rows_cap A rows, in the same swizzled layout
-        // as async_stage_tc (past H both read as zeros; stages never cross
-        // this CTA's K range, which is a whole number of stages)
+        // half the 64 x rows and the CTA's A rows in 16-row boxes, in the same
+        // swizzled layout as async_stage_tc (past H both read as zeros;
+        // stages never cross this CTA's K range, a whole number of stages)
+        const bool a_whole = rl == R && R % 16 == 0;
         auto tma_stage = [&](int st, int b) {
             unsigned char *stg = sm + b * stage_bytes;
             const int h0 = h_begin + st * kK;
-            mbar_arrive_expect_tx(&s_full[b], (uint32_t)(2 * tc_half_bytes(rows_cap)));
+            // full rank (a multiple of 16): the CTA's rows are one block of
+            // rows_cap rows; otherwise (every slice in this CTA's columns)
+            // each slice's rl16 rows as boxes of 64 / 32 / 16 rows
+            mbar_arrive_expect_tx(&s_full[b],
+                                  (uint32_t)(2 * (kTile + (a_whole ? rows_cap : nrows)) * 128));
             for (int hh = 0; hh < 2; ++hh) {
                 unsigned char *region = stg + hh * tc_half_bytes(rows_cap);
                 tma_load_2d(smem_u32(region), &tm_x, h0 + 64 * hh, xrow0, &s_full[b]);
-                tma_load_2d(smem_u32(region + kTile * 128), &tm_a, h0 + 64 * hh,
-                            l * S * R + row0, &s_full[b]);
+                if (a_whole) {
+                    tma_load_2d(smem_u32(region + kTile * 128), &tm_a, h0 + 64 * hh,
+                                l * S * R + row0, &s_full[b]);
+                    continue;
+                }
+                for (int sl = 0; sl < S; ++sl) {
+                    int off = 0;
+                    for (int q = 3; q >= 0; --q) {  // boxes of 128, 64, 32, 16 rows
+                        const int bx = 16 << q;
+                        while (rl16 - off >= bx) {
+                            tma_load_2d(smem_u32(region + (kTile + sl * rl16 + off) * 128),
+                                        &tm_ab.m[q], h0 + 64 * hh, l * S * R + sl * R + off,
+                                        &s_full[b]);
+                            off += bx;
+                        }
+                    }
+                }
             }
         };
         const int NT = (nrows + 7) / 8;
@@ -576,7 +618,7 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                 float sum = 0.f;
                 for (int r = 0; r < ksplit; ++r) sum += Rb[(r * rpo + ii) * rows_cap + c];
                 const int row = s_rows[r0 + ii];
-                if (row >= 0) {
+                if (row >= 0 && s_arow[c] >= 0) {
                     float *yp = a.y + (int64_t)row * a.ldy + s_arow[c];
                     const float v = a.scale * sum;
                     *yp = a.add ? *yp + v : v;
@@ -611,7 +653,7 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
                 for (int r = 0; r < 16; ++r)
                     if (r < ksplit) sum += part[r];
                 const int row = s_rows[i];
-                if (row >= 0) {
+                if (row >= 0 && s_arow[c] >= 0) {
                     float *yp = a.y + (int64_t)row * a.ldy + s_arow[c];
                     const float v = a.scale * sum;
                     *yp = a.add ? *yp + v : v;
@@ -629,8 +671,8 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     }
 }
 
-using ShrinkFn = void (*)(const CUtensorMap, const CUtensorMap, const ShrinkArgs, int, int, int,
-                          int);
+using ShrinkFn = void (*)(const CUtensorMap, const CUtensorMap, const ABoxMaps, const ShrinkArgs,
+                          int, int, int, int);
 
 // Kernel variants: mma.sync with n-split warps, mma.sync with k-split warps,
 // tcgen05 (aligned rows only).
@@ -831,17 +873,25 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     cfg.numAttrs = pdl ? 2 : 1;
     // tensor maps for the tensor-core path's TMA staging of consecutive tiles
     CUtensorMap tm_x, tm_a;
+    ABoxMaps tm_ab;
     memset(&tm_x, 0, sizeof(tm_x));
     memset(&tm_a, 0, sizeof(tm_a));
+    memset(&tm_ab, 0, sizeof(tm_ab));
+    const uint64_t arows = (uint64_t)a.L * a.S * a.R;
     int tma = 0;
-    if (var == kTensor &&
-        make_tensor_map_2d(&tm_x, dt, a.x, (uint64_t)a.T, (uint64_t)a.H, (uint64_t)a.ldx, kTile) ==
-            cudaSuccess &&
-        make_tensor_map_2d(&tm_a, dt, a.A, (uint64_t)a.L * a.S * a.R, (uint64_t)a.H, (uint64_t)a.H,
-                           (uint32_t)rows_cap) == cudaSuccess)
-        tma = 1;
-    return cudaLaunchKernelEx(&cfg, kernel_for(dt, vec, ntc, var), tm_x, tm_a, a, kchunk, rows_cap,
-                              push, tma);
+    if (var == kTensor) {
+        cudaError_t e =
+            make_tensor_map_2d(&tm_x, dt, a.x, (uint64_t)a.T, (uint64_t)a.H, (uint64_t)a.ldx, kTile);
+        if (e == cudaSuccess)
+            e = make_tensor_map_2d(&tm_a, dt, a.A, arows, (uint64_t)a.H, (uint64_t)a.H,
+                                   (uint32_t)rows_cap);
+        for (int q = 0; q < 4 && e == cudaSuccess; ++q)
+            e = make_tensor_map_2d(&tm_ab.m[q], dt, a.A, arows, (uint64_t)a.H, (uint64_t)a.H,
+                                   16u << q);
+        tma = e == cudaSuccess ? 1 : 0;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel_for(dt, vec, ntc, var), tm_x, tm_a, tm_ab, a, kchunk,
+                              rows_cap, push, tma);
 }
 
 }  // namespace lora

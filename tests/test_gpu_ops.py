@@ -230,6 +230,26 @@ def test_segments_interleaving_adapters(cuda_lib, R, ranks, add):
     assert ntiles > (T + 63) // 64 + 2 + 1
 
 
+@pytest.mark.parametrize("R,ranks,Ns", [(24, [24, 5, 13, 0], [256, 128, 96]),
+                                         (64, [64, 40, 17], [512, 256]),
+                                         (32, None, [384, 384, 128])])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("add", [False, True])
+def test_sorted_segments_rank_aware(cuda_lib, R, ranks, Ns, dtype, add):
+    """Long sorted segments (tiles of consecutive token rows, copied by TMA
+    in the tensor-core shrink) with ranks below R, several slices and an H
+    that is not a multiple of the 128-wide stage."""
+    L = len(ranks) if ranks is not None else 3
+    T = 700
+    c = make_case(T, 640, R, L, Ns, dtype, seed=R + L + add, add=add, ranks=ranks)
+    lens = [200, 90, 250, T - 540]
+    c.token_idx = None
+    c.seg_start = torch.tensor(np.cumsum([0] + lens[:-1]), dtype=torch.int32)
+    c.seg_len = torch.tensor(lens, dtype=torch.int32)
+    c.seg_lora = torch.tensor([0, 0, 1, L - 1], dtype=torch.int32)  # sorted: a run of adapter 0
+    full_check(cuda_lib, c)
+
+
 # ---------------------------------------------------------------- edge cases
 
 def make_case(T, H, R, L, N_list, dtype, seed, *, S=None, p_neg=0.2, add=True, scale=0.7,
