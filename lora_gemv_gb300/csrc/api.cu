@@ -5,6 +5,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <unordered_set>
 
 #include "kernels.h"
 
@@ -127,6 +128,29 @@ size_t lora_workspace_size(int32_t T, int32_t L) {
     return lora_plan_layout(T, L, &lay) == LORA_OK ? (size_t)lay.bytes : 0;
 }
 
+}  // extern "C"
+
+namespace {
+// Plans grouped by this library from a segment table, by address.  A hint for
+// the shrink's launch shape only (segment plans mostly hold tiles of
+// consecutive token rows, which the TMA-staging variant copies in bulk);
+// every variant checks each tile itself, so a stale entry costs speed, never
+// correctness.
+std::mutex g_kind_mu;
+std::unordered_set<const void *> g_seg_plans;
+void note_plan_kind(const void *plan, bool segments) {
+    std::lock_guard<std::mutex> lk(g_kind_mu);
+    if (segments) g_seg_plans.insert(plan);
+    else g_seg_plans.erase(plan);
+}
+bool is_seg_plan(const void *plan) {
+    std::lock_guard<std::mutex> lk(g_kind_mu);
+    return g_seg_plans.count(plan) != 0;
+}
+}  // namespace
+
+extern "C" {
+
 lora_status_t lora_group_tokens(const int32_t *token_idx, int32_t T, int32_t L, void *plan,
                                 size_t plan_bytes, lora_stream_t stream) {
     lora_plan_layout_t lay;
@@ -136,6 +160,7 @@ lora_status_t lora_group_tokens(const int32_t *token_idx, int32_t T, int32_t L, 
     if (!aligned(token_idx, 4)) return fail(LORA_ERR_INVALID_ARG, "token_idx misaligned");
     const lora::DeviceInfo *dev;
     if ((s = device_info(&dev)) != LORA_OK) return s;
+    note_plan_kind(plan, false);
     cudaError_t e = lora::launch_group_tokens(token_idx, T, L, plan_ptrs(plan, lay),
                                               reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "group_tokens launch");
@@ -154,6 +179,7 @@ lora_status_t lora_group_segments(const int32_t *seg_start, const int32_t *seg_l
         return fail(LORA_ERR_INVALID_ARG, "segment table misaligned");
     const lora::DeviceInfo *dev;
     if ((s = device_info(&dev)) != LORA_OK) return s;
+    note_plan_kind(plan, true);
     cudaError_t e = lora::launch_group_segments(seg_start, seg_len, seg_lora, num_segs, T, L,
                                                 plan_ptrs(plan, lay),
                                                 reinterpret_cast<cudaStream_t>(stream));
@@ -268,6 +294,7 @@ lora_status_t lora_shrink(lora_dtype_t dtype, const void *x, int64_t ldx, int32_
     a.tiles = p.tiles;
     a.tile_rows = p.tile_rows;
     a.max_tiles = (int)lay.max_tiles;
+    a.seg_plan = is_seg_plan(plan) ? 1 : 0;
     cudaError_t e = lora::launch_shrink(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "shrink launch");
 }
@@ -367,6 +394,7 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
     sa.tiles = p.tiles;
     sa.tile_rows = p.tile_rows;
     sa.max_tiles = (int)lay.max_tiles;
+    sa.seg_plan = is_seg_plan(plan) ? 1 : 0;
     lora::ExpandArgs ea{};
     ea.y = y;
     ea.ldy = ldy;

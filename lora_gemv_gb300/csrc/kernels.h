@@ -32,6 +32,7 @@ struct ShrinkArgs {
     const int4 *tiles;
     const int32_t *tile_rows;
     int max_tiles;
+    int seg_plan;  // the plan was grouped from a segment table (a launch-shape hint only)
 };
 
 struct ExpandArgs {

@@ -210,7 +210,45 @@ struct ABoxMaps {
     CUtensorMap m[4];  // boxes of 16, 32, 64, 128 rows
 };
 
-template <typename E, bool VEC, int NTMAX, bool KS, bool TC>
+// One thread's TMA copies of a tensor-core stage (base `stg`, per 64-wide K
+// half `half_bytes`): per half the 64 x rows at (h0, xrow0) and the CTA's A
+// rows in the same swizzled layout as async_stage_tc.  Full rank that is a
+// multiple of 16: the CTA's A rows are one block of rows_cap rows (A row
+// a_base + row0 ..); otherwise every slice's rl16 rows (A rows a_base + s*R ..)
+// as boxes of 128 / 64 / 32 / 16 rows.  Past H both read as zeros; stages
+// never cross the CTA's K range.  Not inlined: it runs on one thread, and
+// its registers would otherwise count for every thread of the kernel.
+__device__ __noinline__ void shrink_tma_stage(const CUtensorMap *tm_x, const CUtensorMap *tm_a,
+                                              const ABoxMaps *tm_ab, uint32_t stg,
+                                              int half_bytes, uint64_t *bar, int h0, int xrow0,
+                                              int a_base, int row0, int rows_cap, int nrows,
+                                              int S, int R, int rl16, bool a_whole) {
+    mbar_arrive_expect_tx(bar, (uint32_t)(2 * (kTile + (a_whole ? rows_cap : nrows)) * 128));
+    for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t region = stg + hh * half_bytes;
+        tma_load_2d(region, tm_x, h0 + 64 * hh, xrow0, bar);
+        if (a_whole) {
+            tma_load_2d(region + kTile * 128, tm_a, h0 + 64 * hh, a_base + row0, bar);
+            continue;
+        }
+        for (int sl = 0; sl < S; ++sl) {
+            int off = 0;
+            for (int q = 3; q >= 0; --q) {
+                const int bx = 16 << q;
+                while (rl16 - off >= bx) {
+                    tma_load_2d(region + (kTile + sl * rl16 + off) * 128, &tm_ab->m[q],
+                                h0 + 64 * hh, a_base + sl * R + off, bar);
+                    off += bx;
+                }
+            }
+        }
+    }
+}
+
+// TMA (TC only): the TMA-capable variant, launched for plans grouped from a
+// segment table; without it the TMA code is compiled out and the variant
+// keeps the registers (and so the residency) of the cp.async-only kernel.
+template <typename E, bool VEC, int NTMAX, bool KS, bool TC, bool TMA>
 __global__ void __launch_bounds__(kThreads)
 shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a,
               const __grid_constant__ ABoxMaps tm_ab, const ShrinkArgs a, int kchunk,
@@ -282,7 +320,7 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
             mbar_init(&s_mma[1], 1);
             mbar_init(&s_full[0], 1);
             mbar_init(&s_full[1], 1);
-            if (tma) {
+            if (TMA && tma) {
                 tma_prefetch_map(&tm_x);
                 tma_prefetch_map(&tm_a);
                 for (int i = 0; i < 4; ++i) tma_prefetch_map(&tm_ab.m[i]);
@@ -336,7 +374,7 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         bool tma_tile = false;
         int xrow0 = 0;
         const int rl16 = (rl + 15) & ~15;
-        if constexpr (TC) {
+        if constexpr (TC && TMA) {
             xrow0 = s_rows[0];
             const bool cols_ok = ((int)gridDim.z == 1 && S * rl16 <= rows_cap) ||
                                  (rl == R && R % 16 == 0);
@@ -357,40 +395,12 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         __syncthreads();
 
         const E *Al = static_cast<const E *>(a.A) + (int64_t)l * S * R * H;
-        // one thread's TMA copies of stage st into buffer b: per 64-wide K
-        // half the 64 x rows and the CTA's A rows in 16-row boxes, in the same
-        // swizzled layout as async_stage_tc (past H both read as zeros;
-        // stages never cross this CTA's K range, a whole number of stages)
+        // one thread's TMA copies of stage st into buffer b (shrink_tma_stage)
         const bool a_whole = rl == R && R % 16 == 0;
         auto tma_stage = [&](int st, int b) {
-            unsigned char *stg = sm + b * stage_bytes;
-            const int h0 = h_begin + st * kK;
-            // full rank (a multiple of 16): the CTA's rows are one block of
-            // rows_cap rows; otherwise (every slice in this CTA's columns)
-            // each slice's rl16 rows as boxes of 64 / 32 / 16 rows
-            mbar_arrive_expect_tx(&s_full[b],
-                                  (uint32_t)(2 * (kTile + (a_whole ? rows_cap : nrows)) * 128));
-            for (int hh = 0; hh < 2; ++hh) {
-                unsigned char *region = stg + hh * tc_half_bytes(rows_cap);
-                tma_load_2d(smem_u32(region), &tm_x, h0 + 64 * hh, xrow0, &s_full[b]);
-                if (a_whole) {
-                    tma_load_2d(smem_u32(region + kTile * 128), &tm_a, h0 + 64 * hh,
-                                l * S * R + row0, &s_full[b]);
-                    continue;
-                }
-                for (int sl = 0; sl < S; ++sl) {
-                    int off = 0;
-                    for (int q = 3; q >= 0; --q) {  // boxes of 128, 64, 32, 16 rows
-                        const int bx = 16 << q;
-                        while (rl16 - off >= bx) {
-                            tma_load_2d(smem_u32(region + (kTile + sl * rl16 + off) * 128),
-                                        &tm_ab.m[q], h0 + 64 * hh, l * S * R + sl * R + off,
-                                        &s_full[b]);
-                            off += bx;
-                        }
-                    }
-                }
-            }
+            shrink_tma_stage(&tm_x, &tm_a, &tm_ab, smem_u32(sm + b * stage_bytes),
+                             tc_half_bytes(rows_cap), &s_full[b], h_begin + st * kK, xrow0,
+                             l * S * R, row0, rows_cap, nrows, S, R, rl16, a_whole);
         };
         const int NT = (nrows + 7) / 8;
         const int nmb = (n + 15) / 16;
@@ -676,16 +686,16 @@ using ShrinkFn = void (*)(const CUtensorMap, const CUtensorMap, const ABoxMaps, 
 
 // Kernel variants: mma.sync with n-split warps, mma.sync with k-split warps,
 // tcgen05 (aligned rows only).
-enum Variant { kNSplit = 0, kKSplit = 1, kTensor = 2, kVariants = 3 };
+enum Variant { kNSplit = 0, kKSplit = 1, kTensor = 2, kTensorTma = 3, kVariants = 4 };
 
 // Instantiation for n-tile class c (NTMAX = 2 << c).
-template <typename E, bool VEC, bool KS, bool TC>
+template <typename E, bool VEC, bool KS, bool TC, bool TMA = false>
 ShrinkFn kernel_nt(int c) {
     switch (c) {
-        case 0: return shrink_kernel<E, VEC, 2, KS, TC>;
-        case 1: return shrink_kernel<E, VEC, 4, KS, TC>;
-        case 2: return shrink_kernel<E, VEC, 8, KS, TC>;
-        default: return shrink_kernel<E, VEC, 16, KS, TC>;
+        case 0: return shrink_kernel<E, VEC, 2, KS, TC, TMA>;
+        case 1: return shrink_kernel<E, VEC, 4, KS, TC, TMA>;
+        case 2: return shrink_kernel<E, VEC, 8, KS, TC, TMA>;
+        default: return shrink_kernel<E, VEC, 16, KS, TC, TMA>;
     }
 }
 
@@ -693,6 +703,7 @@ ShrinkFn kernel_nt(int c) {
 template <typename E>
 ShrinkFn kernel_e(bool vec, int c, int var) {
     if (var == kTensor) return vec ? kernel_nt<E, true, false, true>(c) : nullptr;
+    if (var == kTensorTma) return vec ? kernel_nt<E, true, false, true, true>(c) : nullptr;
     const bool ks = var == kKSplit;
     if (vec) return ks ? kernel_nt<E, true, true, false>(c) : kernel_nt<E, true, false, false>(c);
     return ks ? kernel_nt<E, false, true, false>(c) : kernel_nt<E, false, false, false>(c);
@@ -783,8 +794,9 @@ cudaError_t configure_shrink_kernels(DeviceInfo *info) {
                     const ShrinkFn k = kernel_for(dt, vec, c, var);
                     if (!k) continue;
                     const int ntmax = 2 << c;
-                    const int stage_max = var == kTensor ? tc_stage_area(std::min(ntmax * 8, kRows))
-                                                         : smem_bytes(kRows, ntmax);
+                    const int stage_max = var == kTensor || var == kTensorTma
+                                              ? tc_stage_area(std::min(ntmax * 8, kRows))
+                                              : smem_bytes(kRows, ntmax);
                     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              stage_max + recv_bytes(kRows));
                     // all of the SM's unified L1 / shared memory may serve as shared
@@ -832,7 +844,9 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     // tensor-memory setup); otherwise tcgen05 for aligned rows, else mma.sync
     // with warps splitting n-tiles.
     const bool ks = a.T <= 16LL * std::min(a.L, a.T);
-    const int var = ks ? kKSplit : (vec ? kTensor : kNSplit);
+    // tcgen05 with TMA staging for plans grouped from segments (their tiles
+    // are mostly consecutive token rows)
+    const int var = ks ? kKSplit : (vec ? (a.seg_plan ? kTensorTma : kTensor) : kNSplit);
     // CTAs resident per SM with `dyn` bytes of dynamic shared memory
     const int vi = vec ? 1 : 0;
     auto resident = [&](size_t dyn) {
@@ -840,7 +854,8 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
             g_smem_sm / ((long long)dyn + g_static_smem[dt][vi][ntc][var] + g_smem_reserved);
         return (int)std::max(1LL, std::min<long long>({by_smem, g_reg_occ[dt][vi][ntc][var], 8}));
     };
-    size_t smem = var == kTensor ? tc_stage_area(rows_cap) : smem_bytes(rows_cap, ntmax);
+    size_t smem = var == kTensor || var == kTensorTma ? tc_stage_area(rows_cap)
+                                                      : smem_bytes(rows_cap, ntmax);
     const int occ = resident(smem);
     // the push reduction's receive buffer, where it costs no residency
     const bool push_fits = resident(smem + recv_bytes(rows_cap)) == occ;
@@ -879,7 +894,7 @@ cudaError_t launch_shrink(lora_dtype_t dt, const ShrinkArgs &a, const DeviceInfo
     memset(&tm_ab, 0, sizeof(tm_ab));
     const uint64_t arows = (uint64_t)a.L * a.S * a.R;
     int tma = 0;
-    if (var == kTensor) {
+    if (var == kTensorTma) {
         cudaError_t e =
             make_tensor_map_2d(&tm_x, dt, a.x, (uint64_t)a.T, (uint64_t)a.H, (uint64_t)a.ldx, kTile);
         if (e == cudaSuccess)
