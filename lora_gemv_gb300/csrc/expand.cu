@@ -20,6 +20,9 @@
 //    two, so the product keeps ~fp32 accuracy of y and never overflows fp16;
 //  - tiles with adapter -1 and adapters of rank 0 load nothing (block
 //    skipping) and, without add_inputs, only store zeros.
+#include <string.h>
+
+#include <algorithm>
 #include <type_traits>
 
 #include "common.cuh"
@@ -548,13 +551,22 @@ __host__ __device__ constexpr int tc_expand_smem(int R) {
            tc_out1_bytes(R);
 }
 
+// Byte offset of (token row i, 16-byte column group c8) in a staged out block:
+// two boxes of 64 columns, each [64 rows][128 B] in the 128-byte swizzled
+// layout a TMA load writes (group g of a row at g ^ (row & 7)), so the
+// epilogue's row-per-lane reads fall in eight different bank groups.
+__device__ __forceinline__ int out_off(int i, int c8) {
+    return (c8 >> 3) * (kTile * 128) + i * 128 + (((c8 & 7) ^ (i & 7)) << 4);
+}
+
 template <typename E, bool ADD>
 __global__ void __launch_bounds__(kTcThreads)
-expand_tc_kernel(const ExpandArgs a, int cpb) {
+expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const ExpandArgs a, int cpb, int tma) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
     __shared__ float s_f[kTile];
     __shared__ uint64_t s_bar;
+    __shared__ uint64_t s_oful[2];  // TMA out block b has landed
     __shared__ uint32_t s_tmem;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int span = blockIdx.y;
@@ -594,6 +606,8 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
 
     bool have_tmem = false;   // TMEM and the barrier are set up on the first tile needing them
     uint32_t tmem = 0, ncommit = 0;
+    uint32_t nof0 = 0, nof1 = 0;  // completed phases of s_oful[0], s_oful[1]
+    int of_pending = 0;           // bit b: out buffer b has a TMA copy not yet waited for
     bool timed_out = false;
     for (; tile < n_tiles; tile += gridDim.x) {
         if (tile != (int)blockIdx.x) {
@@ -627,14 +641,35 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
         const int KS = (rl + 15) / 16;
         const E *Bl = static_cast<const E *>(a.B[s]) + ((int64_t)l * a.N[s] + n_span) * R;
 
-        // chunk j's out block into dst (threads t0, t0 + nt, ...)
-        auto load_out = [&](unsigned char *dst, int j, int t0, int nt) {
-            const int c0 = j * kTcCols, c8n = min(kTcCols, span_cols - c0) / 8;
-            for (int it = t0; it < n * c8n; it += nt) {
+        // Tiles of consecutive token rows (sorted SGMV segments): their out
+        // blocks come by TMA, two 64 x 64 boxes per chunk from one thread.
+        const int xrow0 = s_rows[0];
+        const bool tma_tile =
+            __syncthreads_and(tma && ADD && xrow0 >= 0 &&
+                              ((int)threadIdx.x >= n || (int)threadIdx.x >= kTile ||
+                               s_rows[threadIdx.x] == xrow0 + (int)threadIdx.x)) != 0;
+        // chunk j's out block into buffer b (every thread calls), in the
+        // 128-byte swizzled layout of two 64-column boxes (out_off)
+        auto load_out = [&](int b, int j) {
+            unsigned char *dst = b ? sO1 : sO0;
+            const int c0 = j * kTcCols;
+            if (tma_tile) {
+                if (threadIdx.x == 0) {
+                    fence_proxy_async_smem();  // (the buffer's generic reads came first)
+                    mbar_arrive_expect_tx(&s_oful[b], 2 * kTile * 128);
+                    tma_load_2d(smem_u32(dst), &tm_out, (int)(colbase + c0), xrow0, &s_oful[b]);
+                    tma_load_2d(smem_u32(dst + kTile * 128), &tm_out, (int)(colbase + c0 + 64),
+                                xrow0, &s_oful[b]);
+                }
+                of_pending |= 1 << b;
+                return;
+            }
+            const int c8n = min(kTcCols, span_cols - c0) / 8;
+            for (int it = threadIdx.x; it < n * c8n; it += kTcThreads) {
                 const int i = it / c8n, c8 = it - i * c8n;
                 const int row = s_rows[i];
                 if (row >= 0)
-                    cp_async16(smem_u32(dst + i * kTcOutPitch + 16 * c8),
+                    cp_async16(smem_u32(dst + out_off(i, c8)),
                                out + (int64_t)row * a.ldo + colbase + c0 + 8 * c8, 16);
             }
         };
@@ -652,11 +687,15 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
 
         if (!have_tmem) {
             if (warp == 0) tc_alloc(&s_tmem, kTcCols);
-            if (threadIdx.x == 0) mbar_init(&s_bar, 1);
+            if (threadIdx.x == 0) {
+                mbar_init(&s_bar, 1);
+                mbar_init(&s_oful[0], 1);
+                mbar_init(&s_oful[1], 1);
+            }
         }
 
         // first chunk's out and B blocks (neither written by the previous kernel)
-        if (ADD) load_out(sO0, 0, threadIdx.x, kTcThreads);
+        if (ADD) load_out(0, 0);
         load_b(0, threadIdx.x, kTcThreads);
         cp_async_commit();
 
@@ -716,9 +755,17 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
         for (int j = 0; j < nsub; ++j) {
             unsigned char *sOc = (j & 1) ? sO1 : sO0;
             // next chunk's out block into the other buffer (its epilogue is over)
-            if (ADD && j + 1 < nsub) load_out((j & 1) ? sO0 : sO1, j + 1, threadIdx.x, kTcThreads);
+            if (ADD && j + 1 < nsub) load_out((j + 1) & 1, j + 1);
             cp_async_commit();
             cp_async_wait<1>();          // this chunk's out and B blocks are in
+            if (ADD && tma_tile) {       // (the out block by TMA)
+                const uint32_t nf = (j & 1) ? nof1 : nof0;
+                if (!mbar_wait_cta(&s_oful[j & 1], nf & 1) && threadIdx.x == 0)
+                    atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+                if (j & 1) ++nof1;
+                else ++nof0;
+                of_pending &= ~(1 << (j & 1));
+            }
             fence_proxy_async_smem();    // ... and visible to the tensor cores
             __syncthreads();
             tc_fence_after();
@@ -772,7 +819,7 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
                         for (int k = 0; k < 8; ++k) v[k] = f * d[8 * g + k];
                         if (ADD) {
                             float o[8];
-                            unpack8<E>(*reinterpret_cast<const uint4 *>(sOc + i * kTcOutPitch + 2 * c), o);
+                            unpack8<E>(*reinterpret_cast<const uint4 *>(sOc + out_off(i, c / 8)), o);
 #pragma unroll
                             for (int k = 0; k < 8; ++k) v[k] += o[k];
                         }
@@ -786,6 +833,8 @@ expand_tc_kernel(const ExpandArgs a, int cpb) {
         cp_async_wait<0>();
         if (timed_out) break;
     }
+    for (int b = 0; b < 2; ++b)  // (left by a timed-out chunk) no copy may land after exit
+        if (of_pending & (1 << b)) mbar_wait_cta(&s_oful[b], (b ? nof1 : nof0) & 1);
     if (have_tmem) {
         cp_async_wait<0>();
         // after a timed-out wait, give the MMA one more bounded wait before
@@ -841,8 +890,23 @@ cudaError_t launch_tc(const ExpandArgs &a, dim3 grid, int cpb, cudaStream_t st, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    if (a.add) return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, true>, a, cpb);
-    return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, false>, a, cpb);
+    // out blocks of tiles of consecutive rows by TMA (add_inputs only): a map
+    // over the columns the slices use
+    CUtensorMap tm_out;
+    memset(&tm_out, 0, sizeof(tm_out));
+    int tma = 0;
+    if (a.add) {
+        int64_t used = 0;
+        for (int s = 0; s < a.num_slices; ++s)
+            used = std::max<int64_t>(used, (int64_t)a.off[s] + a.N[s]);
+        tma = make_tensor_map_2d(&tm_out, std::is_same<E, __nv_bfloat16>::value ? LORA_BF16 : LORA_F16,
+                                 a.out, (uint64_t)a.T, (uint64_t)used, (uint64_t)a.ldo, kTile) ==
+                      cudaSuccess
+                  ? 1
+                  : 0;
+    }
+    if (a.add) return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, true>, tm_out, a, cpb, tma);
+    return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, false>, tm_out, a, cpb, tma);
 }
 
 template <typename E>
