@@ -551,6 +551,10 @@ __host__ __device__ constexpr int tc_expand_smem(int R) {
            tc_out1_bytes(R);
 }
 
+struct BMaps {
+    CUtensorMap m[LORA_MAX_SLICES];  // B_s as [L * N_s][R], boxes of 128 rows x 64 ranks
+};
+
 // Byte offset of (token row i, 16-byte column group c8) in a staged out block:
 // two boxes of 64 columns, each [64 rows][128 B] in the 128-byte swizzled
 // layout a TMA load writes (group g of a row at g ^ (row & 7)), so the
@@ -561,12 +565,14 @@ __device__ __forceinline__ int out_off(int i, int c8) {
 
 template <typename E, bool ADD>
 __global__ void __launch_bounds__(kTcThreads)
-expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const ExpandArgs a, int cpb, int tma) {
+expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_constant__ BMaps tm_b,
+                 const ExpandArgs a, int cpb, int tma, int tma_b) {
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
     __shared__ float s_f[kTile];
     __shared__ uint64_t s_bar;
     __shared__ uint64_t s_oful[2];  // TMA out block b has landed
+    __shared__ uint64_t s_bful;     // the TMA B block has landed
     __shared__ uint32_t s_tmem;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int span = blockIdx.y;
@@ -608,6 +614,8 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const ExpandArgs a,
     uint32_t tmem = 0, ncommit = 0;
     uint32_t nof0 = 0, nof1 = 0;  // completed phases of s_oful[0], s_oful[1]
     int of_pending = 0;           // bit b: out buffer b has a TMA copy not yet waited for
+    uint32_t nbf = 0;             // completed phases of s_bful
+    bool bf_timed_out = false;    // (thread 0) a wait for a TMA B block ran out
     bool timed_out = false;
     for (; tile < n_tiles; tile += gridDim.x) {
         if (tile != (int)blockIdx.x) {
@@ -673,8 +681,21 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const ExpandArgs a,
                                out + (int64_t)row * a.ldo + colbase + c0 + 8 * c8, 16);
             }
         };
-        // chunk j's B block (8 ranks per 16-byte piece, ranks >= rl zero-filled)
+        // chunk j's B block (8 ranks per 16-byte piece, ranks >= rl zero-filled);
+        // at full rank R (a multiple of 64) by TMA from the caller's thread t0 == 0:
+        // 128 rows (output columns) of 64 ranks per box, the same swizzled layout
+        const bool b_tma = tma_b && rl == R;
         auto load_b = [&](int j, int t0, int nt) {
+            if (b_tma) {
+                if (t0 == 0) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(&s_bful, (uint32_t)(KH * kTcCols * 128));
+                    for (int h = 0; h < KH; ++h)
+                        tma_load_2d(smem_u32(sB + h * kTcCols * 128), &tm_b.m[s], 64 * h,
+                                    l * a.N[s] + n_span + j * kTcCols, &s_bful);
+                }
+                return;
+            }
             const int c0 = j * kTcCols, nc = min(kTcCols, span_cols - c0);
             const E *Bj = Bl + (int64_t)c0 * R;
             for (int it = t0; it < nc * KS * 2; it += nt) {
@@ -691,6 +712,7 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const ExpandArgs a,
                 mbar_init(&s_bar, 1);
                 mbar_init(&s_oful[0], 1);
                 mbar_init(&s_oful[1], 1);
+                mbar_init(&s_bful, 1);
             }
         }
 
@@ -769,6 +791,13 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const ExpandArgs a,
             fence_proxy_async_smem();    // ... and visible to the tensor cores
             __syncthreads();
             tc_fence_after();
+            if (b_tma) {  // (the B block by TMA: only the issuing thread reads it)
+                if (threadIdx.x == 0 && !mbar_wait_cta(&s_bful, nbf & 1)) {
+                    atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_TIMEOUT);
+                    bf_timed_out = true;
+                }
+                ++nbf;
+            }
             if (threadIdx.x == 0) {
                 for (int k = 0; k < KS; ++k) {
                     const int h = k >> 2;
@@ -835,6 +864,7 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const ExpandArgs a,
     }
     for (int b = 0; b < 2; ++b)  // (left by a timed-out chunk) no copy may land after exit
         if (of_pending & (1 << b)) mbar_wait_cta(&s_oful[b], (b ? nof1 : nof0) & 1);
+    if (bf_timed_out) mbar_wait_cta(&s_bful, (nbf - 1) & 1);
     if (have_tmem) {
         cp_async_wait<0>();
         // after a timed-out wait, give the MMA one more bounded wait before
@@ -905,8 +935,23 @@ cudaError_t launch_tc(const ExpandArgs &a, dim3 grid, int cpb, cudaStream_t st, 
                   ? 1
                   : 0;
     }
-    if (a.add) return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, true>, tm_out, a, cpb, tma);
-    return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, false>, tm_out, a, cpb, tma);
+    // B blocks at full rank by TMA when R is a multiple of 64 (whole 128-byte rows)
+    BMaps tm_b;
+    memset(&tm_b, 0, sizeof(tm_b));
+    int tma_b = 0;
+    if (a.R % 64 == 0) {
+        tma_b = 1;
+        for (int s = 0; s < a.num_slices && tma_b; ++s)
+            if (a.N[s] > 0 &&
+                make_tensor_map_2d(&tm_b.m[s],
+                                   std::is_same<E, __nv_bfloat16>::value ? LORA_BF16 : LORA_F16,
+                                   a.B[s], (uint64_t)a.L * a.N[s], (uint64_t)a.R, (uint64_t)a.R,
+                                   kTcCols) != cudaSuccess)
+                tma_b = 0;
+    }
+    if (a.add)
+        return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, true>, tm_out, tm_b, a, cpb, tma, tma_b);
+    return cudaLaunchKernelEx(&cfg, expand_tc_kernel<E, false>, tm_out, tm_b, a, cpb, tma, tma_b);
 }
 
 template <typename E>
