@@ -656,6 +656,9 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
             __syncthreads_and(tma && ADD && xrow0 >= 0 &&
                               ((int)threadIdx.x >= n || (int)threadIdx.x >= kTile ||
                                s_rows[threadIdx.x] == xrow0 + (int)threadIdx.x)) != 0;
+        // full tiles of consecutive rows also store their full chunks by TMA
+        // (a box covers 64 rows: rows of other tiles must not be written)
+        const bool st_tma = tma_tile && n == kTile;
         // chunk j's out block into buffer b (every thread calls), in the
         // 128-byte swizzled layout of two 64-column boxes (out_off)
         auto load_out = [&](int b, int j) {
@@ -663,6 +666,7 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
             const int c0 = j * kTcCols;
             if (tma_tile) {
                 if (threadIdx.x == 0) {
+                    tma_store_wait_read();     // a TMA store from this buffer has read it
                     fence_proxy_async_smem();  // (the buffer's generic reads came first)
                     mbar_arrive_expect_tx(&s_oful[b], 2 * kTile * 128);
                     tma_load_2d(smem_u32(dst), &tm_out, (int)(colbase + c0), xrow0, &s_oful[b]);
@@ -852,16 +856,31 @@ expand_tc_kernel(const __grid_constant__ CUtensorMap tm_out, const __grid_consta
 #pragma unroll
                             for (int k = 0; k < 8; ++k) v[k] += o[k];
                         }
-                        st_global_v4(out + (int64_t)row * a.ldo + colbase + cj + c, pack8<E>(v));
+                        if (st_tma && nc == kTcCols)  // in place, stored by TMA below
+                            *reinterpret_cast<uint4 *>(sOc + out_off(i, c / 8)) = pack8<E>(v);
+                        else
+                            st_global_v4(out + (int64_t)row * a.ldo + colbase + cj + c, pack8<E>(v));
                     }
                 }
             }
+            const bool chunk_st = st_tma && min(kTcCols, span_cols - j * kTcCols) == kTcCols;
+            if (chunk_st) fence_proxy_async_smem();  // the results -> the TMA store
             tc_fence_before();
             __syncthreads();  // TMEM and this out buffer are free again
+            if (chunk_st && threadIdx.x == 0) {
+                tma_store_2d(&tm_out, (int)(colbase + j * kTcCols), xrow0, smem_u32(sOc));
+                tma_store_2d(&tm_out, (int)(colbase + j * kTcCols + 64), xrow0,
+                             smem_u32(sOc + kTile * 128));
+                tma_store_commit();
+            }
         }
         cp_async_wait<0>();
+        // TMA stores of this tile have read their buffers before the next
+        // tile writes them (the next tile starts with a barrier)
+        if (threadIdx.x == 0) tma_store_wait_read();
         if (timed_out) break;
     }
+    if (threadIdx.x == 0) tma_store_wait_all();
     for (int b = 0; b < 2; ++b)  // (left by a timed-out chunk) no copy may land after exit
         if (of_pending & (1 << b)) mbar_wait_cta(&s_oful[b], (b ? nof1 : nof0) & 1);
     if (bf_timed_out) mbar_wait_cta(&s_bful, (nbf - 1) & 1);
