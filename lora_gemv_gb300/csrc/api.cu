@@ -340,6 +340,7 @@ lora_status_t lora_expand_slice(lora_dtype_t dtype, const float *y, int64_t ldy,
     a.tiles = p.tiles;
     a.tile_rows = p.tile_rows;
     a.max_tiles = (int)lay.max_tiles;
+    a.seg_plan = is_seg_plan(plan) ? 1 : 0;
     cudaError_t e = lora::launch_expand(dtype, a, *dev, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? LORA_OK : cuda_fail(e, "expand launch");
 }
@@ -418,6 +419,7 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
     ea.tiles = p.tiles;
     ea.tile_rows = p.tile_rows;
     ea.max_tiles = (int)lay.max_tiles;
+    ea.seg_plan = is_seg_plan(plan) ? 1 : 0;
     // The shrink waits for the caller's previous kernels, then lets the
     // expand launch early; the expand reads plan, out and B (none written by
     // the shrink) before its own wait and y after it.

@@ -1081,8 +1081,10 @@ cudaError_t launch_expand(lora_dtype_t dt, const ExpandArgs &a_in, const DeviceI
     // prefill gate/up: r = 64 363 -> 155 us, r = 32 150 -> 135 us; at r = 16
     // and for decode batches the warp kernel is faster (its units are lighter
     // than a CTA's load/convert/MMA chain).
+    // For plans grouped from segments (tiles of consecutive rows: out blocks
+    // loaded and stored by TMA) also at r <= 16 when the batch is large.
     const int ksr = (a.R + 15) / 16;
-    if (vec && y_vec && ksr >= 2) {
+    if (vec && y_vec && (ksr >= 2 || a.seg_plan)) {
         // spans of cpb 128-column chunks per slice: cpb is the largest power of
         // two that still leaves at least kTcWaves waves of CTAs
         const int dyn = tc_expand_smem(a.R);

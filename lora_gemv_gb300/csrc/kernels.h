@@ -56,6 +56,7 @@ struct ExpandArgs {
     const int4 *tiles;
     const int32_t *tile_rows;
     int max_tiles;
+    int seg_plan;  // the plan was grouped from a segment table (a launch-shape hint only)
 };
 
 // Plan-free BGMV (tokens in their natural order; every token's adapter read
