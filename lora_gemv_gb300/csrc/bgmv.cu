@@ -684,9 +684,11 @@ bgmv_expand_dense_kernel(const BgmvExpandArgs a, int nchunks) {
     // y rows come from the previous kernel (the shrink)
     grid_dep_wait();
     grid_dep_launch();
-    for (int q = tid; q < kDRows * (RK / 4); q += kFThreads) {
-        const int rr = q / (RK / 4), k4 = q - rr * (RK / 4);
-        const int t = t0 + rr;
+    // each warp stages the y rows it computes (rows warp, warp + 8, ...): no
+    // block-wide barrier
+    for (int q = lane; q < (kDRows / 8) * (RK / 4); q += 32) {
+        const int i = q / (RK / 4), k4 = q - i * (RK / 4);
+        const int rr = i * 8 + warp, t = t0 + rr;
         const bool in = t < a.T && 4 * k4 < rl;  // ranks past r_0 read as zeros
         const float *src =
             in ? a.y + (int64_t)t * a.ldy + (int64_t)s * a.y_slice_stride + 4 * k4 : a.y;
@@ -694,7 +696,7 @@ bgmv_expand_dense_kernel(const BgmvExpandArgs a, int nchunks) {
     }
     cp_async_commit();
     cp_async_wait<0>();
-    __syncthreads();
+    __syncwarp();
     if (!ok || (ADD && rl == 0)) return;  // (rank 0 with add_inputs: out stays as it is)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {

@@ -250,6 +250,26 @@ def test_sorted_segments_rank_aware(cuda_lib, R, ranks, Ns, dtype, add):
     full_check(cuda_lib, c)
 
 
+@pytest.mark.parametrize("T,R,Ns,lens", [
+    (256, 64, [200, 72], [128, 128]),              # full tiles, ragged last chunks
+    (320, 128, [384, 136], [64, 192, 64]),         # R = 128: two TMA B boxes per chunk
+    (2048, 16, [2048, 200], [700, 600, 748]),      # rank 16 on the tensor-core expand
+    (131, 64, [256], [131]),                       # a partial tile ending at T
+])
+@pytest.mark.parametrize("add", [True, False])
+def test_sorted_segments_tma_expand(cuda_lib, T, R, Ns, lens, add):
+    """Tiles of consecutive rows through the tensor-core expand: out blocks
+    loaded (and, for full tiles and full chunks, stored) by TMA, B by TMA at
+    full rank; ragged chunks and partial tiles keep plain stores."""
+    L = len(lens)
+    c = make_case(T, 256, R, L, Ns, torch.bfloat16, seed=T + R + add, add=add)
+    c.token_idx = None
+    c.seg_start = torch.tensor(np.cumsum([0] + lens[:-1]), dtype=torch.int32)
+    c.seg_len = torch.tensor(lens, dtype=torch.int32)
+    c.seg_lora = torch.arange(L, dtype=torch.int32)
+    full_check(cuda_lib, c)
+
+
 # ---------------------------------------------------------------- edge cases
 
 def make_case(T, H, R, L, N_list, dtype, seed, *, S=None, p_neg=0.2, add=True, scale=0.7,
