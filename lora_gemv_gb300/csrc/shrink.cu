@@ -197,8 +197,9 @@ __device__ __forceinline__ void store_stage(const uint4 (&ld)[kMaxLd], unsigned 
 }
 
 // KS: warps of one row block split its k steps (else its n-tiles).  No
-// minimum-occupancy bound: capping registers for more resident CTAs measured
-// slower (the CTAs per SM are limited by shared memory anyway).
+// minimum-occupancy bound except for the TMA variant (shrink_tma_kernel):
+// capping registers for more resident CTAs measured slower elsewhere (the
+// CTAs per SM are limited by shared memory anyway).
 // push: reduce over the cluster through the receive buffers (ksplit > 1).
 // TC: the contraction on the tcgen05 tensor cores (aligned rows; D = X . A^T
 // with M = 128 token lanes, N = rows_cap, accumulated in TMEM), else mma.sync.
@@ -245,14 +246,60 @@ __device__ __noinline__ void shrink_tma_stage(const CUtensorMap *tm_x, const CUt
     }
 }
 
+// Pull form of the split-K reduction: the CTA sums the partials of its nr
+// owned rows (s_rows: their token rows) over the cluster's ksplit CTAs in
+// rank order, four columns at a time with four ranks' loads in flight, and
+// writes scale * sum to y (or adds it).  Columns past nrows are read from the
+// row pitch's slack and never stored.  Not inlined: its registers would
+// otherwise count for the whole kernel.
+__device__ __noinline__ void pull_reduce(const float *Ct, int PP, int r0, int nr, int nrows,
+                                         int ksplit, const int *s_rows, const int *s_arow,
+                                         float *y, int64_t ldy, float scale, int add) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int nc4 = (nrows + 3) >> 2;
+    for (int it = threadIdx.x; it < nr * nc4; it += kThreads) {
+        const int ii = it / nc4, c4 = it - ii * nc4;
+        const int off = (r0 + ii) * PP + 4 * c4;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int rb = 0; rb < ksplit; rb += 4) {
+            float4 p[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (rb + j < ksplit) {
+                    const float *src = ksplit > 1 ? cluster.map_shared_rank(Ct, rb + j) : Ct;
+                    p[j] = *reinterpret_cast<const float4 *>(src + off);
+                }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (rb + j < ksplit) {
+                    s.x += p[j].x;
+                    s.y += p[j].y;
+                    s.z += p[j].z;
+                    s.w += p[j].w;
+                }
+        }
+        const int row = s_rows[ii];
+        if (row < 0) continue;
+        const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = 4 * c4 + j;
+            if (c < nrows && s_arow[c] >= 0) {
+                float *yp = y + (int64_t)row * ldy + s_arow[c];
+                const float v = scale * sv[j];
+                *yp = add ? *yp + v : v;
+            }
+        }
+    }
+}
+
 // TMA (TC only): the TMA-capable variant, launched for plans grouped from a
 // segment table; without it the TMA code is compiled out and the variant
 // keeps the registers (and so the residency) of the cp.async-only kernel.
 template <typename E, bool VEC, int NTMAX, bool KS, bool TC, bool TMA>
-__global__ void __launch_bounds__(kThreads)
-shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a,
-              const __grid_constant__ ABoxMaps tm_ab, const ShrinkArgs a, int kchunk,
-              int rows_cap, int push, int tma) {
+__device__ __forceinline__ void shrink_body(const CUtensorMap &tm_x, const CUtensorMap &tm_a,
+                                            const ABoxMaps &tm_ab, const ShrinkArgs &a,
+                                            int kchunk, int rows_cap, int push, int tma) {
     static_assert(!TC || (VEC && !KS), "the tensor-core path takes aligned rows, no warp split");
     extern __shared__ __align__(16) unsigned char smem[];
     __shared__ int s_rows[kTile];
@@ -643,8 +690,12 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
         if (ksplit > 1) cluster.sync();
         else __syncthreads();
 
-        // fixed-order reduction over the cluster; CTA kc finishes a 1/ksplit share
-        {
+        // fixed-order reduction over the cluster
+        if constexpr (TC) {  // CTA kc sums the rows it owns
+            const int r0 = kc * rpo;
+            pull_reduce(Ct, PP, r0, max(0, min(n - r0, rpo)), nrows, ksplit, s_rows + r0, s_arow,
+                        a.y, a.ldy, a.scale, a.add);
+        } else {  // CTA kc finishes a 1/ksplit share of the elements
             const int E_ = n * nrows;
             const int e0 = (int)((long long)E_ * kc / ksplit), e1 = (int)((long long)E_ * (kc + 1) / ksplit);
             for (int it = e0 + threadIdx.x; it < e1; it += kThreads) {
@@ -681,6 +732,25 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     }
 }
 
+template <typename E, bool VEC, int NTMAX, bool KS, bool TC>
+__global__ void __launch_bounds__(kThreads)
+shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a,
+              const __grid_constant__ ABoxMaps tm_ab, const ShrinkArgs a, int kchunk,
+              int rows_cap, int push, int tma) {
+    shrink_body<E, VEC, NTMAX, KS, TC, false>(tm_x, tm_a, tm_ab, a, kchunk, rows_cap, push, tma);
+}
+
+// The TMA-staging variant, held to 64 registers: 4 CTAs per SM where shared
+// memory allows, so the small-rank prefill shapes split K over clusters of 8
+// in one wave (its partials then summed by the pull reduction).
+template <typename E, int NTMAX>
+__global__ void __launch_bounds__(kThreads, 4)
+shrink_tma_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a,
+                  const __grid_constant__ ABoxMaps tm_ab, const ShrinkArgs a, int kchunk,
+                  int rows_cap, int push, int tma) {
+    shrink_body<E, true, NTMAX, false, true, true>(tm_x, tm_a, tm_ab, a, kchunk, rows_cap, push, tma);
+}
+
 using ShrinkFn = void (*)(const CUtensorMap, const CUtensorMap, const ABoxMaps, const ShrinkArgs,
                           int, int, int, int);
 
@@ -691,11 +761,20 @@ enum Variant { kNSplit = 0, kKSplit = 1, kTensor = 2, kTensorTma = 3, kVariants 
 // Instantiation for n-tile class c (NTMAX = 2 << c).
 template <typename E, bool VEC, bool KS, bool TC, bool TMA = false>
 ShrinkFn kernel_nt(int c) {
-    switch (c) {
-        case 0: return shrink_kernel<E, VEC, 2, KS, TC, TMA>;
-        case 1: return shrink_kernel<E, VEC, 4, KS, TC, TMA>;
-        case 2: return shrink_kernel<E, VEC, 8, KS, TC, TMA>;
-        default: return shrink_kernel<E, VEC, 16, KS, TC, TMA>;
+    if constexpr (TMA) {
+        switch (c) {
+            case 0: return shrink_tma_kernel<E, 2>;
+            case 1: return shrink_tma_kernel<E, 4>;
+            case 2: return shrink_tma_kernel<E, 8>;
+            default: return shrink_tma_kernel<E, 16>;
+        }
+    } else {
+        switch (c) {
+            case 0: return shrink_kernel<E, VEC, 2, KS, TC>;
+            case 1: return shrink_kernel<E, VEC, 4, KS, TC>;
+            case 2: return shrink_kernel<E, VEC, 8, KS, TC>;
+            default: return shrink_kernel<E, VEC, 16, KS, TC>;
+        }
     }
 }
 
