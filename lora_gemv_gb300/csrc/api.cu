@@ -420,6 +420,7 @@ lora_status_t lora_shrink_expand_slice(lora_dtype_t dtype, const void *x, int64_
     ea.tile_rows = p.tile_rows;
     ea.max_tiles = (int)lay.max_tiles;
     ea.seg_plan = is_seg_plan(plan) ? 1 : 0;
+    ea.early = 1;
     // The shrink waits for the caller's previous kernels, then lets the
     // expand launch early; the expand reads plan, out and B (none written by
     // the shrink) before its own wait and y after it.

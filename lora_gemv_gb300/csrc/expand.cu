@@ -298,6 +298,7 @@ expand_kernel(const ExpandArgs a) {
 // measured far lower).
 constexpr int kWThreads = 128;  // 4 independent warps per CTA
 constexpr int kWCols = 32;      // output columns per warp unit
+constexpr int kWPrefetch = 8;   // units of a warp whose out rows are prefetched into L2
 // Token rows per warp unit: MB m16 blocks, MB = 2 for ranks <= 32 and 1 above
 // (the y fragments of a unit live in registers).
 __host__ __device__ constexpr int warp_mb(int ksmax) { return ksmax >= 4 ? 1 : 2; }
@@ -413,6 +414,26 @@ expand_warp_kernel(const ExpandArgs a, int tiles_grid, int ncb, int y_vec) {
     bool col_ok = c0 + 8 * q < a.N[s];
     UnitLoads<MB, KSMAX> cur, nxt;
     if (nrow > 0 && rl > 0) issue_unit<E, ADD, MB, KSMAX>(a, cur, rows, tl.x, rl, KS, s, c0, col, col_ok, g, q);
+    // The warp's later units of the same (tile, row part): their old out
+    // values into L2 now (the loads one unit ahead then hit L2).  Chained
+    // after the shrink this runs before the wait, so from the second unit on;
+    // otherwise the second unit's loads follow at once, so from the third.
+    if (ADD && nrow > 0 && rl > 0) {
+        const int skip = a.early ? 1 : 2;
+        int pc = cbi + skip;
+        for (long long pu = u_begin + skip; pu < u_end && pc < ncb && pu < u_begin + kWPrefetch;
+             ++pu, ++pc) {
+            int ps, pc0;
+            slice_of(pc, ps, pc0);
+            if (pc0 + 8 * q >= a.N[ps]) continue;
+            const int64_t pcol = (int64_t)a.off[ps] + pc0 + 8 * q;
+#pragma unroll
+            for (int mm = 0; mm < MB; ++mm)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    if (rows[mm][h] >= 0) prefetch_l2(out + (int64_t)rows[mm][h] * a.ldo + pcol);
+        }
+    }
 
     int y_s = -1;  // slice whose y fragments are held (same tile and part)
     float fscale[MB][2];

@@ -57,6 +57,7 @@ struct ExpandArgs {
     const int32_t *tile_rows;
     int max_tiles;
     int seg_plan;  // the plan was grouped from a segment table (a launch-shape hint only)
+    int early;     // launched as the programmatic dependent of the shrink that writes y
 };
 
 // Plan-free BGMV (tokens in their natural order; every token's adapter read
