@@ -308,6 +308,7 @@ __device__ __forceinline__ void shrink_body(const CUtensorMap &tm_x, const CUten
     __shared__ uint64_t s_mma[2];  // TC: the MMAs reading stage buffer b are done
     __shared__ uint64_t s_full[2]; // TC with TMA: stage buffer b's copies have landed
     __shared__ uint32_t s_tmem;    // TC: TMEM base address
+    __shared__ int s_rank[kThreads];  // ranks table (when given), adapters < kThreads
     constexpr int PP = part_pitch(NTMAX);
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -332,6 +333,9 @@ __device__ __forceinline__ void shrink_body(const CUtensorMap &tm_x, const CUten
     int row_next = threadIdx.x < kTile && (int)blockIdx.y < a.max_tiles
                        ? __ldcg(a.tile_rows + (int64_t)blockIdx.y * kTile + threadIdx.x)
                        : -1;
+    // ... and the ranks of adapters 0 .. kThreads-1, so a tile's rank costs
+    // no round trip of its own (visible after the tile loop's first barrier)
+    if (a.ranks != nullptr && (int)threadIdx.x < a.L) s_rank[threadIdx.x] = clamp_rank(a.ranks, threadIdx.x, a.R);
     if (h0.x != LORA_PLAN_MAGIC || h0.y != a.T || h0.z != a.L) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
             atomicOr(a.hdr + LORA_HDR_ERR, LORA_PLANERR_MISMATCH);
@@ -391,10 +395,12 @@ __device__ __forceinline__ void shrink_body(const CUtensorMap &tm_x, const CUten
                 row_next = __ldcg(a.tile_rows + (int64_t)(tile + gridDim.y) * kTile + threadIdx.x);
         }
         const int l = tl.x, n = tl.z;
-        const int rl = l >= 0 && l < a.L ? clamp_rank(a.ranks, l, R) : 0;
 
         if (threadIdx.x < kTile) s_rows[threadIdx.x] = my_row;
         __syncthreads();
+        const int rl = l < 0 || l >= a.L ? 0
+                       : a.ranks == nullptr ? R
+                       : l < kThreads ? s_rank[l] : clamp_rank(a.ranks, l, R);
         // y columns that get no term: every column of inactive tokens, the
         // columns i >= r_l of each slice otherwise.  The cluster's CTAs share
         // the tile's rows (row i by CTA i mod ksplit).
