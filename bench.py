@@ -570,9 +570,9 @@ def make_pool(dev, rank: int, l2_bytes: int, only_T=None):
 # from an ncu capture of `bench.py --profile --T 1024` (summaries under
 # profiles/); None until a capture of the current kernel exists.
 NCU_TRAFFIC = {
-    "shrink": {"bytes": 9177088, "source": "ncu --set full, dram__bytes_read.sum 9.177 MB + "
-               "dram__bytes_write.sum 0 (y stays in L2), T=1024 launch of the current "
-               "tcgen05 variant without TMA staging (64 registers)"},
+    "shrink": {"bytes": 9177856, "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum: "
+               "9.178 MB read + 0 written (y stays in L2), T=1024 launch of the current "
+               "tcgen05 variant without TMA staging"},
 }
 
 
