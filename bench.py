@@ -1097,6 +1097,25 @@ def main_profile(args):
         print(json.dumps({"profile": True, "workload": "prefill_gateup", "r": r, "T": c.T,
                           "reps": args.profile_reps}))
         return
+    if args.sweep_point:
+        # one point of the hidden-size x batch sweep: grouping, shrink, expand
+        Hs, bs, sls = (int(v) for v in args.sweep_point.split(","))
+        c = li.sweep(Hs, bs, sls)
+        x, A, B, out = c.x.to(dev), c.A.to(dev), c.B[0].to(dev), c.out.to(dev)
+        y = torch.empty(c.T, c.R, dtype=torch.float32, device=dev)
+        plan = lg.new_plan(c.T, c.L, dev)
+        for _ in range(args.profile_reps):
+            if sls == 1:
+                lg.lora_group_tokens(c.token_idx.to(dev), c.L, plan)
+            else:
+                lg.lora_group_segments(c.seg_start.to(dev), c.seg_len.to(dev), c.seg_lora.to(dev),
+                                       c.T, c.L, plan)
+            lg.lora_shrink(x, A, y, plan)
+            lg.lora_expand(y, B, out, plan, add_inputs=True)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": True, "workload": "sweep", "H": Hs, "batch": bs,
+                          "seq_len": sls, "T": c.T, "reps": args.profile_reps}))
+        return
     if args.path == "single":
         # one adapter, no token index (the mask-free dense expand), at T rows
         g = torch.Generator().manual_seed(li.SEED_BASE + 77)
@@ -1142,6 +1161,8 @@ def main():
     ap.add_argument("--path", choices=["grouped", "bgmv", "fused", "single"], default=STEP_PATH,
                     help="with --profile: the decode pair's path (single: the one-adapter "
                          "expand at T x 2048, r = 16)")
+    ap.add_argument("--sweep-point", default="",
+                    help="with --profile: one sweep point 'H,batch,seq_len' (grouped path)")
     ap.add_argument("--prefill-r", type=int, default=0,
                     help="with --profile: the prefill gate/up workload at this rank instead")
     args = ap.parse_args()

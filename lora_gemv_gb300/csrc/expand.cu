@@ -127,15 +127,32 @@ expand_kernel(const ExpandArgs a) {
         const bool wact = warp * 32 < ncols;
         const int nmb = (n + 15) / 16;
 
-        // 1) issue the reads of out early (they overlap the staging below)
+        // 1) issue the reads of out early (they overlap the staging below);
+        //    unaligned rows element by element, all loads independent
         uint4 old[4][2];
-        if (ADD && VEC && wact && wcol < ncols) {
+        if (ADD && wact && wcol < ncols) {
 #pragma unroll
             for (int mb = 0; mb < 4; ++mb) {
                 if (mb < nmb) {
-                    const int r0 = s_rows[mb * 16 + g], r1 = s_rows[mb * 16 + g + 8];
-                    if (r0 >= 0) old[mb][0] = ld_global_v4(out + (int64_t)r0 * a.ldo + col0 + wcol);
-                    if (r1 >= 0) old[mb][1] = ld_global_v4(out + (int64_t)r1 * a.ldo + col0 + wcol);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int r = s_rows[mb * 16 + g + 8 * h];
+                        if (r < 0) continue;
+                        const E *src = out + (int64_t)r * a.ldo + col0 + wcol;
+                        if (VEC) {
+                            old[mb][h] = ld_global_v4(src);
+                        } else {
+                            const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src);
+                            uint32_t w[4];
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint32_t lo16 = wcol + 2 * k < ncols ? s16[2 * k] : 0u;
+                                const uint32_t hi16 = wcol + 2 * k + 1 < ncols ? s16[2 * k + 1] : 0u;
+                                w[k] = lo16 | (hi16 << 16);
+                            }
+                            old[mb][h] = make_uint4(w[0], w[1], w[2], w[3]);
+                        }
+                    }
                 }
             }
         }
@@ -260,11 +277,13 @@ expand_kernel(const ExpandArgs a) {
                             st_global_v4(p, pack8<E>(res));
                         }
                     } else {
+                        float o[8];
+                        if (ADD) unpack8<E>(old[mb][h], o);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {
                             if (wcol + k < ncols) {
                                 float r = res[k];
-                                if (ADD) r += Elem<E>::to_f(p[k]);
+                                if (ADD) r += o[k];
                                 p[k] = Elem<E>::from_f(r);
                             }
                         }

@@ -746,6 +746,18 @@ shrink_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ 
     shrink_body<E, VEC, NTMAX, KS, TC, false>(tm_x, tm_a, tm_ab, a, kchunk, rows_cap, push, tma);
 }
 
+// Rows that are not 16-byte aligned (odd H or strides): register staging with
+// 2-byte loads, held to 128 registers so that 2 CTAs fit per SM and the K
+// split can spread the launch (unbounded it took 242 registers: one CTA per
+// SM and no K split).
+template <typename E, int NTMAX, bool KS>
+__global__ void __launch_bounds__(kThreads, 2)
+shrink_unaligned_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_a,
+                        const __grid_constant__ ABoxMaps tm_ab, const ShrinkArgs a, int kchunk,
+                        int rows_cap, int push, int tma) {
+    shrink_body<E, false, NTMAX, KS, false, false>(tm_x, tm_a, tm_ab, a, kchunk, rows_cap, push, tma);
+}
+
 // The TMA-staging variant, held to 64 registers: 4 CTAs per SM where shared
 // memory allows, so the small-rank prefill shapes split K over clusters of 8
 // in one wave (its partials then summed by the pull reduction).
@@ -773,6 +785,13 @@ ShrinkFn kernel_nt(int c) {
             case 1: return shrink_tma_kernel<E, 4>;
             case 2: return shrink_tma_kernel<E, 8>;
             default: return shrink_tma_kernel<E, 16>;
+        }
+    } else if constexpr (!VEC) {
+        switch (c) {
+            case 0: return shrink_unaligned_kernel<E, 2, KS>;
+            case 1: return shrink_unaligned_kernel<E, 4, KS>;
+            case 2: return shrink_unaligned_kernel<E, 8, KS>;
+            default: return shrink_unaligned_kernel<E, 16, KS>;
         }
     } else {
         switch (c) {
