@@ -93,6 +93,74 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Streaming 16-byte global accesses for the read-modify-write of out.
+// Eight consecutive 2-byte elements at p, which is only 2-byte aligned (rows
+// of an odd-width matrix): the first nv of them (the rest read as zero), with
+// the widest loads p's alignment allows (one 16-byte, two 8-byte, four
+// 4-byte, or 2 + 4 + 4 + 4 + 2 bytes).  Never reads outside the nv elements.
+// NC: the data is read-only for the kernel's lifetime (non-coherent path).
+template <bool NC>
+__device__ __forceinline__ uint4 ld8_u16(const uint16_t *p, int nv) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    if (nv >= 8) {
+        if ((a & 15) == 0) return NC ? __ldg(reinterpret_cast<const uint4 *>(p)) : *reinterpret_cast<const uint4 *>(p);
+        if ((a & 7) == 0) {
+            const uint2 lo = NC ? __ldg(reinterpret_cast<const uint2 *>(p)) : *reinterpret_cast<const uint2 *>(p);
+            const uint2 hi = NC ? __ldg(reinterpret_cast<const uint2 *>(p + 4)) : *reinterpret_cast<const uint2 *>(p + 4);
+            return make_uint4(lo.x, lo.y, hi.x, hi.y);
+        }
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(p + ((a & 3) ? 1 : 0));
+        if ((a & 3) == 0) {
+            return make_uint4(NC ? __ldg(w) : w[0], NC ? __ldg(w + 1) : w[1], NC ? __ldg(w + 2) : w[2],
+                              NC ? __ldg(w + 3) : w[3]);
+        }
+        // elements 0 and 7 alone, pairs (1,2), (3,4), (5,6) as aligned words
+        const uint32_t e0 = NC ? __ldg(p) : p[0], e7 = NC ? __ldg(p + 7) : p[7];
+        const uint32_t w1 = NC ? __ldg(w) : w[0], w2 = NC ? __ldg(w + 1) : w[1], w3 = NC ? __ldg(w + 2) : w[2];
+        return make_uint4(e0 | (w1 << 16), (w1 >> 16) | (w2 << 16), (w2 >> 16) | (w3 << 16),
+                          (w3 >> 16) | (e7 << 16));
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t lo = 2 * k < nv ? (NC ? __ldg(p + 2 * k) : p[2 * k]) : 0u;
+        const uint32_t hi = 2 * k + 1 < nv ? (NC ? __ldg(p + 2 * k + 1) : p[2 * k + 1]) : 0u;
+        w[k] = lo | (hi << 16);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The first nv of eight 2-byte elements (packed in v) to p, which is only
+// 2-byte aligned, with the widest stores p's alignment allows.
+__device__ __forceinline__ void st8_u16(uint16_t *p, uint4 v, int nv) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    if (nv >= 8) {
+        if ((a & 15) == 0) {
+            *reinterpret_cast<uint4 *>(p) = v;
+        } else if ((a & 7) == 0) {
+            reinterpret_cast<uint2 *>(p)[0] = make_uint2(v.x, v.y);
+            reinterpret_cast<uint2 *>(p)[1] = make_uint2(v.z, v.w);
+        } else if ((a & 3) == 0) {
+            uint32_t *w = reinterpret_cast<uint32_t *>(p);
+            w[0] = v.x;
+            w[1] = v.y;
+            w[2] = v.z;
+            w[3] = v.w;
+        } else {
+            uint32_t *w = reinterpret_cast<uint32_t *>(p + 1);
+            p[0] = (uint16_t)(v.x & 0xffffu);
+            w[0] = (v.x >> 16) | (v.y << 16);
+            w[1] = (v.y >> 16) | (v.z << 16);
+            w[2] = (v.z >> 16) | (v.w << 16);
+            p[7] = (uint16_t)(v.w >> 16);
+        }
+        return;
+    }
+    const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        if (k < nv) p[k] = (uint16_t)((e[k >> 1] >> (16 * (k & 1))) & 0xffffu);
+}
+
 __device__ __forceinline__ uint4 ld_global_v4(const void *p) {
     uint4 v;
     asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"

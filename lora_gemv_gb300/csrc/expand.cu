@@ -108,13 +108,8 @@ expand_kernel(const ExpandArgs a) {
                     const int row = s_rows[i];
                     if (row < 0 || c8 >= ncols) continue;
                     E *p = out + (int64_t)row * a.ldo + col0 + c8;
-                    if (VEC) {
-                        st_global_v4(p, make_uint4(0, 0, 0, 0));
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            if (c8 + k < ncols) p[k] = Elem<E>::from_f(0.f);
-                    }
+                    if (VEC) st_global_v4(p, make_uint4(0, 0, 0, 0));
+                    else st8_u16(reinterpret_cast<uint16_t *>(p), make_uint4(0, 0, 0, 0), ncols - c8);
                 }
             }
             __syncthreads();
@@ -139,19 +134,8 @@ expand_kernel(const ExpandArgs a) {
                         const int r = s_rows[mb * 16 + g + 8 * h];
                         if (r < 0) continue;
                         const E *src = out + (int64_t)r * a.ldo + col0 + wcol;
-                        if (VEC) {
-                            old[mb][h] = ld_global_v4(src);
-                        } else {
-                            const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src);
-                            uint32_t w[4];
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const uint32_t lo16 = wcol + 2 * k < ncols ? s16[2 * k] : 0u;
-                                const uint32_t hi16 = wcol + 2 * k + 1 < ncols ? s16[2 * k + 1] : 0u;
-                                w[k] = lo16 | (hi16 << 16);
-                            }
-                            old[mb][h] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
+                        if (VEC) old[mb][h] = ld_global_v4(src);
+                        else old[mb][h] = ld8_u16<false>(reinterpret_cast<const uint16_t *>(src), ncols - wcol);
                     }
                 }
             }
@@ -174,15 +158,7 @@ expand_kernel(const ExpandArgs a) {
                             w[k] &= (2 * k + 1 < nv) ? 0xffffffffu : (2 * k < nv ? 0xffffu : 0u);
                     }
                 } else {
-                    const uint16_t *s16 = reinterpret_cast<const uint16_t *>(src);
-                    uint32_t w[4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t lo16 = 2 * k < nv ? __ldg(s16 + 2 * k) : 0u;
-                        const uint32_t hi16 = 2 * k + 1 < nv ? __ldg(s16 + 2 * k + 1) : 0u;
-                        w[k] = lo16 | (hi16 << 16);
-                    }
-                    v = make_uint4(w[0], w[1], w[2], w[3]);
+                    v = ld8_u16<true>(reinterpret_cast<const uint16_t *>(src), nv);
                 }
             }
             *reinterpret_cast<uint4 *>(sB + sigma(j) * pitch + c8) = v;
@@ -276,17 +252,14 @@ expand_kernel(const ExpandArgs a) {
                             }
                             st_global_v4(p, pack8<E>(res));
                         }
-                    } else {
-                        float o[8];
-                        if (ADD) unpack8<E>(old[mb][h], o);
+                    } else if (wcol < ncols) {
+                        if (ADD) {
+                            float o[8];
+                            unpack8<E>(old[mb][h], o);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            if (wcol + k < ncols) {
-                                float r = res[k];
-                                if (ADD) r += o[k];
-                                p[k] = Elem<E>::from_f(r);
-                            }
+                            for (int k = 0; k < 8; ++k) res[k] += o[k];
                         }
+                        st8_u16(reinterpret_cast<uint16_t *>(p), pack8<E>(res), ncols - wcol);
                     }
                 }
             }

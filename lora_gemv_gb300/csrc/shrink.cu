@@ -91,15 +91,9 @@ constexpr int kMaxLd = (kTile + kRows) * kCh / kThreads;
 template <typename E, bool VEC>
 __device__ __forceinline__ uint4 load_chunk(const E *row_ptr, int h, int h_end) {
     if (VEC) return h < h_end ? __ldg(reinterpret_cast<const uint4 *>(row_ptr + h)) : make_uint4(0, 0, 0, 0);
-    uint32_t w[4];
-    const uint16_t *src = reinterpret_cast<const uint16_t *>(row_ptr);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t lo = h + 2 * k < h_end ? __ldg(src + h + 2 * k) : 0u;
-        const uint32_t hi = h + 2 * k + 1 < h_end ? __ldg(src + h + 2 * k + 1) : 0u;
-        w[k] = lo | (hi << 16);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    // rows only 2-byte aligned: the widest loads each chunk's alignment allows
+    return h < h_end ? ld8_u16<true>(reinterpret_cast<const uint16_t *>(row_ptr) + h, h_end - h)
+                     : make_uint4(0, 0, 0, 0);
 }
 
 // Stage loads: chunk it < 64*16 -> x row it/16, else A row (it - 1024)/16.
